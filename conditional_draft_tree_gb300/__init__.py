@@ -1,0 +1,262 @@
+"""Python binding of ``libdt.so``, the GB300 conditional draft-tree builder.
+
+Argument marshalling only: every step of a round runs in the library's CUDA
+kernels. PyTorch provides device memory and streams. The functions mirror the
+C ABI of ``include/dt.h`` (same names without the ``dt_`` prefix) and take
+torch tensors where the C ABI takes pointers. When ``libdt.so`` is missing,
+every call raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdt.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, -1, -2, -3
+ERR_NONFINITE, ERR_TIMEOUT, ERR_BAD_TEMPERATURE = -4, -5, -6
+F32, BF16 = 0, 1
+NUM_PHASE_EVENTS = 4
+MAX_SPEC = 16
+
+# every symbol include/dt.h declares
+EXPORTS = ("dt_abi_version", "dt_status_string", "dt_prepared_bytes", "dt_prepare_weights",
+           "dt_workspace_bytes", "dt_build_trees", "dt_host_workspace_bytes",
+           "dt_build_trees_host")
+
+
+class DtDims(C.Structure):
+    _fields_ = [(n, C.c_int) for n in ("V", "d", "d_s", "r", "D", "M", "k", "N", "batch")]
+
+
+class DtWeights(C.Structure):
+    _fields_ = [("E", C.c_void_p), ("W_ih", C.c_void_p), ("W_hh", C.c_void_p),
+                ("b_ih", C.c_void_p), ("b_hh", C.c_void_p), ("W1", C.c_void_p),
+                ("W2", C.c_void_p), ("wdtype", C.c_int)]
+
+
+class DtTreeOut(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("tokens", "parents", "depths", "scores", "mask",
+                                           "topm", "status")]
+
+
+class DtOptions(C.Structure):
+    _fields_ = [("spec_width", C.c_int), ("phase_events", C.POINTER(C.c_void_p))]
+
+
+class DtError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def lib():
+    """Load libdt.so (built by ``build.build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise DtError(f"{LIB_PATH} is not built; run conditional_draft_tree_gb300.build.build()")
+        L = C.CDLL(LIB_PATH)
+        L.dt_abi_version.restype = C.c_int
+        L.dt_status_string.restype = C.c_char_p
+        L.dt_status_string.argtypes = [C.c_int]
+        L.dt_prepared_bytes.restype = C.c_size_t
+        L.dt_prepared_bytes.argtypes = [C.POINTER(DtDims)]
+        L.dt_prepare_weights.argtypes = [C.POINTER(DtDims), C.POINTER(DtWeights), C.c_void_p,
+                                         C.c_size_t, C.c_void_p]
+        L.dt_workspace_bytes.restype = C.c_size_t
+        L.dt_workspace_bytes.argtypes = [C.POINTER(DtDims), C.POINTER(DtOptions)]
+        L.dt_host_workspace_bytes.restype = C.c_size_t
+        L.dt_host_workspace_bytes.argtypes = [C.POINTER(DtDims), C.POINTER(DtOptions)]
+        sig = [C.POINTER(DtDims), C.POINTER(DtWeights), C.c_void_p, C.c_void_p, C.c_void_p,
+               C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
+               C.POINTER(DtTreeOut), C.POINTER(DtOptions), C.c_void_p]
+        L.dt_build_trees.argtypes = sig
+        L.dt_build_trees_host.argtypes = sig
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().dt_status_string(int(code)).decode()
+
+
+def abi_version() -> int:
+    return lib().dt_abi_version()
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise DtError(f"{what}: {status_string(rc)} ({rc})")
+
+
+def dims_of(V, d, d_s, r, D, M, k, N, batch) -> DtDims:
+    return DtDims(V, d, d_s, r, D, M, k, N, batch)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def options(spec_width: int = 0, events=None) -> DtOptions:
+    """Build a dt_options; ``events``: DT_NUM_PHASE_EVENTS torch.cuda.Event or None."""
+    o = DtOptions(spec_width, None)
+    if events is not None:
+        arr = (C.c_void_p * NUM_PHASE_EVENTS)(*[e.cuda_event for e in events])
+        o.phase_events = C.cast(arr, C.POINTER(C.c_void_p))
+        o._keep = arr
+    return o
+
+
+@dataclass
+class DeviceWeights:
+    """Domino head weights on the device (see dt_weights in include/dt.h)."""
+    E: torch.Tensor
+    W_ih: torch.Tensor
+    W_hh: torch.Tensor
+    W1: torch.Tensor
+    W2: torch.Tensor
+    b_ih: torch.Tensor | None = None
+    b_hh: torch.Tensor | None = None
+
+    @property
+    def wdtype(self) -> int:
+        return BF16 if self.E.dtype in (torch.int16, torch.uint16, torch.bfloat16) else F32
+
+    def struct(self) -> DtWeights:
+        return DtWeights(_ptr(self.E), _ptr(self.W_ih), _ptr(self.W_hh), _ptr(self.b_ih),
+                         _ptr(self.b_hh), _ptr(self.W1), _ptr(self.W2), self.wdtype)
+
+
+def prepared_bytes(dims: DtDims) -> int:
+    return lib().dt_prepared_bytes(C.byref(dims))
+
+
+def prepare_weights(dims: DtDims, w: DeviceWeights, prepared: torch.Tensor, stream=None):
+    ws = w.struct()
+    _check(lib().dt_prepare_weights(C.byref(dims), C.byref(ws), prepared.data_ptr(),
+                                    prepared.numel() * prepared.element_size(), _stream(stream)),
+           "dt_prepare_weights")
+
+
+def workspace_bytes(dims: DtDims, opt: DtOptions | None = None) -> int:
+    return lib().dt_workspace_bytes(C.byref(dims), C.byref(opt) if opt else None)
+
+
+def host_workspace_bytes(dims: DtDims, opt: DtOptions | None = None) -> int:
+    return lib().dt_host_workspace_bytes(C.byref(dims), C.byref(opt) if opt else None)
+
+
+def alloc_outputs(dims: DtDims, device, mask=True, topm=True, pin=False):
+    """Output tensors of dt_tree_out (device, or pinned host with device='cpu', pin=True)."""
+    n1 = dims.N + 1
+    kw = dict(device=device, pin_memory=pin) if pin else dict(device=device)
+    out = dict(tokens=torch.empty((dims.batch, n1), dtype=torch.int32, **kw),
+               parents=torch.empty((dims.batch, n1), dtype=torch.int32, **kw),
+               depths=torch.empty((dims.batch, n1), dtype=torch.int32, **kw),
+               scores=torch.empty((dims.batch, n1), dtype=torch.float32, **kw),
+               status=torch.empty((dims.batch,), dtype=torch.int32, **kw))
+    out["mask"] = torch.empty((dims.batch, n1, n1), dtype=torch.uint8, **kw) if mask else None
+    out["topm"] = (torch.empty((dims.batch, dims.D, dims.M), dtype=torch.int32, **kw)
+                   if topm else None)
+    return out
+
+
+def _out_struct(out) -> DtTreeOut:
+    return DtTreeOut(*[_ptr(out.get(n)) for n in ("tokens", "parents", "depths", "scores",
+                                                  "mask", "topm", "status")])
+
+
+def build_trees(dims: DtDims, w: DeviceWeights, prepared, base_logits, H, state0, anchor_tok,
+                temperature, workspace, out, opt: DtOptions | None = None, stream=None):
+    """Enqueue one round on device tensors (dt_build_trees)."""
+    ws = w.struct()
+    o = _out_struct(out)
+    _check(lib().dt_build_trees(C.byref(dims), C.byref(ws), _ptr(prepared), _ptr(base_logits),
+                                _ptr(H), _ptr(state0), _ptr(anchor_tok), _ptr(temperature),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                C.byref(o), C.byref(opt) if opt else None, _stream(stream)),
+           "dt_build_trees")
+
+
+def build_trees_host(dims: DtDims, w: DeviceWeights, prepared, base_logits, H, state0,
+                     anchor_tok, temperature, workspace, host_out, opt: DtOptions | None = None,
+                     stream=None):
+    """Enqueue one round on HOST input/output tensors (dt_build_trees_host). Synchronise
+    the stream before reading ``host_out``."""
+    ws = w.struct()
+    o = _out_struct(host_out)
+    _check(lib().dt_build_trees_host(C.byref(dims), C.byref(ws), _ptr(prepared),
+                                     _ptr(base_logits), _ptr(H), _ptr(state0), _ptr(anchor_tok),
+                                     _ptr(temperature), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), C.byref(o),
+                                     C.byref(opt) if opt else None, _stream(stream)),
+           "dt_build_trees_host")
+
+
+class TreeBuilder:
+    """Holds device weights, the prepared table and a workspace for one shape.
+
+    ``TreeBuilder.from_numpy(workload)`` copies a host workload's weights to the
+    device and prepares them; ``run(...)`` builds one round on device tensors."""
+
+    def __init__(self, dims: DtDims, weights: DeviceWeights, spec_width: int = 0,
+                 device="cuda"):
+        self.dims = dims
+        self.w = weights
+        self.device = torch.device(device)
+        self.opt = options(spec_width)
+        nbytes = prepared_bytes(dims)
+        if nbytes == 0:
+            raise DtError("invalid dims")
+        self.prepared = torch.empty(nbytes // 4, dtype=torch.float32, device=self.device)
+        prepare_weights(dims, weights, self.prepared)
+        wsb = workspace_bytes(dims, self.opt)
+        if wsb == 0:
+            raise DtError("dt_workspace_bytes failed (invalid dims or unsupported device)")
+        self.workspace = torch.empty(wsb, dtype=torch.uint8, device=self.device)
+
+    @staticmethod
+    def weights_from_numpy(wl, device="cuda") -> DeviceWeights:
+        import numpy as np
+
+        def t(a):
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                a = a.view(np.int16)
+            return torch.from_numpy(a).to(device)
+        return DeviceWeights(E=t(wl.E), W_ih=t(wl.W_ih), W_hh=t(wl.W_hh), W1=t(wl.W1),
+                             W2=t(wl.W2), b_ih=t(wl.b_ih), b_hh=t(wl.b_hh))
+
+    @classmethod
+    def from_numpy(cls, wl, spec_width: int = 0, device="cuda", batch=None):
+        dims = dims_of(wl.V, wl.d, wl.d_s, wl.r, wl.D, wl.M, wl.k, wl.N,
+                       wl.batch if batch is None else batch)
+        return cls(dims, cls.weights_from_numpy(wl, device), spec_width, device)
+
+    def run(self, base_logits, H, state0, anchor_tok, temperature=None, out=None, stream=None,
+            opt=None):
+        if out is None:
+            out = alloc_outputs(self.dims, self.device)
+        build_trees(self.dims, self.w, self.prepared, base_logits, H, state0, anchor_tok,
+                    temperature, self.workspace, out, opt or self.opt, stream)
+        return out
+
+    def inputs_to_device(self, wl):
+        import numpy as np
+        f = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(self.device)
+        return dict(base_logits=f(wl.base_logits, np.float32), H=f(wl.H, np.float32),
+                    state0=f(wl.state0, np.float32), anchor_tok=f(wl.anchor, np.int32),
+                    temperature=f(wl.temperature, np.float32))

@@ -1,0 +1,362 @@
+// dt_api.cu -- the C ABI of libdt.so (declared in include/dt.h): argument
+// validation, workspace carve-up and the launch sequence of one round.
+//
+// Round = top-M selection over the base logits ("Riassunto Tecnico: DominoTree",
+// Componenti Core 2) -> per-depth projection U_j = W1_H H_j (Componenti Core 1,
+// H_i shared) -> the conditional best-first search and tree emission
+// (Componenti Core 1, 4, 5). Nothing here allocates device memory.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "dt_internal.h"
+
+namespace dt {
+
+int chain_smem_bytes(const Plan &pl, int e_cap, int wave);
+const void *chain_kernel_ptr(int wdtype, int M);
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t al(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int device_sm_count(int *sms, int *smem_optin) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DT_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+          cudaSuccess)
+    return DT_ERR_CUDA;
+  if (major != 10 || minor != 3) return DT_ERR_UNSUPPORTED;  // built for sm_103a only
+  return DT_OK;
+}
+
+}  // namespace
+
+int validate_dims(const dt_dims *d) {
+  if (!d) return DT_ERR_INVALID_ARG;
+  if (d->V < 1 || d->batch < 1) return DT_ERR_INVALID_ARG;
+  if (d->d < 8 || d->d % 8) return DT_ERR_INVALID_ARG;
+  if (d->d_s < 8 || d->d_s % 8 || d->d_s > DT_MAX_DS) return DT_ERR_INVALID_ARG;
+  if (d->r < 8 || d->r % 8 || d->r > DT_MAX_R) return DT_ERR_INVALID_ARG;
+  if (d->D < 1 || d->D > DT_MAX_D) return DT_ERR_INVALID_ARG;
+  if (d->M < 1 || d->M > DT_MAX_M || d->M > d->V) return DT_ERR_INVALID_ARG;
+  if (d->k < 1 || d->k > DT_MAX_K || d->k > d->M) return DT_ERR_INVALID_ARG;
+  if (d->N < 0 || d->N > DT_MAX_N) return DT_ERR_INVALID_ARG;
+  return DT_OK;
+}
+
+int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
+  int rc = validate_dims(dims);
+  if (rc) return rc;
+  if (wdtype != DT_F32 && wdtype != DT_BF16) return DT_ERR_INVALID_ARG;
+  if (opt && (opt->spec_width < 0 || opt->spec_width > DT_MAX_SPEC)) return DT_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof *p);
+  p->dims = *dims;
+  p->wdtype = wdtype;
+  int smem_optin = 0;
+  rc = device_sm_count(&p->num_sms, &smem_optin);
+  if (rc) return rc;
+  const dt_dims &d = *dims;
+  p->spec = (opt && opt->spec_width > 0) ? opt->spec_width : 8;
+
+  // top-M segments: at most 64K elements per block, enough blocks to fill the GPU
+  const long long rows = static_cast<long long>(d.batch) * d.D;
+  if (rows > 65535) return DT_ERR_UNSUPPORTED;  // one grid row of the top-M launch per (b, j)
+  const long long by_size = (d.V + 65535) / 65536;
+  const long long by_util = (4LL * p->num_sms + rows - 1) / rows;
+  const long long by_min = (d.V + 4095) / 4096;
+  long long ns = by_size;
+  if (by_util > ns) ns = by_util < by_min ? by_util : (by_min > ns ? by_min : ns);
+  p->nsplit = static_cast<int>(ns < 1 ? 1 : ns);
+
+  // search kernel: expansion slots, shared memory and co-resident grid
+  const void *fn = chain_kernel_ptr(wdtype, d.M);
+  int wave = d.batch < 256 ? d.batch : 256;
+  if (wave > p->num_sms) wave = p->num_sms;
+  int e_cap = d.N + 1 + (p->spec > 1 ? d.N + 1 : 0);
+  int smem = chain_smem_bytes(*p, e_cap, wave);
+  while (smem > smem_optin && e_cap > d.N + 1) {
+    e_cap = d.N + 1 + (e_cap - d.N - 1) / 2;
+    smem = chain_smem_bytes(*p, e_cap, wave);
+  }
+  if (smem > smem_optin) return DT_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return DT_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256, smem) != cudaSuccess)
+    return DT_ERR_CUDA;
+  if (per_sm < 1) return DT_ERR_UNSUPPORTED;
+  p->chain_grid = per_sm * p->num_sms;
+  if (wave > p->chain_grid) wave = p->chain_grid;
+  p->wave = wave;
+  p->e_cap = e_cap;
+  p->chain_smem = static_cast<size_t>(smem);
+
+  // workspace carve-up
+  size_t off = 0;
+  p->off_ctrl = off;
+  off = al(off + kCtrlHeader + sizeof(unsigned) * rows + sizeof(int) * d.batch);
+  p->off_part = off;
+  off = al(off + (p->nsplit > 1 ? sizeof(uint64_t) * rows * p->nsplit * d.M : 0));
+  p->off_cand_id = off;   off = al(off + sizeof(int32_t) * rows * d.M);
+  p->off_cand_val = off;  off = al(off + sizeof(float) * rows * d.M);
+  p->off_U = off;         off = al(off + sizeof(float) * rows * d.r);
+  const size_t slots_e = static_cast<size_t>(wave) * (e_cap + 1);
+  p->off_S = off;         off = al(off + sizeof(float) * slots_e * d.d_s);
+  p->off_gh = off;        off = al(off + sizeof(float) * slots_e * 3 * d.d_s);
+  const size_t cols = static_cast<size_t>(wave) * p->spec;
+  p->off_gin = off;       off = al(off + sizeof(float) * cols * d.d_s);
+  p->off_p = off;         off = al(off + sizeof(float) * cols * d.r);
+  p->off_colexp = off;    off = al(off + sizeof(int) * (cols + wave));
+  p->off_end = off;
+  return DT_OK;
+}
+
+}  // namespace dt
+
+using dt::Plan;
+
+namespace {
+
+int check_weights(const dt_weights *w) {
+  if (!w || !w->E || !w->W_ih || !w->W_hh || !w->W1 || !w->W2) return DT_ERR_INVALID_ARG;
+  if (!dt::aligned16(w->E) || !dt::aligned16(w->W_ih) || !dt::aligned16(w->W_hh) ||
+      !dt::aligned16(w->W1) || !dt::aligned16(w->W2))
+    return DT_ERR_INVALID_ARG;
+  if ((w->b_ih && !dt::aligned4(w->b_ih)) || (w->b_hh && !dt::aligned4(w->b_hh)))
+    return DT_ERR_INVALID_ARG;
+  if (w->wdtype != DT_F32 && w->wdtype != DT_BF16) return DT_ERR_INVALID_ARG;
+  return DT_OK;
+}
+
+int check_out(const dt_tree_out *o) {
+  if (!o || !o->tokens || !o->parents || !o->depths || !o->scores || !o->status)
+    return DT_ERR_INVALID_ARG;
+  if (!dt::aligned4(o->tokens) || !dt::aligned4(o->parents) || !dt::aligned4(o->depths) ||
+      !dt::aligned4(o->scores) || !dt::aligned4(o->status) || (o->topm && !dt::aligned4(o->topm)))
+    return DT_ERR_INVALID_ARG;
+  return DT_OK;
+}
+
+int record(const dt_options *opt, int i, cudaStream_t st) {
+  if (!opt || !opt->phase_events || !opt->phase_events[i]) return DT_OK;
+  return cudaEventRecord(static_cast<cudaEvent_t>(opt->phase_events[i]), st) == cudaSuccess
+             ? DT_OK
+             : DT_ERR_CUDA;
+}
+
+// The round on device buffers; `plan` is already made.
+int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const float *base_logits,
+              const float *H, const float *state0, const int32_t *anchor_tok,
+              const float *temperature, void *ws, const dt_tree_out *out, const dt_options *opt,
+              cudaStream_t st) {
+  const dt_dims &d = pl.dims;
+  int rc = record(opt, 0, st);
+  if (rc) return rc;
+  char *wsb = static_cast<char *>(ws);
+  if (cudaMemsetAsync(wsb + pl.off_ctrl, 0, pl.off_part - pl.off_ctrl, st) != cudaSuccess)
+    return DT_ERR_CUDA;
+  if (dt::launch_topm(pl, base_logits, ws, out->topm, st) != cudaSuccess) return DT_ERR_CUDA;
+  float *U = reinterpret_cast<float *>(wsb + pl.off_U);
+  if (dt::launch_gemm_nt(d.batch * d.D, d.r, d.d, H, DT_F32, d.d, w->W1, w->wdtype,
+                         static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r, st) != cudaSuccess)
+    return DT_ERR_CUDA;
+  rc = record(opt, 1, st);
+  if (rc) return rc;
+  dt::ChainArgs a;
+  a.w = w;
+  a.G = static_cast<const float *>(prepared);
+  a.state0 = state0;
+  a.anchor = anchor_tok;
+  a.temperature = temperature;
+  a.out = out;
+  for (int b0 = 0; b0 < d.batch; b0 += pl.wave) {
+    a.b0 = b0;
+    a.nb = (d.batch - b0) < pl.wave ? (d.batch - b0) : pl.wave;
+    if (dt::launch_chain(pl, a, ws, st) != cudaSuccess) return DT_ERR_CUDA;
+  }
+  rc = record(opt, 2, st);
+  if (rc) return rc;
+  return record(opt, 3, st);
+}
+
+struct HostStaging {
+  size_t base, H, state0, anchor, temp, tokens, parents, depths, scores, mask, topm, status, end;
+};
+
+HostStaging host_staging(const dt_dims &d, size_t start) {
+  HostStaging s;
+  const size_t n1 = static_cast<size_t>(d.N) + 1;
+  size_t off = start;
+  s.base = off;    off = dt::al(off + sizeof(float) * d.batch * d.D * static_cast<size_t>(d.V));
+  s.H = off;       off = dt::al(off + sizeof(float) * d.batch * d.D * static_cast<size_t>(d.d));
+  s.state0 = off;  off = dt::al(off + sizeof(float) * d.batch * static_cast<size_t>(d.d_s));
+  s.anchor = off;  off = dt::al(off + sizeof(int32_t) * d.batch);
+  s.temp = off;    off = dt::al(off + sizeof(float) * d.batch);
+  s.tokens = off;  off = dt::al(off + sizeof(int32_t) * d.batch * n1);
+  s.parents = off; off = dt::al(off + sizeof(int32_t) * d.batch * n1);
+  s.depths = off;  off = dt::al(off + sizeof(int32_t) * d.batch * n1);
+  s.scores = off;  off = dt::al(off + sizeof(float) * d.batch * n1);
+  s.mask = off;    off = dt::al(off + d.batch * n1 * n1);
+  s.topm = off;    off = dt::al(off + sizeof(int32_t) * d.batch * d.D * static_cast<size_t>(d.M));
+  s.status = off;  off = dt::al(off + sizeof(int32_t) * d.batch);
+  s.end = off;
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dt_abi_version(void) { return DT_ABI_VERSION; }
+
+const char *dt_status_string(int code) {
+  switch (code) {
+    case DT_OK: return "ok";
+    case DT_ERR_INVALID_ARG: return "invalid argument (size, null pointer, alignment or limit)";
+    case DT_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case DT_ERR_CUDA: return "CUDA runtime or launch error";
+    case DT_ERR_NONFINITE: return "a base logit of the request is NaN or +inf";
+    case DT_ERR_TIMEOUT: return "bounded inter-block wait expired; request output invalid";
+    case DT_ERR_BAD_TEMPERATURE: return "temperature is negative or not finite";
+    default: return "unknown status code";
+  }
+}
+
+size_t dt_prepared_bytes(const dt_dims *dims) {
+  if (dt::validate_dims(dims)) return 0;
+  return sizeof(float) * static_cast<size_t>(dims->V) * 3 * dims->d_s;
+}
+
+int dt_prepare_weights(const dt_dims *dims, const dt_weights *w, void *prepared,
+                       size_t prepared_bytes, void *stream) {
+  int rc = dt::validate_dims(dims);
+  if (rc) return rc;
+  rc = check_weights(w);
+  if (rc) return rc;
+  if (!prepared || (reinterpret_cast<uintptr_t>(prepared) & 255u) ||
+      prepared_bytes < dt_prepared_bytes(dims))
+    return DT_ERR_INVALID_ARG;
+  int sms = 0, smem = 0;
+  rc = dt::device_sm_count(&sms, &smem);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dt::launch_gemm_nt(dims->V, 3 * dims->d_s, dims->d, w->E, w->wdtype, dims->d, w->W_ih,
+                         w->wdtype, dims->d, w->b_ih, static_cast<float *>(prepared),
+                         3 * static_cast<size_t>(dims->d_s), st) != cudaSuccess)
+    return DT_ERR_CUDA;
+  return DT_OK;
+}
+
+size_t dt_workspace_bytes(const dt_dims *dims, const dt_options *opt) {
+  Plan pl;
+  if (!dims) return 0;
+  if (dt::make_plan(dims, DT_BF16, opt, &pl)) return 0;
+  Plan pf;
+  if (dt::make_plan(dims, DT_F32, opt, &pf)) return 0;
+  return pl.off_end > pf.off_end ? pl.off_end : pf.off_end;
+}
+
+int dt_build_trees(const dt_dims *dims, const dt_weights *w, const void *prepared,
+                   const float *base_logits, const float *H, const float *state0,
+                   const int32_t *anchor_tok, const float *temperature, void *workspace,
+                   size_t workspace_bytes, const dt_tree_out *out, const dt_options *opt,
+                   void *stream) {
+  int rc = dt::validate_dims(dims);
+  if (rc) return rc;
+  rc = check_weights(w);
+  if (rc) return rc;
+  rc = check_out(out);
+  if (rc) return rc;
+  if (!prepared || !base_logits || !H || !state0 || !anchor_tok || !workspace)
+    return DT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || !dt::aligned16(prepared) ||
+      !dt::aligned16(H) || !dt::aligned16(state0) || !dt::aligned4(base_logits) ||
+      !dt::aligned4(anchor_tok) || (temperature && !dt::aligned4(temperature)))
+    return DT_ERR_INVALID_ARG;
+  if (dims->V % 4 == 0 && !dt::aligned16(base_logits)) return DT_ERR_INVALID_ARG;
+  Plan pl;
+  rc = dt::make_plan(dims, w->wdtype, opt, &pl);
+  if (rc) return rc;
+  if (workspace_bytes < pl.off_end) return DT_ERR_INVALID_ARG;
+  return run_round(pl, w, prepared, base_logits, H, state0, anchor_tok, temperature, workspace,
+                   out, opt, static_cast<cudaStream_t>(stream));
+}
+
+size_t dt_host_workspace_bytes(const dt_dims *dims, const dt_options *opt) {
+  size_t ws = dt_workspace_bytes(dims, opt);
+  if (!ws) return 0;
+  return host_staging(*dims, dt::al(ws)).end;
+}
+
+int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *prepared,
+                        const float *base_logits, const float *H, const float *state0,
+                        const int32_t *anchor_tok, const float *temperature, void *workspace,
+                        size_t workspace_bytes, const dt_tree_out *host_out,
+                        const dt_options *opt, void *stream) {
+  int rc = dt::validate_dims(dims);
+  if (rc) return rc;
+  rc = check_weights(w);
+  if (rc) return rc;
+  if (!host_out || !host_out->tokens || !host_out->parents || !host_out->depths ||
+      !host_out->scores || !host_out->status || !prepared || !base_logits || !H || !state0 ||
+      !anchor_tok || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return DT_ERR_INVALID_ARG;
+  Plan pl;
+  rc = dt::make_plan(dims, w->wdtype, opt, &pl);
+  if (rc) return rc;
+  const size_t ws_dev = dt_workspace_bytes(dims, opt);
+  const HostStaging s = host_staging(*dims, dt::al(ws_dev));
+  if (workspace_bytes < s.end) return DT_ERR_INVALID_ARG;
+  const dt_dims &d = *dims;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char *wsb = static_cast<char *>(workspace);
+  const size_t n1 = static_cast<size_t>(d.N) + 1;
+  auto h2d = [&](size_t off, const void *src, size_t bytes) {
+    return cudaMemcpyAsync(wsb + off, src, bytes, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  };
+  auto d2h = [&](void *dst, size_t off, size_t bytes) {
+    return cudaMemcpyAsync(dst, wsb + off, bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  };
+  const size_t nb = static_cast<size_t>(d.batch);
+  if (!h2d(s.base, base_logits, sizeof(float) * nb * d.D * d.V) ||
+      !h2d(s.H, H, sizeof(float) * nb * d.D * d.d) ||
+      !h2d(s.state0, state0, sizeof(float) * nb * d.d_s) ||
+      !h2d(s.anchor, anchor_tok, sizeof(int32_t) * nb) ||
+      (temperature && !h2d(s.temp, temperature, sizeof(float) * nb)))
+    return DT_ERR_CUDA;
+  dt_tree_out dev;
+  dev.tokens = reinterpret_cast<int32_t *>(wsb + s.tokens);
+  dev.parents = reinterpret_cast<int32_t *>(wsb + s.parents);
+  dev.depths = reinterpret_cast<int32_t *>(wsb + s.depths);
+  dev.scores = reinterpret_cast<float *>(wsb + s.scores);
+  dev.mask = host_out->mask ? reinterpret_cast<uint8_t *>(wsb + s.mask) : nullptr;
+  dev.topm = host_out->topm ? reinterpret_cast<int32_t *>(wsb + s.topm) : nullptr;
+  dev.status = reinterpret_cast<int32_t *>(wsb + s.status);
+  rc = run_round(pl, w, prepared, reinterpret_cast<const float *>(wsb + s.base),
+                 reinterpret_cast<const float *>(wsb + s.H),
+                 reinterpret_cast<const float *>(wsb + s.state0),
+                 reinterpret_cast<const int32_t *>(wsb + s.anchor),
+                 temperature ? reinterpret_cast<const float *>(wsb + s.temp) : nullptr, workspace,
+                 &dev, opt, st);
+  if (rc) return rc;
+  if (!d2h(host_out->tokens, s.tokens, sizeof(int32_t) * nb * n1) ||
+      !d2h(host_out->parents, s.parents, sizeof(int32_t) * nb * n1) ||
+      !d2h(host_out->depths, s.depths, sizeof(int32_t) * nb * n1) ||
+      !d2h(host_out->scores, s.scores, sizeof(float) * nb * n1) ||
+      !d2h(host_out->status, s.status, sizeof(int32_t) * nb) ||
+      (host_out->mask && !d2h(host_out->mask, s.mask, nb * n1 * n1)) ||
+      (host_out->topm && !d2h(host_out->topm, s.topm, sizeof(int32_t) * nb * d.D * d.M)))
+    return DT_ERR_CUDA;
+  return DT_OK;
+}
+
+}  // extern "C"

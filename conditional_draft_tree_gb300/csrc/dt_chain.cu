@@ -1,0 +1,731 @@
+// dt_chain.cu -- the best-first conditional search, one persistent cooperative
+// kernel for a wave of requests.
+//
+// What it computes ("Riassunto Tecnico: DominoTree", Componenti Core 1, 2, 4, 5;
+// "Domino", core method): node 0 is the root (anchor token, score 0) with GRU
+// state S_0 = GRU(state0, E[anchor]). Expanding a node x of depth j-1 scores the
+// top-M candidates C_j of depth j with the correction along x's path,
+//   h    = SiLU(U_j + W1_S S_x),    U_j = W1_H H_j precomputed per depth
+//   L_c  = (L_base^j[c] + W2[c,:] h) / T,   lp_c = L_c - logsumexp_{C_j} L
+// and offers its k best candidates (L desc, id asc) as children with score
+// score(x) + lp_c. Nodes are popped best first, (score desc, push order asc),
+// until N nodes are out; a popped node gets the state S = GRU(S_parent, E[tok])
+// and is expanded unless it is at depth D or is the N-th pop.
+//
+// How (GB300 design): the requests advance in lockstep steps. A step is
+//   GEMM phase  (all blocks): [gh_x; p_x] = [W_hh; W1_S] S_x (+[b_hh; 0]) for the
+//               nodes x of every request that were chosen for expansion;
+//   grid barrier;
+//   tail phase  (block b = request b): score the children of those nodes, pop
+//               as far as the exact best-first order allows, choose the next
+//               nodes to expand, advance their GRU states;
+//   grid barrier.
+// The GRU input half W_ih E[tok] + b_ih is a row of the prepared table G, and
+// the recurrent half gh of a node is produced by the GEMM of the step that
+// expanded its parent, so the per-node GRU is elementwise.
+//
+// Exact speculative expansion: the order in which nodes are popped depends only
+// on scores, so expanding a node earlier than the one-at-a-time builder would
+// changes nothing but the time at which its children become known. The tail
+// replays the canonical best-first order over the discovered nodes and stops at
+// the first popped node that still needs its children ("stall"). It then expands
+// that node together with up to P-1 of the next best unexpanded frontier nodes
+// (P = spec width). Each step therefore pops at least one node, the trees are
+// identical for every P, and the number of lockstep steps drops from about N
+// to about the depth of the tree when the tree is bushy.
+//
+// Frontier representation: the children of an expanded node are stored sorted
+// (their scores are non-increasing in rank), so the frontier is a set of sorted
+// runs, one per popped expanded node, created in pop order. The next pop is the
+// best run head under (score desc, run index asc) -- run index order is the
+// parents' pop order and rank order is push order, which is exactly the heap's
+// (score desc, push sequence asc) key.
+#include <cstdint>
+
+#include "dt_common.cuh"
+#include "dt_internal.h"
+
+namespace dt {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kGemmCols = 8;     // columns per GEMM work unit
+constexpr int kGemmKC = 1024;    // K chunk staged in shared memory
+constexpr int kState0 = -2;      // column code: the state0 column of the first step
+
+struct ChainParams {
+  int V, d, d_s, r, D, M, k, N;
+  int nb, b0, P, e_cap;
+  const void *W_hh, *W1, *W2;
+  const float *b_hh;
+  const float *G;
+  const float *state0;
+  const int32_t *anchor;
+  const float *temperature;
+  const int32_t *cand_id;
+  const float *cand_val;
+  const float *U;
+  float *S_store, *gh_store, *gin, *pbuf;
+  int *colexp, *col_count;
+  Ctrl *ctrl;
+  const int *req_flags;
+  int32_t *tokens, *parents, *depths;
+  float *scores;
+  uint8_t *mask;
+  int32_t *status;
+  unsigned long long limit_ns;
+  // dynamic shared memory carve-up (byte offsets)
+  int sm_child_score, sm_child_tok, sm_child_exp, sm_exp_depth, sm_exp_parent, sm_exp_score,
+      sm_exp_tok, sm_run_e, sm_run_head, sm_run_pos, sm_vhead, sm_par, sm_scratch, sm_total;
+};
+
+struct TailState {
+  int count;      // nodes popped so far (root excluded)
+  int n_runs;
+  int e_count;    // expansions assigned
+  int done;
+  int n_sel;
+  int spec_used;  // speculative (non-stall) expansions made so far
+  int sel_e[DT_MAX_SPEC];
+  float T;
+  int status;
+};
+
+__device__ __forceinline__ float ldcg(const float *p) { return __ldcg(p); }
+
+// Sum of v[i] over the 32 lanes, scattered: lane l returns the total of v[l].
+__device__ __forceinline__ float reduce_scatter32(float v[32], int lane) {
+#pragma unroll
+  for (int m = 16, n = 32; m >= 1; m >>= 1, n >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      float send = hi ? v[i] : v[i + n / 2];
+      float keep = hi ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFull, send, m);
+    }
+  }
+  return v[0];
+}
+
+// Full descending bitonic sort of 32*SLOTS keys held slot-major in a warp.
+template <int SLOTS>
+__device__ __forceinline__ void warp_sort_desc(uint64_t v[SLOTS], int lane) {
+  constexpr int n = 32 * SLOTS;
+#pragma unroll
+  for (int size = 2; size <= n; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride >= 1; stride >>= 1) {
+      if (stride >= 32) {
+        const int ds = stride >> 5;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+          if ((s & ds) == 0) {
+            const int i = s * 32 + lane;
+            const bool desc = (i & size) == 0;
+            uint64_t a = v[s], b = v[s + ds];
+            bool sw = desc ? (a < b) : (a > b);
+            v[s] = sw ? b : a;
+            v[s + ds] = sw ? a : b;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+          const int i = s * 32 + lane;
+          const bool desc = (i & size) == 0;
+          uint64_t o = shfl64_xor(v[s], stride);
+          const bool low = (lane & stride) == 0;
+          // lower index keeps the larger key in a descending run
+          const bool keep_max = (low == desc);
+          uint64_t mx = v[s] > o ? v[s] : o, mn = v[s] > o ? o : v[s];
+          v[s] = keep_max ? mx : mn;
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- GEMM phase
+
+// [gh; p] = [W_hh; W1_S] x (+ [b_hh; 0]) for every active column.
+template <int WDT>
+__device__ void gemm_phase(const ChainParams &p, unsigned char *smem) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ds = p.d_s;
+  const int R = 3 * ds + p.r;
+  // compact the active columns: slot ids in (request, rank) order. nb <= 256
+  // requests per wave: one thread per request, block-wide exclusive scan.
+  int *slots = reinterpret_cast<int *>(smem);  // [nb * P]
+  __shared__ int s_warp_sum[kWarps];
+  __shared__ int s_total;
+  const int b_me = threadIdx.x;
+  const int c_me = (b_me < p.nb) ? __ldcg(p.col_count + b_me) : 0;
+  int incl = c_me;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_warp_sum[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += s_warp_sum[w];
+  if (threadIdx.x == kThreads - 1) s_total = base + incl;
+  for (int i = 0; i < c_me; ++i) slots[base + incl - c_me + i] = b_me * p.P + i;
+  __syncthreads();
+  const int total = s_total;
+  if (total == 0) return;
+  float *stage = reinterpret_cast<float *>(smem + ((p.nb * p.P * 4 + 15) & ~15));  // [8][KC]
+  const int nct = (total + kGemmCols - 1) / kGemmCols;
+  int rparts = max(1, static_cast<int>(gridDim.x) / nct);
+  const int rgroups = (R + 3) / 4;
+  rparts = min(rparts, rgroups);
+  const int groups_per_part = (rgroups + rparts - 1) / rparts;
+  const int units = nct * rparts;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int ct = u % nct, rp = u / nct;
+    const int c0 = ct * kGemmCols;
+    const int ncol = min(kGemmCols, total - c0);
+    const int g0 = rp * groups_per_part, g1 = min(rgroups, g0 + groups_per_part);
+    for (int kc0 = 0; kc0 < ds; kc0 += kGemmKC) {
+      const int kc1 = min(ds, kc0 + kGemmKC);
+      const int kw = kc1 - kc0;
+      // groups are processed per K chunk; accumulators live only within a group
+      // when ds <= KC (the common case); for larger ds partial sums go to the
+      // outputs through a second pass below.
+      __syncthreads();
+      for (int i = threadIdx.x; i < kGemmCols * (kw / 4); i += kThreads) {
+        const int c = i / (kw / 4), q = i % (kw / 4);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < ncol) {
+          const int slot = slots[c0 + c];
+          v = __ldcg(reinterpret_cast<const float4 *>(p.gin + static_cast<size_t>(slot) * ds +
+                                                      kc0) + q);
+        }
+        reinterpret_cast<float4 *>(stage + c * kGemmKC)[q] = v;
+      }
+      __syncthreads();
+      for (int g = g0 + warp; g < g1; g += kWarps) {
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+        const void *wrow[4];
+        bool rok[4];
+#pragma unroll
+        for (int ri = 0; ri < 4; ++ri) {
+          const int row = g * 4 + ri;
+          rok[ri] = row < R;
+          if (row < 3 * ds) {
+            wrow[ri] = static_cast<const char *>(p.W_hh) +
+                       static_cast<size_t>(row) * ds * (WDT ? 2 : 4);
+          } else {
+            const int t = rok[ri] ? row - 3 * ds : 0;
+            wrow[ri] = static_cast<const char *>(p.W1) +
+                       (static_cast<size_t>(t) * (p.d + ds) + p.d) * (WDT ? 2 : 4);
+          }
+        }
+        for (int k = lane * 8; k < kw; k += 256) {
+          float wf[4][8];
+#pragma unroll
+          for (int ri = 0; ri < 4; ++ri) {
+            if (rok[ri]) {
+              load8<WDT>(wrow[ri], kc0 + k, wf[ri]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) wf[ri][e] = 0.f;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < kGemmCols; ++c) {
+            const float4 x0 = *reinterpret_cast<const float4 *>(stage + c * kGemmKC + k);
+            const float4 x1 = *reinterpret_cast<const float4 *>(stage + c * kGemmKC + k + 4);
+#pragma unroll
+            for (int ri = 0; ri < 4; ++ri) {
+              float a = acc[ri * 8 + c];
+              a = fmaf(wf[ri][0], x0.x, a); a = fmaf(wf[ri][1], x0.y, a);
+              a = fmaf(wf[ri][2], x0.z, a); a = fmaf(wf[ri][3], x0.w, a);
+              a = fmaf(wf[ri][4], x1.x, a); a = fmaf(wf[ri][5], x1.y, a);
+              a = fmaf(wf[ri][6], x1.z, a); a = fmaf(wf[ri][7], x1.w, a);
+              acc[ri * 8 + c] = a;
+            }
+          }
+        }
+        const float sum = reduce_scatter32(acc, lane);
+        const int ri = lane >> 3, c = lane & 7;
+        const int row = g * 4 + ri;
+        if (row < R && c < ncol) {
+          const int slot = slots[c0 + c];
+          const int b = slot / p.P;
+          const int e = __ldcg(p.colexp + slot);
+          if (row < 3 * ds) {
+            const int e_slot = (e == kState0) ? p.e_cap : e;
+            float *dst = p.gh_store + (static_cast<size_t>(b) * (p.e_cap + 1) + e_slot) * 3 * ds + row;
+            const float prev = (kc0 == 0) ? (p.b_hh ? p.b_hh[row] : 0.f) : __ldcg(dst);
+            *dst = prev + sum;
+          } else {
+            float *dst = p.pbuf + static_cast<size_t>(slot) * p.r + (row - 3 * ds);
+            const float prev = (kc0 == 0) ? 0.f : __ldcg(dst);
+            *dst = prev + sum;
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- tail phase
+
+struct Tables {
+  float *child_score;    // [e_cap][k]
+  int32_t *child_tok;    // [e_cap][k]
+  int16_t *child_exp;    // [e_cap][k]
+  int8_t *exp_depth;     // [e_cap]
+  int16_t *exp_parent;   // [e_cap]
+  float *exp_score;      // [e_cap]
+  int32_t *exp_tok;      // [e_cap]
+  int16_t *run_e;        // [N+1]
+  uint8_t *run_head;     // [N+1]
+  int16_t *run_pos;      // [N+1]
+  uint8_t *vhead;        // [N+1]
+  int16_t *par;          // [N+1] parents of the output rows
+  float *scratch;
+};
+
+__device__ Tables tables(const ChainParams &p, unsigned char *smem) {
+  Tables t;
+  t.child_score = reinterpret_cast<float *>(smem + p.sm_child_score);
+  t.child_tok = reinterpret_cast<int32_t *>(smem + p.sm_child_tok);
+  t.child_exp = reinterpret_cast<int16_t *>(smem + p.sm_child_exp);
+  t.exp_depth = reinterpret_cast<int8_t *>(smem + p.sm_exp_depth);
+  t.exp_parent = reinterpret_cast<int16_t *>(smem + p.sm_exp_parent);
+  t.exp_score = reinterpret_cast<float *>(smem + p.sm_exp_score);
+  t.exp_tok = reinterpret_cast<int32_t *>(smem + p.sm_exp_tok);
+  t.run_e = reinterpret_cast<int16_t *>(smem + p.sm_run_e);
+  t.run_head = reinterpret_cast<uint8_t *>(smem + p.sm_run_head);
+  t.run_pos = reinterpret_cast<int16_t *>(smem + p.sm_run_pos);
+  t.vhead = reinterpret_cast<uint8_t *>(smem + p.sm_vhead);
+  t.par = reinterpret_cast<int16_t *>(smem + p.sm_par);
+  t.scratch = reinterpret_cast<float *>(smem + p.sm_scratch);
+  return t;
+}
+
+// Warp-wide best run head under (score desc, run index asc) using heads `hd`.
+// Returns the run index or -1 when every run is exhausted.
+__device__ __forceinline__ int best_run(const ChainParams &p, const Tables &t, const uint8_t *hd,
+                                        int n_runs, int lane) {
+  float best = 0.f;
+  int br = -1;
+  for (int r = lane; r < n_runs; r += 32) {
+    const int h = hd[r];
+    if (h < p.k) {
+      const float s = t.child_score[t.run_e[r] * p.k + h];
+      if (br < 0 || s > best) { best = s; br = r; }   // r ascending within a lane
+    }
+  }
+#pragma unroll
+  for (int m = 16; m; m >>= 1) {
+    const float ob = __shfl_xor_sync(kFull, best, m);
+    const int orr = __shfl_xor_sync(kFull, br, m);
+    const bool take = orr >= 0 && (br < 0 || ob > best || (ob == best && orr < br));
+    if (take) { best = ob; br = orr; }
+  }
+  return br;
+}
+
+// GRU cell for node e of request b: S_e = GRU(S_parent, x = E[tok]) with the
+// input half taken from the prepared table row G[tok] (= W_ih E[tok] + b_ih) and
+// the recurrent half gh_parent (= W_hh S_parent + b_hh) from an earlier GEMM.
+__device__ __forceinline__ void gru_node(const ChainParams &p, int b, int tok, const float *gh,
+                                         const float *sp, float *s_out, float *col_out) {
+  const int ds = p.d_s;
+  const float *gi = p.G + static_cast<size_t>(tok) * 3 * ds;
+  for (int u = threadIdx.x; u < ds; u += kThreads) {
+    const float r = sigmoidf_(__ldg(gi + u) + ldcg(gh + u));
+    const float z = sigmoidf_(__ldg(gi + ds + u) + ldcg(gh + ds + u));
+    const float n = tanhf(__ldg(gi + 2 * ds + u) + r * ldcg(gh + 2 * ds + u));
+    const float s = (1.f - z) * n + z * ldcg(sp + u);
+    s_out[u] = s;
+    col_out[u] = s;
+  }
+}
+
+
+// Children of expansion e (warp-level): h = SiLU(U_j + p), L over the M
+// candidates of depth j, log-sum-exp over them, the k best by (L desc, id asc).
+template <int WDT, int SLOTS>
+__device__ void score_node(const ChainParams &p, const Tables &t, float T, int b, int slot, int e,
+                           float *hbuf, int lane) {
+  const int j = t.exp_depth[e] + 1;
+  const size_t row = static_cast<size_t>(p.b0 + b) * p.D + (j - 1);
+  const float *U = p.U + row * p.r;
+  const float *pv = p.pbuf + static_cast<size_t>(slot) * p.r;
+  for (int q = lane; q < p.r; q += 32) hbuf[q] = siluf_(__ldg(U + q) + ldcg(pv + q));
+  __syncwarp();
+  const int32_t *cid = p.cand_id + row * p.M;
+  const float *cval = p.cand_val + row * p.M;
+  const float ninf = -__int_as_float(0x7f800000);
+  uint64_t key[SLOTS];
+  float Lv[SLOTS];
+  float mx = ninf;
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) {
+    const int c = s * 32 + lane;
+    key[s] = 0ull;
+    Lv[s] = ninf;
+    if (c < p.M) {
+      const int id = __ldg(cid + c);
+      const size_t w0 = static_cast<size_t>(id) * p.r;
+      float acc = 0.f;
+      for (int q = 0; q < p.r; q += 8) {
+        float wf[8];
+        load8<WDT>(p.W2, w0 + q, wf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc = fmaf(wf[i], hbuf[q + i], acc);
+      }
+      const float L = __fdiv_rn(__ldg(cval + c) + acc, T);
+      Lv[s] = L;
+      key[s] = make_key(L, static_cast<uint32_t>(id));
+      mx = fmaxf(mx, L);
+    }
+  }
+  mx = warp_max(mx);
+  float sum = 0.f;
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s)
+    if (s * 32 + lane < p.M) sum += expf(Lv[s] - mx);
+  sum = warp_sum(sum);
+  const float lse = (mx == ninf) ? ninf : mx + logf(sum);
+  warp_sort_desc<SLOTS>(key, lane);
+  const float base_score = t.exp_score[e];
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) {
+    const int i = s * 32 + lane;
+    if (i < p.k) {
+      const float L = key_value(key[s]);
+      const float lp = (lse == ninf) ? ninf : L - lse;
+      t.child_score[e * p.k + i] = base_score + lp;
+      t.child_tok[e * p.k + i] = static_cast<int32_t>(key_id(key[s]));
+      t.child_exp[e * p.k + i] = -1;
+    }
+  }
+}
+
+__device__ void write_row(const ChainParams &p, int b, int pos, int tok, int par, int dep,
+                          float sc) {
+  const size_t o = static_cast<size_t>(p.b0 + b) * (p.N + 1) + pos;
+  p.tokens[o] = tok;
+  p.parents[o] = par;
+  p.depths[o] = dep;
+  p.scores[o] = sc;
+}
+
+// Rows after the last pop, the ancestor mask, the status; then leave the search.
+__device__ void finalize(const ChainParams &p, const Tables &t, TailState &ts, int b,
+                         bool counted) {
+  __syncthreads();
+  const int count = ts.count;
+  const int first_empty = ts.status ? 0 : count + 1;
+  for (int i = first_empty + threadIdx.x; i <= p.N; i += kThreads)
+    write_row(p, b, i, -1, -1, -1, -__int_as_float(0x7f800000));
+  if (p.mask) {
+    const size_t n1 = static_cast<size_t>(p.N) + 1;
+    uint8_t *mb = p.mask + static_cast<size_t>(p.b0 + b) * n1 * n1;
+    for (size_t i = threadIdx.x; i < n1 * n1; i += kThreads) mb[i] = 0;
+    __syncthreads();
+    if (!ts.status) {
+      for (int i = threadIdx.x; i <= count; i += kThreads)
+        for (int a = i; a >= 0; a = t.par[a]) mb[static_cast<size_t>(i) * n1 + a] = 1;
+    }
+  }
+  if (threadIdx.x == 0) {
+    p.status[p.b0 + b] = ts.status;
+    ts.done = 1;
+    if (counted) atomicSub(&p.ctrl->active, 1);
+  }
+  __syncthreads();
+}
+
+// Pop in canonical order until done or until a popped node needs children that
+// are not known yet; then choose the next nodes to expand. Warp 0 only.
+__device__ void replay_and_select(const ChainParams &p, const Tables &t, TailState &ts, int b,
+                                  int lane) {
+  int count = ts.count, n_runs = ts.n_runs;
+  bool done = false;
+  while (true) {
+    if (count >= p.N) { done = true; break; }
+    const int r = best_run(p, t, t.run_head, n_runs, lane);
+    if (r < 0) { done = true; break; }
+    const int h = t.run_head[r], er = t.run_e[r];
+    const int dep = t.exp_depth[er] + 1, pos = count + 1;
+    const int ce = t.child_exp[er * p.k + h];
+    const bool need = dep < p.D && pos < p.N;
+    if (need && ce < 0) break;  // stall: this node's children are not known yet
+    if (lane == 0) {
+      write_row(p, b, pos, t.child_tok[er * p.k + h], t.run_pos[r], dep,
+                t.child_score[er * p.k + h]);
+      t.par[pos] = t.run_pos[r];
+      t.run_head[r] = static_cast<uint8_t>(h + 1);
+      if (need) {
+        t.run_e[n_runs] = static_cast<int16_t>(ce);
+        t.run_head[n_runs] = 0;
+        t.run_pos[n_runs] = static_cast<int16_t>(pos);
+      }
+    }
+    n_runs += need ? 1 : 0;
+    count = pos;
+    __syncwarp();
+  }
+  if (done) {
+    if (lane == 0) { ts.count = count; ts.n_runs = n_runs; ts.n_sel = 0; ts.done = 2; }
+    __syncwarp();
+    return;
+  }
+  // choose the stalled node plus up to P-1 of the next frontier nodes in order
+  const int spec_left = p.e_cap - p.N - ts.spec_used;
+  for (int r = lane; r < n_runs; r += 32) t.vhead[r] = t.run_head[r];
+  __syncwarp();
+  int nsel = 0, nspec = 0, i = 0;
+  int e_count = ts.e_count;
+  while (nsel < p.P) {
+    const int r = best_run(p, t, t.vhead, n_runs, lane);
+    if (r < 0) break;
+    ++i;
+    if (count + i >= p.N) break;
+    const int h = t.vhead[r], er = t.run_e[r];
+    const int dep = t.exp_depth[er] + 1;
+    const bool fresh = dep < p.D && t.child_exp[er * p.k + h] < 0;
+    const bool take = fresh && (nsel == 0 || nspec < spec_left);
+    if (lane == 0) {
+      t.vhead[r] = static_cast<uint8_t>(h + 1);
+      if (take) {
+        const int e = e_count + nsel;
+        t.child_exp[er * p.k + h] = static_cast<int16_t>(e);
+        t.exp_depth[e] = static_cast<int8_t>(dep);
+        t.exp_parent[e] = static_cast<int16_t>(er);
+        t.exp_score[e] = t.child_score[er * p.k + h];
+        t.exp_tok[e] = t.child_tok[er * p.k + h];
+        ts.sel_e[nsel] = e;
+        p.colexp[b * p.P + nsel] = e;
+      }
+    }
+    if (take) {
+      nspec += (nsel > 0) ? 1 : 0;
+      ++nsel;
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    ts.count = count;
+    ts.n_runs = n_runs;
+    ts.e_count = e_count + nsel;
+    ts.n_sel = nsel;
+    ts.spec_used += nspec;
+    p.col_count[b] = nsel;
+  }
+  __syncwarp();
+}
+
+
+__device__ void tail_init(const ChainParams &p, const Tables &t, TailState &ts, int b) {
+  if (threadIdx.x == 0) {
+    ts.count = 0; ts.n_runs = 0; ts.e_count = 0; ts.done = 0; ts.n_sel = 0; ts.spec_used = 0;
+    ts.status = DT_OK;
+    float T = p.temperature ? p.temperature[p.b0 + b] : 1.0f;
+    if (p.req_flags[p.b0 + b] & kReqFlagNonfinite) ts.status = DT_ERR_NONFINITE;
+    else if (!(T >= 0.0f) || T == __int_as_float(0x7f800000)) ts.status = DT_ERR_BAD_TEMPERATURE;
+    ts.T = (T == 0.0f) ? 1.0f : T;  // T = 0: greedy ordering, read as T = 1
+    t.par[0] = -1;
+    p.col_count[b] = 0;
+  }
+  __syncthreads();
+  if (ts.status != DT_OK) { finalize(p, t, ts, b, false); return; }
+  const int anchor = p.anchor[p.b0 + b];
+  if (threadIdx.x == 0) write_row(p, b, 0, anchor, -1, 0, 0.0f);
+  if (p.N == 0) { finalize(p, t, ts, b, false); return; }
+  // first GEMM column: the initial state, for W_hh state0 + b_hh
+  const float *s0 = p.state0 + static_cast<size_t>(p.b0 + b) * p.d_s;
+  float *col = p.gin + static_cast<size_t>(b) * p.P * p.d_s;
+  for (int u = threadIdx.x; u < p.d_s; u += kThreads) col[u] = s0[u];
+  if (threadIdx.x == 0) {
+    p.colexp[b * p.P] = kState0;
+    p.col_count[b] = 1;
+    atomicAdd(&p.ctrl->active, 1);
+  }
+  __syncthreads();
+}
+
+template <int WDT, int SLOTS>
+__device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, int b) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ncols = ts.n_sel;
+  const size_t ebase = static_cast<size_t>(b) * (p.e_cap + 1);
+  if (ts.e_count == 0) {
+    // the root: S_0 = GRU(state0, E[anchor]); its recurrent half came from the state0 column
+    const int anchor = p.anchor[p.b0 + b];
+    gru_node(p, b, anchor, p.gh_store + (ebase + p.e_cap) * 3 * p.d_s,
+             p.state0 + static_cast<size_t>(p.b0 + b) * p.d_s, p.S_store + ebase * p.d_s,
+             p.gin + static_cast<size_t>(b) * p.P * p.d_s);
+    if (threadIdx.x == 0) {
+      t.exp_depth[0] = 0; t.exp_parent[0] = -1; t.exp_score[0] = 0.0f; t.exp_tok[0] = anchor;
+      ts.e_count = 1;
+      ts.n_sel = 1;
+      ts.sel_e[0] = 0;
+      p.colexp[b * p.P] = 0;
+      p.col_count[b] = 1;
+    }
+    __syncthreads();
+    return;
+  }
+  // 1. children of the nodes expanded by the last GEMM (one warp per node)
+  float *hbuf = t.scratch + warp * p.r;
+  for (int i = warp; i < ncols; i += kWarps)
+    score_node<WDT, SLOTS>(p, t, ts.T, b, b * p.P + i, ts.sel_e[i], hbuf, lane);
+  __syncthreads();
+  if (threadIdx.x == 0 && ts.n_runs == 0) {  // the root's children form the first run
+    t.run_e[0] = 0; t.run_head[0] = 0; t.run_pos[0] = 0;
+    ts.n_runs = 1;
+  }
+  __syncthreads();
+  // 2. canonical pops, then the next expansions
+  if (warp == 0) replay_and_select(p, t, ts, b, lane);
+  __syncthreads();
+  if (ts.done == 2) { finalize(p, t, ts, b, true); return; }
+  // 3. GRU states of the chosen nodes
+  for (int i = 0; i < ts.n_sel; ++i) {
+    const int e = ts.sel_e[i];
+    const int pe = t.exp_parent[e];
+    gru_node(p, b, t.exp_tok[e], p.gh_store + (ebase + pe) * 3 * p.d_s,
+             p.S_store + (ebase + pe) * p.d_s, p.S_store + (ebase + e) * p.d_s,
+             p.gin + (static_cast<size_t>(b) * p.P + i) * p.d_s);
+  }
+  __syncthreads();
+}
+
+template <int WDT, int SLOTS>
+__global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ TailState ts;
+  __shared__ int s_active;
+  const Tables t = tables(p, smem);
+  const int b = blockIdx.x;
+  const bool tail = b < p.nb;
+  if (tail) tail_init(p, t, ts, b);
+  bool ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
+                         p.limit_ns);
+  for (int step = 0; ok && step < p.N + 3; ++step) {
+    gemm_phase<WDT>(p, smem + p.sm_scratch);
+    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
+                      p.limit_ns);
+    if (!ok) break;
+    if (tail && !ts.done) tail_step<WDT, SLOTS>(p, t, ts, b);
+    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
+                      p.limit_ns);
+    if (!ok) break;
+    if (threadIdx.x == 0) s_active = ld_acquire_s32(&p.ctrl->active);
+    __syncthreads();
+    if (s_active == 0) break;
+  }
+  if (tail && !ts.done) {
+    if (threadIdx.x == 0) ts.status = DT_ERR_TIMEOUT;
+    finalize(p, t, ts, b, true);
+  }
+}
+
+}  // namespace
+
+// Shared-memory carve-up of the search kernel for e_cap expansion slots.
+static int chain_smem_layout(const Plan &pl, int e_cap, int wave, ChainParams *cp) {
+  const dt_dims &d = pl.dims;
+  auto al = [](int x, int a) { return (x + a - 1) / a * a; };
+  int off = 0;
+  const int k = d.k, n1 = d.N + 1;
+  cp->sm_child_score = off; off = al(off + e_cap * k * 4, 16);
+  cp->sm_child_tok = off;   off = al(off + e_cap * k * 4, 16);
+  cp->sm_child_exp = off;   off = al(off + e_cap * k * 2, 16);
+  cp->sm_exp_depth = off;   off = al(off + e_cap, 16);
+  cp->sm_exp_parent = off;  off = al(off + e_cap * 2, 16);
+  cp->sm_exp_score = off;   off = al(off + e_cap * 4, 16);
+  cp->sm_exp_tok = off;     off = al(off + e_cap * 4, 16);
+  cp->sm_run_e = off;       off = al(off + n1 * 2, 16);
+  cp->sm_run_head = off;    off = al(off + n1, 16);
+  cp->sm_run_pos = off;     off = al(off + n1 * 2, 16);
+  cp->sm_vhead = off;       off = al(off + n1, 16);
+  cp->sm_par = off;         off = al(off + n1 * 2, 16);
+  cp->sm_scratch = off;
+  const int gemm_scratch = al(wave * pl.spec * 4, 16) + kGemmCols * kGemmKC * 4;
+  const int tail_scratch = kWarps * d.r * 4;
+  off += gemm_scratch > tail_scratch ? gemm_scratch : tail_scratch;
+  cp->sm_total = off;
+  return off;
+}
+
+int chain_smem_bytes(const Plan &pl, int e_cap, int wave) {
+  ChainParams cp;
+  return chain_smem_layout(pl, e_cap, wave, &cp);
+}
+
+template <int WDT, int SLOTS>
+static const void *chain_fn() {
+  return reinterpret_cast<const void *>(&chain_kernel<WDT, SLOTS>);
+}
+
+const void *chain_kernel_ptr(int wdtype, int M) {
+  const int mp = M <= 32 ? 1 : M <= 64 ? 2 : M <= 128 ? 4 : 8;
+  if (wdtype == DT_BF16) {
+    switch (mp) {
+      case 1: return chain_fn<1, 1>();
+      case 2: return chain_fn<1, 2>();
+      case 4: return chain_fn<1, 4>();
+      default: return chain_fn<1, 8>();
+    }
+  }
+  switch (mp) {
+    case 1: return chain_fn<0, 1>();
+    case 2: return chain_fn<0, 2>();
+    case 4: return chain_fn<0, 4>();
+    default: return chain_fn<0, 8>();
+  }
+}
+
+cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStream_t st) {
+  const dt_dims &d = pl.dims;
+  char *w = static_cast<char *>(ws);
+  ChainParams cp;
+  chain_smem_layout(pl, pl.e_cap, pl.wave, &cp);
+  cp.V = d.V; cp.d = d.d; cp.d_s = d.d_s; cp.r = d.r; cp.D = d.D; cp.M = d.M; cp.k = d.k;
+  cp.N = d.N;
+  cp.nb = a.nb; cp.b0 = a.b0; cp.P = pl.spec; cp.e_cap = pl.e_cap;
+  cp.W_hh = a.w->W_hh; cp.W1 = a.w->W1; cp.W2 = a.w->W2; cp.b_hh = a.w->b_hh;
+  cp.G = a.G;
+  cp.state0 = a.state0; cp.anchor = a.anchor; cp.temperature = a.temperature;
+  cp.cand_id = reinterpret_cast<const int32_t *>(w + pl.off_cand_id);
+  cp.cand_val = reinterpret_cast<const float *>(w + pl.off_cand_val);
+  cp.U = reinterpret_cast<const float *>(w + pl.off_U);
+  cp.S_store = reinterpret_cast<float *>(w + pl.off_S);
+  cp.gh_store = reinterpret_cast<float *>(w + pl.off_gh);
+  cp.gin = reinterpret_cast<float *>(w + pl.off_gin);
+  cp.pbuf = reinterpret_cast<float *>(w + pl.off_p);
+  cp.colexp = reinterpret_cast<int *>(w + pl.off_colexp);
+  cp.col_count = cp.colexp + static_cast<size_t>(pl.wave) * pl.spec;
+  cp.ctrl = reinterpret_cast<Ctrl *>(w + pl.off_ctrl);
+  cp.req_flags = reinterpret_cast<const int *>(w + pl.off_ctrl + kCtrlHeader +
+                                               sizeof(unsigned) * static_cast<size_t>(d.batch) * d.D);
+  cp.tokens = a.out->tokens; cp.parents = a.out->parents; cp.depths = a.out->depths;
+  cp.scores = a.out->scores; cp.mask = a.out->mask; cp.status = a.out->status;
+  cp.limit_ns = 10000000000ull;  // 10 s per grid barrier wait
+  const void *fn = chain_kernel_ptr(pl.wdtype, d.M);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(pl.chain_smem));
+  if (e != cudaSuccess) return e;
+  // the barrier counters of the control block are re-zeroed for every wave
+  e = cudaMemsetAsync(cp.ctrl, 0, sizeof(Ctrl), st);
+  if (e != cudaSuccess) return e;
+  void *args[] = {&cp};
+  return cudaLaunchCooperativeKernel(fn, dim3(pl.chain_grid), dim3(kThreads), args,
+                                     pl.chain_smem, st);
+}
+
+}  // namespace dt

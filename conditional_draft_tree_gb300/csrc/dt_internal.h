@@ -1,0 +1,67 @@
+// dt_internal.h -- declarations shared by the translation units of libdt.so.
+// Host-side only: workspace layout, launch parameters and kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/dt.h"
+
+namespace dt {
+
+// Sizes and pointers of one dt_build_trees call, resolved on the host.
+struct Plan {
+  dt_dims dims;
+  int wdtype;          // DT_F32 / DT_BF16
+  int spec;            // speculative expansions per request and step (P)
+  int e_cap;           // expansion slots per request
+  int nsplit;          // top-M row segments
+  int num_sms;
+  int chain_grid;      // co-resident blocks of the search kernel
+  int wave;            // requests per search launch (<= chain_grid)
+  size_t chain_smem;   // dynamic shared memory of the search kernel
+  // workspace carve-up (byte offsets)
+  size_t off_ctrl, off_part, off_cand_id, off_cand_val, off_U, off_S, off_gh, off_gin, off_p,
+      off_colexp, off_end;
+};
+
+// Control block at the start of the workspace; zeroed by every call.
+struct Ctrl {
+  unsigned int bar_count;
+  unsigned int bar_gen;
+  int abort;           // set when a bounded wait expired
+  int active;          // requests of the current wave still searching
+  unsigned int pad[4];
+  // followed by: unsigned row_ticket[batch * D]; int req_flags[batch]; int col_count[batch]
+};
+
+constexpr int kCtrlHeader = sizeof(Ctrl);
+constexpr int kReqFlagNonfinite = 1;
+
+int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p);
+int validate_dims(const dt_dims *dims);
+
+// top-M over base logits -> candidate ids/values (+ optional user copy)
+cudaError_t launch_topm(const Plan &p, const float *base_logits, void *ws, int32_t *topm_out,
+                        cudaStream_t st);
+
+// C[m][n] = sum_k A[m][k] * B[n][k] (+ bias[n]); fp32 accumulation.
+// a_dtype/b_dtype: DT_F32 or DT_BF16.
+cudaError_t launch_gemm_nt(int M, int N, int K, const void *A, int a_dtype, size_t lda,
+                           const void *B, int b_dtype, size_t ldb, const float *bias, float *C,
+                           size_t ldc, cudaStream_t st);
+
+// The best-first search for requests [b0, b0 + nb).
+struct ChainArgs {
+  const dt_weights *w;
+  const float *G;            // prepared [V][3 d_s]
+  const float *state0;       // [batch][d_s]
+  const int32_t *anchor;     // [batch]
+  const float *temperature;  // [batch] or null
+  const dt_tree_out *out;
+  int b0, nb;
+};
+cudaError_t launch_chain(const Plan &p, const ChainArgs &a, void *ws, cudaStream_t st);
+
+}  // namespace dt

@@ -1,0 +1,171 @@
+/*
+ * dt.h -- C ABI of the GB300 (sm_103a) conditional draft-tree builder.
+ *
+ * One call of dt_build_trees() runs one drafting round of DominoTree for a batch
+ * of independent requests: per-depth top-M candidate selection over the base
+ * logits, then a best-first search whose node scores re-run the Domino GRU
+ * correction along each root-to-node path, then the emission of the tree and
+ * its ancestor attention mask.
+ *
+ * Sources (page title, section):
+ *  - "Riassunto Tecnico: DominoTree" (gist.science/it/paper/2607.08642),
+ *    Componenti Core 1 (best-first max-heap on cumulative path log-probability;
+ *    children scored by re-running the GRU correction along the node's path;
+ *    the backbone states H_i are shared and path independent), 2 (correction
+ *    restricted to the top-M marginal candidates of each depth, then top-k
+ *    children), 4 (fixed node budget), 5 (verification with an ancestor mask).
+ *  - "Domino：在投机解码中将因果建模与自回归草稿解耦" (paper.rainbus.top/paper/2605.29707),
+ *    core method (S_{i-1} = GRU(E_{<=i-1}); dL_i = W2 SiLU(W1 [H_i; S_{i-1}]);
+ *    L_i = L_base^i + dL_i) and method steps (draft block of size B anchored on
+ *    the last verified token; base logits for the B-1 future positions).
+ *
+ * Conventions used throughout:
+ *  - All pointers passed to dt_build_trees / dt_prepare_weights are DEVICE
+ *    pointers on the current CUDA device unless a comment says "host".
+ *  - Arrays are dense and row-major. Float tensors are IEEE fp32. Weights are
+ *    fp32 or bf16 (raw 16-bit patterns) as dt_weights.wdtype says.
+ *  - The caller owns every buffer. No entry point allocates or frees device
+ *    memory; scratch memory is the caller's `workspace`.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and is asynchronous. The host return value covers argument
+ *    validation and launch errors only; conditions found on the device are
+ *    written to out->status[b].
+ *  - Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef DT_H_
+#define DT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DT_ABI_VERSION 1
+
+/* ------------------------------------------------------------ status codes */
+#define DT_OK 0
+#define DT_ERR_INVALID_ARG (-1)   /* bad size, null pointer, misalignment, limit exceeded */
+#define DT_ERR_UNSUPPORTED (-2)   /* no sm_103a device, or a shape beyond this build's kernels */
+#define DT_ERR_CUDA (-3)          /* a CUDA runtime call or kernel launch failed */
+#define DT_ERR_NONFINITE (-4)     /* device: a base logit of the request is NaN or +inf */
+#define DT_ERR_TIMEOUT (-5)       /* device: a bounded inter-block wait expired; request output invalid */
+#define DT_ERR_BAD_TEMPERATURE (-6) /* device: temperature < 0 or not finite */
+
+/* Hard limits of this build (checked by every entry point). */
+#define DT_MAX_M 256        /* candidates per depth */
+#define DT_MAX_K 32         /* children per node */
+#define DT_MAX_D 64         /* draft depths (block size - 1) */
+#define DT_MAX_N 1024       /* node budget (non-root nodes) */
+#define DT_MAX_DS 4096      /* GRU state width */
+#define DT_MAX_R 1024       /* correction rank */
+#define DT_MAX_SPEC 16      /* speculative expansions per request and step */
+
+typedef enum { DT_F32 = 0, DT_BF16 = 1 } dt_dtype;
+
+/* Problem sizes. Notation of the pages: V vocabulary, d backbone hidden size,
+ * d_s GRU state size, r correction rank, D = B - 1 draft depths, M candidates per
+ * depth, k children per expanded node, N node budget (non-root nodes). */
+typedef struct {
+  int V, d, d_s, r, D, M, k, N;
+  int batch;          /* requests per call (>= 1) */
+} dt_dims;
+
+/* Domino head weights (device, read-only). Layouts:
+ *   E    [V][d]          token embedding (the GRU input)
+ *   W_ih [3 d_s][d]      GRU input weights, row blocks ordered r, z, n
+ *   W_hh [3 d_s][d_s]    GRU recurrent weights, row blocks ordered r, z, n
+ *   b_ih, b_hh [3 d_s]   fp32 GRU biases, or NULL for zero
+ *   W1   [r][d + d_s]    columns 0..d-1 act on H_i, columns d.. on the GRU state
+ *   W2   [V][r]          correction output rows (gathered for the M candidates)
+ * Every pointer must be 16-byte aligned. */
+typedef struct {
+  const void *E, *W_ih, *W_hh;
+  const float *b_ih, *b_hh;
+  const void *W1, *W2;
+  dt_dtype wdtype;
+} dt_weights;
+
+/* Per-request outputs (device, caller-owned). Row 0 of each tree is the root
+ * (anchor token, parent -1, depth 0, score 0). Rows 1..N are nodes in best-first
+ * pop order, so parents[i] < i and scores never increase with i. Rows after the
+ * last node (when the candidate tree has fewer than N nodes) hold token, parent
+ * and depth -1 and score -inf. */
+typedef struct {
+  int32_t *tokens;    /* [batch][N+1] */
+  int32_t *parents;   /* [batch][N+1] */
+  int32_t *depths;    /* [batch][N+1] */
+  float *scores;      /* [batch][N+1] cumulative path log-probability */
+  uint8_t *mask;      /* [batch][N+1][N+1]: mask[i][j] = 1 iff j is i or an ancestor of i; or NULL */
+  int32_t *topm;      /* [batch][D][M]: candidate ids of each depth, (logit desc, id asc); or NULL */
+  int32_t *status;    /* [batch]: DT_OK or a device-side DT_ERR_* code; required */
+} dt_tree_out;
+
+/* Optional tuning and instrumentation (may be NULL in every call). */
+typedef struct {
+  int spec_width;     /* speculative expansions per request and step, 1..DT_MAX_SPEC;
+                         0 = library default. Any value yields the same trees. */
+  void **phase_events;/* NULL, or DT_NUM_PHASE_EVENTS cudaEvent_t handles recorded on
+                         the stream at phase boundaries (for timing) */
+} dt_options;
+
+#define DT_NUM_PHASE_EVENTS 4 /* start, after top-M + projections, after the search, end */
+
+/* Bytes of the prepared-weights buffer for `dims`: the GRU input projection of
+ * every vocabulary row, G[v] = W_ih E[v] + b_ih, as fp32 [V][3 d_s]. */
+size_t dt_prepared_bytes(const dt_dims *dims);
+
+/* Fill `prepared` (device, dt_prepared_bytes() bytes, 256-byte aligned) from the
+ * weights. Run once per set of weights; every later dt_build_trees call with the
+ * same weights reads it. The GRU gate input W_ih E[tok] depends only on the
+ * weights, so computing it for the whole vocabulary once replaces a 3 d_s x d
+ * mat-vec per tree node by a 3 d_s row gather. Returns a DT_ status. */
+int dt_prepare_weights(const dt_dims *dims, const dt_weights *w, void *prepared,
+                       size_t prepared_bytes, void *stream);
+
+/* Scratch bytes dt_build_trees needs for `dims` and `opt` (may be NULL). */
+size_t dt_workspace_bytes(const dt_dims *dims, const dt_options *opt);
+
+/* Build one round of draft trees for dims->batch requests.
+ *   base_logits [batch][D][V] fp32  base logits L_base^j of depths j = 1..D
+ *   H           [batch][D][d] fp32  backbone states H_j of depths 1..D
+ *   state0      [batch][d_s]  fp32  initial GRU state (zeros in the pages' setting)
+ *   anchor_tok  [batch]       int32 last verified token x_t, in [0, V)
+ *   temperature [batch]       fp32  per request; NULL = 1.0; 0.0 reads as 1.0
+ *                                   (greedy ordering); < 0 or non-finite gives
+ *                                   DT_ERR_BAD_TEMPERATURE for that request
+ *   prepared    dt_prepare_weights() output for the same weights
+ *   workspace   dt_workspace_bytes() bytes, 256-byte aligned, not shared by
+ *               overlapping calls
+ * Float inputs must be 16-byte aligned when their row length is a multiple of 4
+ * floats. Returns DT_OK when the work was enqueued. */
+int dt_build_trees(const dt_dims *dims, const dt_weights *w, const void *prepared,
+                   const float *base_logits, const float *H, const float *state0,
+                   const int32_t *anchor_tok, const float *temperature,
+                   void *workspace, size_t workspace_bytes, const dt_tree_out *out,
+                   const dt_options *opt, void *stream);
+
+/* Same as dt_build_trees, but the per-round inputs and outputs are HOST buffers
+ * (pinned memory gives asynchronous copies). The call copies the inputs into
+ * the workspace, builds the trees and copies the outputs back, all on `stream`;
+ * synchronise the stream before reading the outputs. The workspace must be
+ * dt_host_workspace_bytes() bytes. The weights and `prepared` stay on the device.
+ * Host output pointers follow dt_tree_out (mask and topm may be NULL). */
+size_t dt_host_workspace_bytes(const dt_dims *dims, const dt_options *opt);
+int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *prepared,
+                        const float *base_logits, const float *H, const float *state0,
+                        const int32_t *anchor_tok, const float *temperature,
+                        void *workspace, size_t workspace_bytes, const dt_tree_out *host_out,
+                        const dt_options *opt, void *stream);
+
+/* Static description of a status code. */
+const char *dt_status_string(int code);
+
+/* DT_ABI_VERSION of the loaded library. */
+int dt_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DT_H_ */

@@ -1,0 +1,81 @@
+"""The C-ABI library builds, loads and exports every symbol include/dt.h declares.
+
+CPU only: no call here launches device work. Argument validation happens before
+any device access, so invalid shapes are rejected without a GPU.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def dt():
+    from conditional_draft_tree_gb300 import build
+    build.build()
+    import conditional_draft_tree_gb300 as dt
+    return dt
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(dt_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_expected_entry_points(dt):
+    assert declared_functions() == sorted(dt.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(dt):
+    lib = C.CDLL(dt.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_host_only_calls(dt):
+    assert dt.abi_version() == 1
+    assert dt.status_string(dt.OK) == "ok"
+    assert "NaN" in dt.status_string(dt.ERR_NONFINITE)
+    dims = dt.dims_of(V=151936, d=4096, d_s=1024, r=256, D=15, M=64, k=8, N=64, batch=32)
+    assert dt.prepared_bytes(dims) == 4 * 151936 * 3 * 1024
+
+
+@pytest.mark.parametrize("bad", [dict(k=9, M=8), dict(M=300), dict(d=12), dict(d_s=0),
+                                 dict(r=7), dict(D=0), dict(N=-1), dict(batch=0), dict(M=2000, V=1000)])
+def test_invalid_dims_rejected_before_device_work(dt, bad):
+    base = dict(V=1024, d=64, d_s=32, r=32, D=7, M=16, k=4, N=32, batch=1)
+    base.update(bad)
+    dims = dt.dims_of(**base)
+    assert dt.prepared_bytes(dims) == 0
+    w = dt.DtWeights(16, 16, 16, None, None, 16, 16, 0)
+    out = dt.DtTreeOut(16, 16, 16, 16, None, None, 16)
+    rc = dt.lib().dt_build_trees(C.byref(dims), C.byref(w), 256, 256, 256, 256, 256, None, 256,
+                                 1 << 20, C.byref(out), None, None)
+    assert rc == dt.ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers_rejected(dt):
+    dims = dt.dims_of(V=1024, d=64, d_s=32, r=32, D=7, M=16, k=4, N=32, batch=1)
+    out = dt.DtTreeOut(16, 16, 16, 16, None, None, 16)
+    w_null = dt.DtWeights(None, 16, 16, None, None, 16, 16, 0)
+    assert dt.lib().dt_build_trees(C.byref(dims), C.byref(w_null), 256, 256, 256, 256, 256, None,
+                                   256, 1 << 20, C.byref(out), None, None) == dt.ERR_INVALID_ARG
+    w_mis = dt.DtWeights(18, 16, 16, None, None, 16, 16, 0)
+    assert dt.lib().dt_build_trees(C.byref(dims), C.byref(w_mis), 256, 256, 256, 256, 256, None,
+                                   256, 1 << 20, C.byref(out), None, None) == dt.ERR_INVALID_ARG
+    w = dt.DtWeights(16, 16, 16, None, None, 16, 16, 0)
+    assert dt.lib().dt_build_trees(C.byref(dims), C.byref(w), 256, 256, 256, 256, 256, None,
+                                   255, 1 << 20, C.byref(out), None, None) == dt.ERR_INVALID_ARG
+
+
+def test_package_refuses_to_run_without_library(dt, monkeypatch, tmp_path):
+    monkeypatch.setattr(dt, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(dt, "_lib", None)
+    with pytest.raises(dt.DtError):
+        dt.lib()

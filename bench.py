@@ -1,0 +1,327 @@
+#!/usr/bin/env python
+"""Benchmark of one conditional draft-tree building round (DominoTree).
+
+Metric: draft trees built per second (whole job) and ms per round, on the
+Qwen3-8B-shaped serving batch: 32 independent requests, V = 151936, d = 4096,
+d_s = 1024, r = 256, B = 16 (D = 15), M = 64, k = 8, node budget N = 64.
+Inputs are seeded synthetic tensors of those shapes (dt_workloads).
+
+A step is one dt_build_trees call: top-M over the base logits, the per-depth
+projection and the conditional best-first search with tree and mask emission,
+from device-resident inputs to device-resident outputs. The prepared weight
+table (dt_prepare_weights) is built once, before timing, like any weight
+layout transform; its time is reported as config.prepare_ms.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch with torch.distributed.run; every rank builds its own batch of
+32 requests (replicas, weak scaling; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft trees built/sec and µs per tree-build round (Qwen3-8B shape, batch 32)"
+UNIT = "trees/s"
+CFG = 3
+L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2
+FFMA_LANES_PER_SM = 128
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--spec", type=int, default=0, help="speculative expansions per step (0=default)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), sm_max_mhz=float(d.get("sm_max_mhz", 2070.0)),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, sm_max_mhz=2070.0, source="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(wl, reqs, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.build_trees(wl, reqs, threads=threads, mask=True, topm_out=False)
+    return time.perf_counter() - t0
+
+
+def algorithmic_counts(wl, out_tokens, out_depths):
+    """Per-round algorithmic bytes of each phase and useful GEMM flops of the
+    search, from the trees actually built (expansions = root + popped nodes
+    below depth D that are not the N-th pop)."""
+    import numpy as np
+    B, D, V, d, ds, r, M, N = wl.batch, wl.D, wl.V, wl.d, wl.d_s, wl.r, wl.M, wl.N
+    w = 2 if wl.wdtype == "bf16" else 4
+    topm_bytes = B * D * V * 4 + B * D * M * 8
+    proj_bytes = B * D * d * 4 + r * d * w + B * D * r * 4
+    proj_flops = 2 * B * D * r * d
+    n_exp = 0
+    depths_touched = 0
+    for b in range(B):
+        dep = out_depths[b]
+        n = int((out_tokens[b] >= 0).sum())
+        idx = np.arange(n)
+        exp_nodes = 1 + int(((dep[1:n] < D) & (idx[1:] < N)).sum())
+        n_exp += exp_nodes
+        depths_touched += len(set((dep[:n][(dep[:n] < D) & (idx < N)] + 1).tolist()))
+    search_bytes = ((3 * ds * ds + r * ds) * w + n_exp * 3 * ds * 4
+                    + depths_touched * (M * r * w + r * 4 + M * 8)
+                    + B * (N + 1) * (16 + N + 1))
+    search_flops = n_exp * 2 * (3 * ds + r) * ds
+    return dict(topm_bytes=topm_bytes, proj_bytes=proj_bytes, proj_flops=proj_flops,
+                search_bytes=search_bytes, search_flops=search_flops, expansions=n_exp)
+
+
+def run_reference(args, rank):
+    """The oracle, as it stands, on the host cores: each step a bounded sample."""
+    if rank != 0:
+        return
+    import dt_workloads as W
+    wl = W.make_workload(CFG)
+    cores = os.cpu_count() or 1
+    reqs = list(range(min(wl.batch, cores)))
+    for _ in range(args.warmup):
+        oracle_sample(wl, reqs[:1], 1)
+    total = sum(oracle_sample(wl, reqs, cores) for _ in range(args.steps))
+    value = len(reqs) * args.steps / total
+    sample = f"{len(reqs)} of the 32 requests per step, {cores} threads, warm-up {args.warmup} single requests"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "qwen3-8b-b32: V=151936 d=4096 d_s=1024 r=256 D=15 M=64 k=8 N=64 batch=32",
+                       "parallelism": "oracle on host cores"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import conditional_draft_tree_gb300 as dt
+    import dt_workloads as W
+    from conditional_draft_tree_gb300 import build as dtbuild
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        dtbuild.build()
+    if world > 1:
+        dist.barrier()
+    wl = W.make_workload(CFG)
+    dev = torch.device("cuda", local)
+
+    t0 = time.perf_counter()
+    tb = dt.TreeBuilder.from_numpy(wl, spec_width=args.spec, device=dev)
+    torch.cuda.synchronize()
+    prep = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    prep[0].record()
+    dt.prepare_weights(tb.dims, tb.w, tb.prepared)
+    prep[1].record()
+    torch.cuda.synchronize()
+    prepare_ms = prep[0].elapsed_time(prep[1])
+    inp = tb.inputs_to_device(wl)
+    out = dt.alloc_outputs(tb.dims, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    K, Wm = args.steps, max(3, args.warmup)
+    st = torch.cuda.current_stream()
+
+    ph = [[torch.cuda.Event(enable_timing=True) for _ in range(dt.NUM_PHASE_EVENTS)]
+          for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for _ in range(Wm):
+        flush.fill_(1)
+        tb.run(**inp, out=out)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk = Clocks(local)
+    clk.start()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xff)                       # L2 flush outside the timed interval
+        tb.run(**inp, out=out, opt=dt.options(args.spec, ph[i]))
+        ends[i].record(st)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = clk.stop()
+    per = [ph[i][0].elapsed_time(ph[i][3]) for i in range(K)]
+    topm_ms = [ph[i][0].elapsed_time(ph[i][1]) for i in range(K)]
+    proj_ms = [ph[i][1].elapsed_time(ph[i][2]) for i in range(K)]
+    search_ms = [ph[i][2].elapsed_time(ph[i][3]) for i in range(K)]
+    total_ms = sum(per)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    value = world * wl.batch * K / (total_ms / 1000.0)
+
+    # end to end through the host-buffer entry point: pinned inputs in, results out
+    host_ws = torch.empty(dt.host_workspace_bytes(tb.dims, tb.opt), dtype=torch.uint8, device=dev)
+    pin = lambda a, tt: torch.from_numpy(np.ascontiguousarray(a, dtype=tt)).pin_memory()
+    hin = dict(base_logits=pin(wl.base_logits, np.float32), H=pin(wl.H, np.float32),
+               state0=pin(wl.state0, np.float32), anchor_tok=pin(wl.anchor, np.int32),
+               temperature=pin(wl.temperature, np.float32))
+    hout = dt.alloc_outputs(tb.dims, "cpu", pin=True)
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = sum(v.numel() * v.element_size() for v in hout.values() if v is not None)
+
+    def e2e_step():
+        dt.build_trees_host(tb.dims, tb.w, tb.prepared, hin["base_logits"], hin["H"],
+                            hin["state0"], hin["anchor_tok"], hin["temperature"], host_ws, hout,
+                            tb.opt)
+    for _ in range(Wm):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = 0.0
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(K):
+        flush.fill_(i & 0xff)
+        ea.record(st)
+        e2e_step()
+        eb.record(st)
+        eb.synchronize()
+        e_ms += ea.elapsed_time(eb)
+    te = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = world * wl.batch * K / (float(te.item()) / 1000.0)
+    ok_e2e = bool((hout["status"] == 0).all())
+
+    if rank == 0:
+        o = {k: v.cpu().numpy() for k, v in out.items() if v is not None}
+        cnt = algorithmic_counts(wl, o["tokens"], o["depths"])
+        pk = peaks()
+        props = torch.cuda.get_device_properties(dev)
+        sms = props.multi_processor_count
+        ffma_tflops = sms * FFMA_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+        phases = {"topm": statistics.mean(topm_ms), "projection": statistics.mean(proj_ms),
+                  "search": statistics.mean(search_ms)}
+        dominant = max(phases, key=phases.get)
+        if dominant == "topm":
+            ach = cnt["topm_bytes"] / (phases["topm"] * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / pk["hbm_gbs"], "traffic": None, "kernel": "dt::topm_kernel"}
+        else:
+            key = "search" if dominant == "search" else "proj"
+            fl = cnt["search_flops"] if key == "search" else cnt["proj_flops"]
+            ach = fl / (phases[dominant] * 1e-3) / 1e12
+            roof = {"bound": "alu", "achieved": ach, "peak": ffma_tflops, "unit": "TFLOP/s",
+                    "frac": ach / ffma_tflops, "traffic": None,
+                    "kernel": "dt::chain_kernel" if key == "search" else "dt::gemm_nt_kernel"}
+        round_bytes = cnt["topm_bytes"] + cnt["proj_bytes"] + cnt["search_bytes"]
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": Wm, "ms_per_step": total_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "qwen3-8b-b32: V=151936 d=4096 d_s=1024 r=256 D=15 M=64 k=8 N=64 batch=32",
+                       "us_per_round": 1000.0 * total_ms / K, "global_batch": world * wl.batch,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed (256 MB write) before every timed round",
+                       "spec_width": tb.opt.spec_width or 8, "prepare_ms": prepare_ms,
+                       "phases_ms": phases, "expansions_per_round": cnt["expansions"],
+                       "round_algorithmic_bytes": round_bytes,
+                       "round_hbm_frac": round_bytes / (total_ms / K * 1e-3) / 1e9 / pk["hbm_gbs"],
+                       "peaks": pk["source"], "wall_s": wall},
+            "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ok": ok_e2e},
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            cores = os.cpu_count() or 1
+            reqs = list(range(wl.batch))
+            secs = oracle_sample(wl, reqs, cores)
+            line["cpu_baseline"] = {"value": len(reqs) / secs, "unit": UNIT, "cores": cores,
+                                    "kind": "oracle",
+                                    "sample": f"all {len(reqs)} requests of one round, {cores} threads"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -165,11 +165,13 @@ int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const f
   if (cudaMemsetAsync(wsb + pl.off_ctrl, 0, pl.off_part - pl.off_ctrl, st) != cudaSuccess)
     return DT_ERR_CUDA;
   if (dt::launch_topm(pl, base_logits, ws, out->topm, st) != cudaSuccess) return DT_ERR_CUDA;
+  rc = record(opt, 1, st);
+  if (rc) return rc;
   float *U = reinterpret_cast<float *>(wsb + pl.off_U);
   if (dt::launch_gemm_nt(d.batch * d.D, d.r, d.d, H, DT_F32, d.d, w->W1, w->wdtype,
                          static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r, st) != cudaSuccess)
     return DT_ERR_CUDA;
-  rc = record(opt, 1, st);
+  rc = record(opt, 2, st);
   if (rc) return rc;
   dt::ChainArgs a;
   a.w = w;
@@ -183,8 +185,6 @@ int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const f
     a.nb = (d.batch - b0) < pl.wave ? (d.batch - b0) : pl.wave;
     if (dt::launch_chain(pl, a, ws, st) != cudaSuccess) return DT_ERR_CUDA;
   }
-  rc = record(opt, 2, st);
-  if (rc) return rc;
   return record(opt, 3, st);
 }
 

@@ -110,7 +110,7 @@ typedef struct {
                          the stream at phase boundaries (for timing) */
 } dt_options;
 
-#define DT_NUM_PHASE_EVENTS 4 /* start, after top-M + projections, after the search, end */
+#define DT_NUM_PHASE_EVENTS 4 /* start, after top-M, after the projection, after the search */
 
 /* Bytes of the prepared-weights buffer for `dims`: the GRU input projection of
  * every vocabulary row, G[v] = W_ih E[v] + b_ih, as fp32 [V][3 d_s]. */

@@ -206,6 +206,9 @@ def main():
 
     ph = [[torch.cuda.Event(enable_timing=True) for _ in range(dt.NUM_PHASE_EVENTS)]
           for _ in range(K)]
+    for evs in ph:            # torch creates the CUDA event at its first record
+        for e in evs:
+            e.record(st)
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     for _ in range(Wm):
         flush.fill_(1)

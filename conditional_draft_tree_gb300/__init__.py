@@ -26,7 +26,8 @@ MAX_SPEC = 16
 # every symbol include/dt.h declares
 EXPORTS = ("dt_abi_version", "dt_status_string", "dt_prepared_bytes", "dt_prepare_weights",
            "dt_workspace_bytes", "dt_build_trees", "dt_host_workspace_bytes",
-           "dt_build_trees_host")
+           "dt_build_trees_host", "dt_select_topm_noalloc")
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class DtDims(C.Structure):
@@ -78,6 +79,8 @@ def lib():
                C.POINTER(DtTreeOut), C.POINTER(DtOptions), C.c_void_p]
         L.dt_build_trees.argtypes = sig
         L.dt_build_trees_host.argtypes = sig
+        L.dt_select_topm_noalloc.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
+                                             C.c_void_p, C.c_void_p, C.c_void_p]
         _lib = L
     return _lib
 
@@ -202,6 +205,16 @@ def build_trees_host(dims: DtDims, w: DeviceWeights, prepared, base_logits, H, s
                                      workspace.numel() * workspace.element_size(), C.byref(o),
                                      C.byref(opt) if opt else None, _stream(stream)),
            "dt_build_trees_host")
+
+
+def select_topm_noalloc(base_logits, M: int, topm, status, stream=None) -> int:
+    """dt_select_topm_noalloc on device tensors: base_logits [batch][D][V] fp32,
+    topm [batch][D][M] int32 and status [batch] int32 outputs. Allocates no
+    device memory (the library's static scratch is used; see include/dt.h).
+    Returns the C status code."""
+    batch, D, V = base_logits.shape
+    return lib().dt_select_topm_noalloc(_ptr(base_logits), batch, D, V, int(M), _ptr(topm),
+                                        _ptr(status), _stream(stream))
 
 
 class TreeBuilder:

@@ -254,6 +254,34 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
 
 }  // namespace
 
+// The same kernel on explicit scratch pointers (used by the allocation-free
+// entry point, whose scratch is a static device array).
+cudaError_t launch_topm_raw(const float *base_logits, int batch, int D, int V, int M, int nsplit,
+                            uint64_t *partial, unsigned *ticket, int *req_flags, int32_t *cand_id,
+                            float *cand_val, int32_t *topm_out, cudaStream_t st) {
+  dim3 grid(nsplit, batch * D);
+  const int mp = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  switch (mp) {
+    case 32:
+      topm_kernel<1><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, partial, ticket,
+                                                   req_flags, cand_id, cand_val, topm_out);
+      break;
+    case 64:
+      topm_kernel<2><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, partial, ticket,
+                                                   req_flags, cand_id, cand_val, topm_out);
+      break;
+    case 128:
+      topm_kernel<4><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, partial, ticket,
+                                                   req_flags, cand_id, cand_val, topm_out);
+      break;
+    default:
+      topm_kernel<8><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, partial, ticket,
+                                                   req_flags, cand_id, cand_val, topm_out);
+      break;
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topm(const Plan &p, const float *base_logits, void *ws, int32_t *topm_out,
                         cudaStream_t st) {
   char *w = static_cast<char *>(ws);

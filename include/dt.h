@@ -159,6 +159,32 @@ int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *pr
                         void *workspace, size_t workspace_bytes, const dt_tree_out *host_out,
                         const dt_options *opt, void *stream);
 
+/* Allocation-free top-M selection (the pages have no counterpart: this entry
+ * point exists for callers of this library that may not allocate device memory,
+ * such as a serving runtime whose device memory is entirely pre-reserved for its
+ * own pool, a latency-critical loop that cannot afford cudaMalloc's implicit
+ * device synchronisation, or a plug-in running inside a host framework that
+ * owns every device allocation).
+ *
+ * Computes what dt_build_trees writes to out->topm: for every request b and
+ * depth j, the M token ids of base_logits[b][j][:] with the largest values,
+ * ordered by (value desc, id asc); status[b] = DT_OK or DT_ERR_NONFINITE (a
+ * NaN or +inf logit; the ids of that request are then unspecified).
+ *   base_logits [batch][D][V] fp32 device (16-byte aligned when V % 4 == 0)
+ *   topm        [batch][D][M] int32 device output
+ *   status      [batch]       int32 device output
+ * No memory is allocated: the scratch is a static device array of
+ * DT_NOALLOC_SCRATCH_BYTES bytes that every device loading the library holds
+ * until the process exits. A call needs about batch*D*(4*M + 4) bytes of it
+ * (plus 8*M bytes per extra row segment, which the call drops first when short
+ * of room); shapes that do not fit return DT_ERR_INVALID_ARG. The first call on
+ * a device resolves the array's address (cudaGetSymbolAddress) with that device
+ * current; make it before any stream capture. All calls share the array, so
+ * calls that overlap on the GPU race; serialise them. Asynchronous on `stream`. */
+#define DT_NOALLOC_SCRATCH_BYTES (8u << 20)
+int dt_select_topm_noalloc(const float *base_logits, int batch, int D, int V, int M,
+                           int32_t *topm, int32_t *status, void *stream);
+
 /* Static description of a status code. */
 const char *dt_status_string(int code);
 

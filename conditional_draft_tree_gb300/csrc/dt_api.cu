@@ -77,17 +77,40 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   if (by_util > ns) ns = by_util < by_min ? by_util : (by_min > ns ? by_min : ns);
   p->nsplit = static_cast<int>(ns < 1 ? 1 : ns);
 
+  // search GEMM on the tensor cores when the weights are bf16: 128-row tiles of
+  // [W_hh; W1_S] times K chunks, one (tile, chunk) per block, at most one block
+  // per SM and at most 512 K columns per chunk
+  p->umma = 0;
+  if (wdtype == DT_BF16) {
+    const int R = 3 * d.d_s + d.r;
+    const int n_mt = (R + 127) / 128;
+    int ks = p->num_sms / n_mt;
+    if (ks >= 1) {
+      int kc = ((d.d_s + ks - 1) / ks + 15) / 16 * 16;
+      ks = (d.d_s + kc - 1) / kc;
+      if (kc <= 512 && n_mt * ks <= p->num_sms) {
+        p->umma = 1;
+        p->n_mt = n_mt;
+        p->ks = ks;
+        p->kc = kc;
+      }
+    }
+  }
   // search kernel: expansion slots, shared memory and co-resident grid
   const void *fn = chain_kernel_ptr(wdtype, d.M);
   int wave = d.batch < 256 ? d.batch : 256;
   if (wave > p->num_sms) wave = p->num_sms;
+  // the opt-in limit covers static + dynamic shared memory of a block
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return DT_ERR_CUDA;
+  const int smem_max = smem_optin - static_cast<int>(fa.sharedSizeBytes);
   int e_cap = d.N + 1 + (p->spec > 1 ? d.N + 1 : 0);
   int smem = chain_smem_bytes(*p, e_cap, wave);
-  while (smem > smem_optin && e_cap > d.N + 1) {
+  while (smem > smem_max && e_cap > d.N + 1) {
     e_cap = d.N + 1 + (e_cap - d.N - 1) / 2;
     smem = chain_smem_bytes(*p, e_cap, wave);
   }
-  if (smem > smem_optin) return DT_ERR_UNSUPPORTED;
+  if (smem > smem_max) return DT_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return DT_ERR_CUDA;
   int per_sm = 0;
@@ -100,10 +123,19 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   p->e_cap = e_cap;
   p->chain_smem = static_cast<size_t>(smem);
 
+  // projection GEMM: split K until about two blocks per SM
+  {
+    const int tiles = gemm_tiles(static_cast<int>(rows), d.r);
+    int ks = (2 * p->num_sms + tiles - 1) / tiles;
+    const int kmax = (d.d + 15) / 16;
+    p->proj_ksplit = ks < 1 ? 1 : (ks > 16 ? 16 : (ks > kmax ? kmax : ks));
+  }
   // workspace carve-up
   size_t off = 0;
   p->off_ctrl = off;
-  off = al(off + kCtrlHeader + sizeof(unsigned) * rows + sizeof(int) * d.batch);
+  p->off_gemm_tickets = kCtrlHeader + sizeof(unsigned) * rows + sizeof(int) * d.batch;
+  off = al(off + p->off_gemm_tickets +
+           sizeof(unsigned) * gemm_tiles(static_cast<int>(rows), d.r));
   p->off_part = off;
   off = al(off + (p->nsplit > 1 ? sizeof(uint64_t) * rows * p->nsplit * d.M : 0));
   p->off_cand_id = off;   off = al(off + sizeof(int32_t) * rows * d.M);
@@ -116,6 +148,12 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   p->off_gin = off;       off = al(off + sizeof(float) * cols * d.d_s);
   p->off_p = off;         off = al(off + sizeof(float) * cols * d.r);
   p->off_colexp = off;    off = al(off + sizeof(int) * (cols + wave));
+  p->off_upart = off;
+  off = al(off + (p->proj_ksplit > 1 ? sizeof(float) * p->proj_ksplit * rows * d.r : 0));
+  p->off_partial = off;
+  off = al(off + (p->umma ? sizeof(float) * p->ks * cols * (3 * d.d_s + d.r) : 0));
+  p->off_gin16 = off;
+  off = al(off + (p->umma ? sizeof(uint16_t) * cols * 3 * d.d_s : 0));
   p->off_end = off;
   return DT_OK;
 }
@@ -169,7 +207,10 @@ int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const f
   if (rc) return rc;
   float *U = reinterpret_cast<float *>(wsb + pl.off_U);
   if (dt::launch_gemm_nt(d.batch * d.D, d.r, d.d, H, DT_F32, d.d, w->W1, w->wdtype,
-                         static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r, st) != cudaSuccess)
+                         static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r, pl.proj_ksplit,
+                         reinterpret_cast<float *>(wsb + pl.off_upart),
+                         reinterpret_cast<unsigned *>(wsb + pl.off_ctrl + pl.off_gemm_tickets),
+                         st) != cudaSuccess)
     return DT_ERR_CUDA;
   rc = record(opt, 2, st);
   if (rc) return rc;
@@ -251,7 +292,8 @@ int dt_prepare_weights(const dt_dims *dims, const dt_weights *w, void *prepared,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dt::launch_gemm_nt(dims->V, 3 * dims->d_s, dims->d, w->E, w->wdtype, dims->d, w->W_ih,
                          w->wdtype, dims->d, w->b_ih, static_cast<float *>(prepared),
-                         3 * static_cast<size_t>(dims->d_s), st) != cudaSuccess)
+                         3 * static_cast<size_t>(dims->d_s), 1, nullptr, nullptr,
+                         st) != cudaSuccess)
     return DT_ERR_CUDA;
   return DT_OK;
 }

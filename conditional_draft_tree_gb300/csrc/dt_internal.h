@@ -17,13 +17,17 @@ struct Plan {
   int spec;            // speculative expansions per request and step (P)
   int e_cap;           // expansion slots per request
   int nsplit;          // top-M row segments
+  int proj_ksplit;     // K split of the projection GEMM
+  int umma;            // search GEMM on tcgen05 (bf16 weights)
+  int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
   int num_sms;
   int chain_grid;      // co-resident blocks of the search kernel
   int wave;            // requests per search launch (<= chain_grid)
   size_t chain_smem;   // dynamic shared memory of the search kernel
   // workspace carve-up (byte offsets)
   size_t off_ctrl, off_part, off_cand_id, off_cand_val, off_U, off_S, off_gh, off_gin, off_p,
-      off_colexp, off_end;
+      off_colexp, off_upart, off_partial, off_gin16, off_end;
+  size_t off_gemm_tickets;  // inside the control region
 };
 
 // Control block at the start of the workspace; zeroed by every call.
@@ -32,8 +36,13 @@ struct Ctrl {
   unsigned int bar_gen;
   int abort;           // set when a bounded wait expired
   int active;          // requests of the current wave still searching
-  unsigned int pad[4];
-  // followed by: unsigned row_ticket[batch * D]; int req_flags[batch]; int col_count[batch]
+  unsigned int steps;      // lockstep steps of the last search launch
+  unsigned int expansions; // expansions of the last search launch
+  unsigned int pad[2];
+  // block 0 of the last search launch: ns spent in GEMM, barrier, reduction,
+  // barrier, tail, barrier (summed over steps)
+  unsigned long long t_ns[6];
+  // followed by: unsigned row_ticket[batch * D]; int req_flags[batch]; gemm tickets
 };
 
 constexpr int kCtrlHeader = sizeof(Ctrl);
@@ -48,9 +57,13 @@ cudaError_t launch_topm(const Plan &p, const float *base_logits, void *ws, int32
 
 // C[m][n] = sum_k A[m][k] * B[n][k] (+ bias[n]); fp32 accumulation.
 // a_dtype/b_dtype: DT_F32 or DT_BF16.
+// ksplit > 1 splits K over blockIdx.z; partial: ksplit*M*N floats, tickets:
+// gemm_tiles(M, N) zeroed counters (left zeroed on return).
 cudaError_t launch_gemm_nt(int M, int N, int K, const void *A, int a_dtype, size_t lda,
                            const void *B, int b_dtype, size_t ldb, const float *bias, float *C,
-                           size_t ldc, cudaStream_t st);
+                           size_t ldc, int ksplit, float *partial, unsigned *tickets,
+                           cudaStream_t st);
+int gemm_tiles(int M, int N);
 
 // The best-first search for requests [b0, b0 + nb).
 struct ChainArgs {

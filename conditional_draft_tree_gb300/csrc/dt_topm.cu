@@ -24,6 +24,8 @@ namespace {
 
 constexpr int kTopmThreads = 256;
 constexpr int kTopmWarps = kTopmThreads / 32;
+constexpr int kQ = 4;                          // float4 loads per lane per iteration
+constexpr int kBuf = 32 + 4 * 32;              // per-warp candidate buffer (keys)
 
 // Sorted (descending) list of 32*SLOTS keys spread over a warp: element
 // i = s*32 + lane lives in register v[s] of `lane`.
@@ -35,56 +37,46 @@ struct WarpList {
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) v[s] = 0;
   }
-  // element i (warp-uniform i)
+  // element i (warp-uniform i); every slot is shuffled so that no register is
+  // selected by a runtime index
   __device__ __forceinline__ uint64_t at(int i) const {
     uint64_t x = 0;
 #pragma unroll
-    for (int s = 0; s < SLOTS; ++s)
-      if (s == (i >> 5)) x = v[s];
-    return shfl64(x, i & 31);
+    for (int s = 0; s < SLOTS; ++s) {
+      const uint64_t y = shfl64(v[s], i & 31);
+      x = (s == (i >> 5)) ? y : x;
+    }
+    return x;
   }
-  // insert warp-uniform key c (unique), dropping the smallest element
-  __device__ __forceinline__ void insert(uint64_t c, int lane) {
-    int p = 0;
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) p += __popc(__ballot_sync(kFull, v[s] > c));
-    uint64_t carry = 0;
+  // compare-exchange of registers s and s + DS (lower index keeps the max)
+  template <int DS>
+  __device__ __forceinline__ void cmpx_slots() {
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
-      uint64_t up = shfl64_up(v[s], 1);
-      uint64_t last = shfl64(v[s], 31);
-      if (lane == 0) up = carry;
-      int i = s * 32 + lane;
-      v[s] = (i < p) ? v[s] : (i == p ? c : up);
-      carry = last;
+      if ((s & DS) == 0 && s + DS < SLOTS) {
+        const uint64_t a = v[s], b = v[s + DS];
+        v[s] = a > b ? a : b;
+        v[s + DS] = a > b ? b : a;
+      }
     }
   }
   // this <- top 32*SLOTS of (this U other), both sorted descending
   __device__ __forceinline__ void merge(const WarpList &o, int lane) {
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
-      uint64_t rev = shfl64(o.v[SLOTS - 1 - s], 31 - lane);
+      const uint64_t rev = shfl64(o.v[SLOTS - 1 - s], 31 - lane);
       v[s] = v[s] > rev ? v[s] : rev;  // bitonic sequence holding the top elements
     }
-#pragma unroll
-    for (int stride = SLOTS * 16; stride >= 32; stride >>= 1) {
-      const int ds = stride >> 5;
-#pragma unroll
-      for (int s = 0; s < SLOTS; ++s) {
-        if ((s & ds) == 0) {
-          uint64_t a = v[s], b = v[s + ds];
-          v[s] = a > b ? a : b;
-          v[s + ds] = a > b ? b : a;
-        }
-      }
-    }
+    if (SLOTS >= 8) cmpx_slots<4>();
+    if (SLOTS >= 4) cmpx_slots<2>();
+    if (SLOTS >= 2) cmpx_slots<1>();
 #pragma unroll
     for (int stride = 16; stride >= 1; stride >>= 1) {
 #pragma unroll
       for (int s = 0; s < SLOTS; ++s) {
-        uint64_t o2 = shfl64_xor(v[s], stride);
-        bool low = (lane & stride) == 0;
-        uint64_t mx = v[s] > o2 ? v[s] : o2, mn = v[s] > o2 ? o2 : v[s];
+        const uint64_t o2 = shfl64_xor(v[s], stride);
+        const bool low = (lane & stride) == 0;
+        const uint64_t mx = v[s] > o2 ? v[s] : o2, mn = v[s] > o2 ? o2 : v[s];
         v[s] = low ? mx : mn;
       }
     }
@@ -105,33 +97,85 @@ struct WarpList {
   }
 };
 
+// Descending bitonic sort of one key per lane.
+__device__ __forceinline__ uint64_t sort32_desc(uint64_t v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride >= 1; stride >>= 1) {
+      const uint64_t o = shfl64_xor(v, stride);
+      const bool desc = (lane & size) == 0 || size == 32;
+      const bool low = (lane & stride) == 0;
+      const uint64_t mx = v > o ? v : o, mn = v > o ? o : v;
+      v = (low == desc) ? mx : mn;
+    }
+  }
+  return v;
+}
+
+// Streaming top-M of one warp. Candidates above the current threshold are
+// appended to a per-warp shared-memory buffer; every 32 buffered keys are
+// sorted and merged into the register-resident list in one bitonic merge. The
+// threshold is the larger of this warp's M-th key and the block-wide maximum of
+// all warps' M-th keys (each is a lower bound of the block's M-th key).
 template <int SLOTS>
-struct Stream {
+struct Select {
   WarpList<SLOTS> L;
-  uint64_t tau;   // current M-th key
+  uint64_t tau;
   float tau_v;
-  uint32_t tau_id;
-  int M, lane;
+  uint64_t *buf;                 // [kBuf] per warp
+  unsigned long long *s_tau;     // block-wide threshold
+  int cnt, M, lane;
   bool bad;
 
-  __device__ __forceinline__ void refresh() {
-    tau = L.at(M - 1);
-    tau_v = key_value(tau);
-    tau_id = key_id(tau);
+  __device__ __forceinline__ void set_tau(uint64_t t) {
+    tau = t;
+    tau_v = (t == 0ull) ? -__int_as_float(0x7f800000) : key_value(t);
   }
-  // offer one candidate per lane; lanes with valid == false offer nothing
-  __device__ __forceinline__ void offer(float v, uint32_t id, bool valid) {
-    bad |= valid && ((v != v) || v == __int_as_float(0x7f800000));
+  __device__ __forceinline__ void sync_tau() {
+    const uint64_t sh = *reinterpret_cast<volatile unsigned long long *>(s_tau);
+    if (sh > tau) set_tau(sh);
+  }
+  __device__ __forceinline__ void merge_batch(uint64_t k) {
+    WarpList<SLOTS> b;
+    b.clear();
+    b.v[0] = sort32_desc(k, lane);
+    L.merge(b, lane);
+    const uint64_t own = L.at(M - 1);
+    if (own != 0ull) {
+      if (lane == 0) atomicMax(s_tau, static_cast<unsigned long long>(own));
+      if (own > tau) set_tau(own);
+    }
+  }
+  // one candidate per lane: keys above the threshold are appended to the
+  // buffer; the merges happen in drain(), after every four pushes (keeping the
+  // merge code out of the per-element path keeps the kernel small enough for
+  // the instruction cache)
+  __device__ __forceinline__ void push(float v, uint32_t id, bool valid) {
+    bad |= valid && !(v < __int_as_float(0x7f800000));
     const uint64_t key = make_key(v, id);
-    bool pass = valid && (v == v) && key > tau;
-    unsigned m = __ballot_sync(kFull, pass);
-    while (m) {
-      int src = __ffs(m) - 1;
-      uint64_t c = shfl64(key, src);
-      L.insert(c, lane);
-      refresh();
-      pass = pass && lane != src && key > tau;
-      m = __ballot_sync(kFull, pass);
+    const bool pass = valid && (v >= tau_v) && key > tau;
+    const unsigned m = __ballot_sync(kFull, pass);
+    if (pass) buf[cnt + __popc(m & ((1u << lane) - 1u))] = key;
+    cnt += __popc(m);
+  }
+  // merge full batches of 32, taken from the end of the buffer
+  __device__ __forceinline__ void drain() {
+    __syncwarp();
+    while (cnt >= 32) {
+      const uint64_t k = buf[cnt - 32 + lane];
+      cnt -= 32;
+      __syncwarp();
+      merge_batch(k);
+    }
+  }
+  __device__ __forceinline__ void flush() {
+    __syncwarp();
+    if (cnt > 0) {
+      const uint64_t k = (lane < cnt) ? buf[lane] : 0ull;
+      cnt = 0;
+      __syncwarp();
+      merge_batch(k);
     }
   }
 };
@@ -154,18 +198,22 @@ __device__ void block_merge_lists(uint64_t *lists /* [8][MP] */, int warp, int l
 }
 
 template <int SLOTS>
-__global__ void __launch_bounds__(kTopmThreads)
+__global__ void __launch_bounds__(kTopmThreads, 3)
 topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
             uint64_t *__restrict__ partial, unsigned *__restrict__ ticket,
             int *__restrict__ req_flags, int32_t *__restrict__ cand_id,
             float *__restrict__ cand_val, int32_t *__restrict__ topm_out) {
   constexpr int MP = SLOTS * 32;
   __shared__ uint64_t lists[kTopmWarps * MP];
+  __shared__ uint64_t bufs[kTopmWarps * kBuf];
+  __shared__ unsigned long long s_tau;
   __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int row = blockIdx.y, split = blockIdx.x;
   const size_t row_base = static_cast<size_t>(row) * V;
   const float *rowp = logits + row_base;
+  if (threadIdx.x == 0) s_tau = 0ull;
+  __syncthreads();
 
   // vector part [a0, a0 + 4 nv) is 16-byte aligned; scalar head [0, a0), tail
   const int a0 = min(V, static_cast<int>((4 - (row_base & 3)) & 3));
@@ -176,43 +224,72 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
   const int w0 = u0 + static_cast<int>(static_cast<long long>(warp) * cnt / kTopmWarps);
   const int w1 = u0 + static_cast<int>(static_cast<long long>(warp + 1) * cnt / kTopmWarps);
 
-  Stream<SLOTS> st;
+  Select<SLOTS> st;
   st.L.clear();
   st.M = M;
   st.lane = lane;
   st.bad = false;
-  st.refresh();
+  st.cnt = 0;
+  st.buf = bufs + warp * kBuf;
+  st.s_tau = &s_tau;
+  st.set_tau(0ull);
 
+  // kQ float4 per lane per iteration, the next iteration's loads in flight
   const float4 *vec = reinterpret_cast<const float4 *>(rowp + a0);
-  for (int u = w0 + lane; u - lane < w1; u += 32) {
-    bool ok = u < w1;
-    float4 x = ok ? __ldcs(vec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const uint32_t id = static_cast<uint32_t>(a0 + 4 * u);
-    bool any = ok && (x.x >= st.tau_v || x.y >= st.tau_v || x.z >= st.tau_v ||
-                      x.w >= st.tau_v || st.tau == 0ull);
-    bool nonfin = ok && ((x.x != x.x) || (x.y != x.y) || (x.z != x.z) || (x.w != x.w) ||
-                         x.x == __int_as_float(0x7f800000) || x.y == __int_as_float(0x7f800000) ||
-                         x.z == __int_as_float(0x7f800000) || x.w == __int_as_float(0x7f800000));
-    st.bad |= nonfin;
-    if (__any_sync(kFull, any)) {
-      st.offer(x.x, id + 0, ok);
-      st.offer(x.y, id + 1, ok);
-      st.offer(x.z, id + 2, ok);
-      st.offer(x.w, id + 3, ok);
+  float4 cur[kQ], nxt[kQ];
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) {
+    const int u = w0 + q * 32 + lane;
+    cur[q] = (u < w1) ? __ldcs(vec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int base = w0; base < w1; base += kQ * 32) {
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const int u = base + kQ * 32 + q * 32 + lane;
+      nxt[q] = (u < w1) ? __ldcs(vec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    st.sync_tau();
+    bool any = false;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const bool ok = base + q * 32 + lane < w1;
+      any |= ok && (cur[q].x >= st.tau_v || cur[q].y >= st.tau_v || cur[q].z >= st.tau_v ||
+                    cur[q].w >= st.tau_v);
+      st.bad |= ok && !(cur[q].x < __int_as_float(0x7f800000) &&
+                        cur[q].y < __int_as_float(0x7f800000) &&
+                        cur[q].z < __int_as_float(0x7f800000) &&
+                        cur[q].w < __int_as_float(0x7f800000));
+    }
+    if (__any_sync(kFull, any)) {
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const int u = base + q * 32 + lane;
+        const bool ok = u < w1;
+        const uint32_t id = static_cast<uint32_t>(a0 + 4 * u);
+        st.push(cur[q].x, id + 0, ok);
+        st.push(cur[q].y, id + 1, ok);
+        st.push(cur[q].z, id + 2, ok);
+        st.push(cur[q].w, id + 3, ok);
+        st.drain();
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) cur[q] = nxt[q];
   }
   // scalar head (split 0) and tail (last split), warp 0
   if (warp == 0) {
     if (split == 0 && a0 > 0) {
       bool ok = lane < a0;
-      st.offer(ok ? __ldg(rowp + lane) : 0.f, static_cast<uint32_t>(lane), ok);
+      st.push(ok ? __ldg(rowp + lane) : 0.f, static_cast<uint32_t>(lane), ok);
     }
     const int t0 = a0 + 4 * nv;
     if (split == nsplit - 1 && t0 < V) {
       bool ok = t0 + lane < V;
-      st.offer(ok ? __ldg(rowp + t0 + lane) : 0.f, static_cast<uint32_t>(t0 + lane), ok);
+      st.push(ok ? __ldg(rowp + t0 + lane) : 0.f, static_cast<uint32_t>(t0 + lane), ok);
     }
+    st.drain();
   }
+  st.flush();
   if (__any_sync(kFull, st.bad) && lane == 0) atomicOr(req_flags + row / D, kReqFlagNonfinite);
 
   st.L.store(lists + warp * MP, lane);

@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--spec", type=int, default=0, help="speculative expansions per step (0=default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     return ap.parse_args()
 
 
@@ -163,6 +164,43 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def e2e_leg(args, tb, wl, dt, np, torch, dist, world, dev, flush, st, K, Wm):
+    """Same metric through dt_build_trees_host: pinned host inputs copied in and
+    the trees copied back inside the timed region."""
+    host_ws = torch.empty(dt.host_workspace_bytes(tb.dims, tb.opt), dtype=torch.uint8, device=dev)
+    pin = lambda a, tt: torch.from_numpy(np.ascontiguousarray(a, dtype=tt)).pin_memory()
+    hin = dict(base_logits=pin(wl.base_logits, np.float32), H=pin(wl.H, np.float32),
+               state0=pin(wl.state0, np.float32), anchor_tok=pin(wl.anchor, np.int32),
+               temperature=pin(wl.temperature, np.float32))
+    hout = dt.alloc_outputs(tb.dims, "cpu", pin=True)
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = sum(v.numel() * v.element_size() for v in hout.values() if v is not None)
+
+    def e2e_step():
+        dt.build_trees_host(tb.dims, tb.w, tb.prepared, hin["base_logits"], hin["H"],
+                            hin["state0"], hin["anchor_tok"], hin["temperature"], host_ws, hout,
+                            tb.opt)
+    for _ in range(Wm):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = 0.0
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(K):
+        flush.fill_(i & 0xff)
+        ea.record(st)
+        e2e_step()
+        eb.record(st)
+        eb.synchronize()
+        e_ms += ea.elapsed_time(eb)
+    te = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = world * wl.batch * K / (float(te.item()) / 1000.0)
+    ok_e2e = bool((hout["status"] == 0).all())
+
+    return e2e_value, h2d, d2h, ok_e2e
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -229,6 +267,11 @@ def main():
     if world > 1:
         dist.barrier()
     clocks = clk.stop()
+    ctrl = tb.workspace[:96].view(torch.int32).cpu().tolist()   # search counters of the last round
+    search_steps, search_expansions = ctrl[4], ctrl[5]
+    t_ns = tb.workspace[32:80].view(torch.int64).cpu().tolist()
+    search_split_us = dict(zip(["gemm", "barrier1", "reduce", "barrier2", "tail", "barrier3"],
+                               [x / 1000.0 for x in t_ns]))
     per = [ph[i][0].elapsed_time(ph[i][3]) for i in range(K)]
     topm_ms = [ph[i][0].elapsed_time(ph[i][1]) for i in range(K)]
     proj_ms = [ph[i][1].elapsed_time(ph[i][2]) for i in range(K)]
@@ -241,37 +284,10 @@ def main():
     value = world * wl.batch * K / (total_ms / 1000.0)
 
     # end to end through the host-buffer entry point: pinned inputs in, results out
-    host_ws = torch.empty(dt.host_workspace_bytes(tb.dims, tb.opt), dtype=torch.uint8, device=dev)
-    pin = lambda a, tt: torch.from_numpy(np.ascontiguousarray(a, dtype=tt)).pin_memory()
-    hin = dict(base_logits=pin(wl.base_logits, np.float32), H=pin(wl.H, np.float32),
-               state0=pin(wl.state0, np.float32), anchor_tok=pin(wl.anchor, np.int32),
-               temperature=pin(wl.temperature, np.float32))
-    hout = dt.alloc_outputs(tb.dims, "cpu", pin=True)
-    h2d = sum(v.numel() * v.element_size() for v in hin.values())
-    d2h = sum(v.numel() * v.element_size() for v in hout.values() if v is not None)
-
-    def e2e_step():
-        dt.build_trees_host(tb.dims, tb.w, tb.prepared, hin["base_logits"], hin["H"],
-                            hin["state0"], hin["anchor_tok"], hin["temperature"], host_ws, hout,
-                            tb.opt)
-    for _ in range(Wm):
-        e2e_step()
-    torch.cuda.synchronize()
-    e_ms = 0.0
-    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for i in range(K):
-        flush.fill_(i & 0xff)
-        ea.record(st)
-        e2e_step()
-        eb.record(st)
-        eb.synchronize()
-        e_ms += ea.elapsed_time(eb)
-    te = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = world * wl.batch * K / (float(te.item()) / 1000.0)
-    ok_e2e = bool((hout["status"] == 0).all())
-
+    e2e_value, h2d, d2h, ok_e2e = None, 0, 0, None
+    if not args.no_e2e:
+        e2e_value, h2d, d2h, ok_e2e = e2e_leg(args, tb, wl, dt, np, torch, dist, world, dev, flush,
+                                               st, K, Wm)
     if rank == 0:
         o = {k: v.cpu().numpy() for k, v in out.items() if v is not None}
         cnt = algorithmic_counts(wl, o["tokens"], o["depths"])
@@ -304,12 +320,14 @@ def main():
                        "l2": "flushed (256 MB write) before every timed round",
                        "spec_width": tb.opt.spec_width or 8, "prepare_ms": prepare_ms,
                        "phases_ms": phases, "expansions_per_round": cnt["expansions"],
+                       "search_steps": search_steps, "search_expansions": search_expansions,
+                       "search_block0_us": search_split_us,
                        "round_algorithmic_bytes": round_bytes,
                        "round_hbm_frac": round_bytes / (total_ms / K * 1e-3) / 1e9 / pk["hbm_gbs"],
                        "peaks": pk["source"], "wall_s": wall},
             "roofline": roof,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ok": ok_e2e},
+            "e2e": ({"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                     "d2h_bytes_per_step": d2h, "ok": ok_e2e} if e2e_value is not None else None),
             "gpu_launches": 3 * K,
             "clocks": clocks,
         }

@@ -42,8 +42,11 @@
 // (score desc, push sequence asc) key.
 #include <cstdint>
 
+#include <cuda_bf16.h>
+
 #include "dt_common.cuh"
 #include "dt_internal.h"
+#include "dt_umma.cuh"
 
 namespace dt {
 
@@ -69,6 +72,11 @@ struct ChainParams {
   const float *U;
   float *S_store, *gh_store, *gin, *pbuf;
   int *colexp, *col_count;
+  // tensor-core GEMM path (bf16 weights): A tiles of 128 rows x kc K stay in
+  // shared memory; the input columns arrive as three bf16 terms per state
+  int umma, n_mt, ks, kc, cols_cap;
+  float *partial;      // [ks][cols_cap][R] per-K-chunk partial products
+  uint16_t *gin16;     // [cols_cap][3][d_s]
   Ctrl *ctrl;
   const int *req_flags;
   int32_t *tokens, *parents, *depths;
@@ -79,6 +87,15 @@ struct ChainParams {
   // dynamic shared memory carve-up (byte offsets)
   int sm_child_score, sm_child_tok, sm_child_exp, sm_exp_depth, sm_exp_parent, sm_exp_score,
       sm_exp_tok, sm_run_e, sm_run_head, sm_run_pos, sm_vhead, sm_par, sm_scratch, sm_total;
+  int sm_A, sm_B, sm_mbar, sm_tmem;
+};
+
+// One GRU cell to evaluate: input row G[tok], recurrent half gh, previous state
+// sp; the new state goes to s_out and to GEMM input column `slot`.
+struct GruJob {
+  int tok, slot;
+  const float *gh, *sp;
+  float *s_out;
 };
 
 struct TailState {
@@ -89,6 +106,7 @@ struct TailState {
   int n_sel;
   int spec_used;  // speculative (non-stall) expansions made so far
   int sel_e[DT_MAX_SPEC];
+  GruJob jobs[DT_MAX_SPEC];
   float T;
   int status;
 };
@@ -150,15 +168,11 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t v[SLOTS], int lane) {
 
 // ---------------------------------------------------------------- GEMM phase
 
-// [gh; p] = [W_hh; W1_S] x (+ [b_hh; 0]) for every active column.
-template <int WDT>
-__device__ void gemm_phase(const ChainParams &p, unsigned char *smem) {
+// Active GEMM columns in (request, rank) order: slot ids written to `slots`,
+// count returned. nb <= 256 requests per wave: one thread per request, then a
+// block-wide exclusive scan.
+__device__ int compact_slots(const ChainParams &p, int *slots) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ds = p.d_s;
-  const int R = 3 * ds + p.r;
-  // compact the active columns: slot ids in (request, rank) order. nb <= 256
-  // requests per wave: one thread per request, block-wide exclusive scan.
-  int *slots = reinterpret_cast<int *>(smem);  // [nb * P]
   __shared__ int s_warp_sum[kWarps];
   __shared__ int s_total;
   const int b_me = threadIdx.x;
@@ -176,7 +190,18 @@ __device__ void gemm_phase(const ChainParams &p, unsigned char *smem) {
   if (threadIdx.x == kThreads - 1) s_total = base + incl;
   for (int i = 0; i < c_me; ++i) slots[base + incl - c_me + i] = b_me * p.P + i;
   __syncthreads();
-  const int total = s_total;
+  return s_total;
+}
+
+// [gh; p] = [W_hh; W1_S] x (+ [b_hh; 0]) for every active column, on CUDA
+// cores in fp32 (the path for fp32 weights).
+template <int WDT>
+__device__ void gemm_phase(const ChainParams &p, unsigned char *smem) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ds = p.d_s;
+  const int R = 3 * ds + p.r;
+  int *slots = reinterpret_cast<int *>(smem);  // [nb * P]
+  const int total = compact_slots(p, slots);
   if (total == 0) return;
   float *stage = reinterpret_cast<float *>(smem + ((p.nb * p.P * 4 + 15) & ~15));  // [8][KC]
   const int nct = (total + kGemmCols - 1) / kGemmCols;
@@ -276,6 +301,177 @@ __device__ void gemm_phase(const ChainParams &p, unsigned char *smem) {
   }
 }
 
+// ------------------------------------------------- tensor-core GEMM phase
+
+constexpr int kUmmaN = 32;        // columns per MMA (one B buffer)
+constexpr int kUmmaPass = 256;    // TMEM columns (fp32 accumulators) per pass
+constexpr uint32_t kTmemCols = 256;
+
+// Rows [mt*128, mt*128+128) of [W_hh; W1_S] and K columns [kz*kc, kz*kc+kc) as
+// bf16 into the A tile (zero beyond R rows or d_s columns). Once per launch.
+__device__ void load_a_tile(const ChainParams &p, unsigned char *sA) {
+  const int g = blockIdx.x;
+  const int mt = g / p.ks, kz = g % p.ks;
+  const int R = 3 * p.d_s + p.r, k0 = kz * p.kc;
+  const int kg = p.kc / 8;
+  for (int i = threadIdx.x; i < 128 * kg; i += kThreads) {
+    const int r = i / kg, q = i % kg;
+    const int row = mt * 128 + r, k = k0 + q * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row < R && k < p.d_s) {
+      const uint16_t *src =
+          (row < 3 * p.d_s)
+              ? static_cast<const uint16_t *>(p.W_hh) + static_cast<size_t>(row) * p.d_s + k
+              : static_cast<const uint16_t *>(p.W1) +
+                    static_cast<size_t>(row - 3 * p.d_s) * (p.d + p.d_s) + p.d + k;
+      v = __ldg(reinterpret_cast<const uint4 *>(src));
+    }
+    *reinterpret_cast<uint4 *>(sA + umma_offset(r, q * 8, p.kc)) = v;
+  }
+}
+
+// B chunk: columns [c0, c0 + 32) of the active list, three bf16 terms, K range
+// of this block, into one buffer (zero for missing columns and k >= d_s), with
+// asynchronous 16-byte copies so that all of them are in flight at once.
+__device__ void load_b_chunk(const ChainParams &p, const int *slots, int total, int c0,
+                             unsigned char *sB) {
+  const int kz = blockIdx.x % p.ks, k0 = kz * p.kc;
+  const int kg = p.kc / 8;
+  const int per_split = kUmmaN * p.kc * 2;
+  for (int i = threadIdx.x; i < 3 * kUmmaN * kg; i += kThreads) {
+    const int q = i % kg, n = (i / kg) % kUmmaN, sp = i / (kg * kUmmaN);
+    const int c = c0 + n, k = k0 + q * 8;
+    const bool live = c < total && k < p.d_s;
+    const uint16_t *src =
+        live ? p.gin16 + (static_cast<size_t>(slots[c]) * 3 + sp) * p.d_s + k : p.gin16;
+    cp_async16(sB + sp * per_split + umma_offset(n, q * 8, p.kc), src, live ? 16u : 0u);
+  }
+  cp_async_commit();
+}
+
+// Completion of MMA batch number `use` of a buffer; an expired wait is retried
+// once so that no MMA is left in flight, and reported as failure.
+__device__ __forceinline__ bool wait_mma(uint64_t *mbar, uint32_t use, uint64_t limit_ns) {
+  if (mbar_wait(mbar, use & 1u, limit_ns)) return true;
+  mbar_wait(mbar, use & 1u, limit_ns);
+  return false;
+}
+
+struct UmmaState {
+  uint32_t tmem;      // TMEM base column address
+  uint32_t uses[2];   // commits issued on each B-buffer mbarrier
+};
+
+// Partial products of this block's (M tile, K chunk) for every active column,
+// written to p.partial[kz][column][row]. D = A B^T with A = 128 weight rows
+// (K-major, resident) and B = 32 columns of hi / mid / lo terms accumulated into
+// the same fp32 TMEM tile. Returns false if an MMA completion wait expired.
+__device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsigned char *scratch,
+                                UmmaState &u) {
+  int *slots = reinterpret_cast<int *>(scratch);
+  const int total = compact_slots(p, slots);
+  if (total == 0 || blockIdx.x >= p.n_mt * p.ks) return true;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int mt = blockIdx.x / p.ks, kz = blockIdx.x % p.ks;
+  const int R = 3 * p.d_s + p.r;
+  unsigned char *sA = smem + p.sm_A;
+  unsigned char *sB = smem + p.sm_B;
+  uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
+  const int buf_bytes = 3 * kUmmaN * p.kc * 2;
+  const uint32_t idesc = umma_idesc_bf16(128, kUmmaN);
+  const uint32_t sbo = 16u * p.kc;
+  const int nkb = p.kc / 16;
+  bool ok = true;
+  for (int pass0 = 0; pass0 < total; pass0 += kUmmaPass) {
+    const int pass_cols = min(kUmmaPass, total - pass0);
+    const int nch = (pass_cols + kUmmaN - 1) / kUmmaN;
+    uint32_t wait0 = 0u, wait1 = 0u;   // commit numbers awaited on buffers 0 / 1
+    bool pend0 = false, pend1 = false;
+    load_b_chunk(p, slots, total, pass0, sB);
+    for (int c = 0; c < nch; ++c) {
+      const int bi = c & 1;
+      cp_async_wait_all();
+      fence_async_smem();
+      tmem_fence_before();
+      __syncthreads();
+      tmem_fence_after();
+      if (threadIdx.x == 0) {
+        const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + bi * buf_bytes);
+        for (int kb = 0; kb < nkb; ++kb) {
+          const uint64_t ad = umma_desc(a0 + kb * 256, 128, sbo);
+#pragma unroll
+          for (int sp = 0; sp < 3; ++sp) {
+            const uint64_t bd = umma_desc(b0 + sp * (kUmmaN * p.kc * 2) + kb * 256, 128, sbo);
+            umma_bf16(u.tmem + c * kUmmaN, ad, bd, idesc, kb > 0 || sp > 0);
+          }
+        }
+        umma_commit(&mbar[bi]);
+      }
+      if (bi == 0) { wait0 = u.uses[0]++; pend0 = true; }
+      else { wait1 = u.uses[1]++; pend1 = true; }
+      if (c + 1 < nch) {
+        // the MMAs of chunk c-1 may still read the other buffer
+        if (bi == 0 && pend1) { ok &= wait_mma(&mbar[1], wait1, p.limit_ns); pend1 = false; }
+        if (bi == 1 && pend0) { ok &= wait_mma(&mbar[0], wait0, p.limit_ns); pend0 = false; }
+        load_b_chunk(p, slots, total, pass0 + (c + 1) * kUmmaN, sB + (bi ^ 1) * buf_bytes);
+      }
+    }
+    if (pend0) ok &= wait_mma(&mbar[0], wait0, p.limit_ns);
+    if (pend1) ok &= wait_mma(&mbar[1], wait1, p.limit_ns);
+    tmem_fence_after();
+    // epilogue: TMEM lane = row of the tile; warps w and w+4 share a lane quarter
+    const int quarter = warp & 3;
+    const int row = mt * 128 + quarter * 32 + lane;
+    for (int grp = warp >> 2; grp * 8 < pass_cols; grp += 2) {
+      float v[8];
+      tmem_ld8(u.tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * 8, v);
+      tmem_wait_ld();
+      if (row < R) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int col = pass0 + grp * 8 + j;
+          if (col < total)
+            p.partial[(static_cast<size_t>(kz) * p.cols_cap + col) * R + row] = v[j];
+        }
+      }
+    }
+    tmem_fence_before();
+    __syncthreads();
+  }
+  return ok;
+}
+
+// Sum of the K-chunk partials (fixed order) + b_hh into gh_store / pbuf.
+__device__ void reduce_phase(const ChainParams &p, unsigned char *scratch) {
+  int *slots = reinterpret_cast<int *>(scratch);
+  const int total = compact_slots(p, slots);
+  const int ds = p.d_s, R = 3 * ds + p.r, R4 = R / 4;
+  const size_t plane = static_cast<size_t>(p.cols_cap) * R;
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < total * R4; i += gridDim.x * kThreads) {
+    const int col = i / R4, row = (i % R4) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int z = 0; z < p.ks; ++z) {
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+          p.partial + z * plane + static_cast<size_t>(col) * R + row));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const int slot = slots[col];
+    const int b = slot / p.P;
+    if (row < 3 * ds) {
+      const int e = __ldcg(p.colexp + slot);
+      const int e_slot = (e == kState0) ? p.e_cap : e;
+      if (p.b_hh) {
+        acc.x += p.b_hh[row]; acc.y += p.b_hh[row + 1];
+        acc.z += p.b_hh[row + 2]; acc.w += p.b_hh[row + 3];
+      }
+      *reinterpret_cast<float4 *>(
+          p.gh_store + (static_cast<size_t>(b) * (p.e_cap + 1) + e_slot) * 3 * ds + row) = acc;
+    } else {
+      *reinterpret_cast<float4 *>(p.pbuf + static_cast<size_t>(slot) * p.r + (row - 3 * ds)) = acc;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- tail phase
 
 struct Tables {
@@ -335,62 +531,201 @@ __device__ __forceinline__ int best_run(const ChainParams &p, const Tables &t, c
   return br;
 }
 
-// GRU cell for node e of request b: S_e = GRU(S_parent, x = E[tok]) with the
-// input half taken from the prepared table row G[tok] (= W_ih E[tok] + b_ih) and
-// the recurrent half gh_parent (= W_hh S_parent + b_hh) from an earlier GEMM.
-__device__ __forceinline__ void gru_node(const ChainParams &p, int b, int tok, const float *gh,
-                                         const float *sp, float *s_out, float *col_out) {
-  const int ds = p.d_s;
-  const float *gi = p.G + static_cast<size_t>(tok) * 3 * ds;
-  for (int u = threadIdx.x; u < ds; u += kThreads) {
-    const float r = sigmoidf_(__ldg(gi + u) + ldcg(gh + u));
-    const float z = sigmoidf_(__ldg(gi + ds + u) + ldcg(gh + ds + u));
-    const float n = tanhf(__ldg(gi + 2 * ds + u) + r * ldcg(gh + 2 * ds + u));
-    const float s = (1.f - z) * n + z * ldcg(sp + u);
-    s_out[u] = s;
-    col_out[u] = s;
+// The GEMM input column of a state: fp32 (CUDA-core path) or three bf16 terms
+// hi + mid + lo that reproduce the fp32 value to about 24 bits (tensor-core
+// path; the products with the exact bf16 weights then keep fp32 accuracy).
+__device__ __forceinline__ void write_column(const ChainParams &p, int slot, int u, float s) {
+  if (p.umma) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(s);
+    const float r1 = s - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    uint16_t *c = p.gin16 + static_cast<size_t>(slot) * 3 * p.d_s + u;
+    c[0] = __bfloat16_as_ushort(hi);
+    c[p.d_s] = __bfloat16_as_ushort(mid);
+    c[2 * p.d_s] = __bfloat16_as_ushort(lo);
+  } else {
+    p.gin[static_cast<size_t>(slot) * p.d_s + u] = s;
   }
 }
 
+__device__ __forceinline__ void write_column4(const ChainParams &p, int slot, int u, float4 s) {
+  if (p.umma) {
+    const float v[4] = {s.x, s.y, s.z, s.w};
+    uint32_t hb[4], mb[4], lb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v[i]);
+      const float r1 = v[i] - __bfloat162float(hi);
+      const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+      hb[i] = __bfloat16_as_ushort(hi);
+      mb[i] = __bfloat16_as_ushort(mid);
+      lb[i] = __bfloat16_as_ushort(lo);
+    }
+    uint16_t *c = p.gin16 + static_cast<size_t>(slot) * 3 * p.d_s + u;
+    *reinterpret_cast<uint2 *>(c) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+    *reinterpret_cast<uint2 *>(c + p.d_s) =
+        make_uint2(mb[0] | (mb[1] << 16), mb[2] | (mb[3] << 16));
+    *reinterpret_cast<uint2 *>(c + 2 * p.d_s) =
+        make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
+  } else {
+    *reinterpret_cast<float4 *>(p.gin + static_cast<size_t>(slot) * p.d_s + u) = s;
+  }
+}
+
+// GRU cells of the chosen nodes: S_e = GRU(S_parent, x = E[tok]) with the input
+// half taken from the prepared table row G[tok] (= W_ih E[tok] + b_ih) and the
+// recurrent half gh_parent (= W_hh S_parent + b_hh) from an earlier GEMM. All
+// nodes are processed together, four units per item and two items per thread
+// in flight, so that the gathers of G rows overlap.
+__device__ __forceinline__ float gru_unit(float gir, float giz, float gin, float ghr, float ghz,
+                                          float ghn, float sp) {
+  const float r = sigmoidf_(gir + ghr);
+  const float z = sigmoidf_(giz + ghz);
+  const float n = tanhf(gin + r * ghn);
+  return (1.f - z) * n + z * sp;
+}
+
+__device__ void gru_jobs(const ChainParams &p, const GruJob *jobs, int njobs) {
+  const int ds = p.d_s, q4 = ds / 4;
+  const int items = njobs * q4;
+  constexpr int IT = 2;
+  for (int i0 = threadIdx.x; i0 < items; i0 += IT * kThreads) {
+    float4 gi[IT][3], gh[IT][3], sp[IT];
+    int jn[IT], u[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      const int i = i0 + k * kThreads;
+      jn[k] = (i < items) ? i / q4 : -1;
+      u[k] = (i % q4) * 4;
+      if (jn[k] >= 0) {
+        const GruJob &J = jobs[jn[k]];
+        const float *g = p.G + static_cast<size_t>(J.tok) * 3 * ds + u[k];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          gi[k][q] = __ldg(reinterpret_cast<const float4 *>(g + q * ds));
+          gh[k][q] = __ldcg(reinterpret_cast<const float4 *>(J.gh + q * ds + u[k]));
+        }
+        sp[k] = __ldcg(reinterpret_cast<const float4 *>(J.sp + u[k]));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      if (jn[k] < 0) continue;
+      const GruJob &J = jobs[jn[k]];
+      float4 s;
+      s.x = gru_unit(gi[k][0].x, gi[k][1].x, gi[k][2].x, gh[k][0].x, gh[k][1].x, gh[k][2].x, sp[k].x);
+      s.y = gru_unit(gi[k][0].y, gi[k][1].y, gi[k][2].y, gh[k][0].y, gh[k][1].y, gh[k][2].y, sp[k].y);
+      s.z = gru_unit(gi[k][0].z, gi[k][1].z, gi[k][2].z, gh[k][0].z, gh[k][1].z, gh[k][2].z, sp[k].z);
+      s.w = gru_unit(gi[k][0].w, gi[k][1].w, gi[k][2].w, gh[k][0].w, gh[k][1].w, gh[k][2].w, sp[k].w);
+      *reinterpret_cast<float4 *>(J.s_out + u[k]) = s;
+      write_column4(p, J.slot, u[k], s);
+    }
+  }
+}
 
 // Children of expansion e (warp-level): h = SiLU(U_j + p), L over the M
 // candidates of depth j, log-sum-exp over them, the k best by (L desc, id asc).
-template <int WDT, int SLOTS>
+// The lanes split the rank dimension into 8-wide chunks: a candidate's W2 row
+// is read by the whole warp in one coalesced access, candidate ids and base
+// logits are loaded up front, and eight rows are in flight at a time; lane
+// c % 32 keeps candidate c for the sort. With r <= 256 each lane's h chunk
+// stays in registers; larger ranks read h from a per-warp shared buffer.
+template <int WDT, int SLOTS, bool SMALL_R>
 __device__ void score_node(const ChainParams &p, const Tables &t, float T, int b, int slot, int e,
-                           float *hbuf, int lane) {
+                           int lane, float *hbuf) {
   const int j = t.exp_depth[e] + 1;
   const size_t row = static_cast<size_t>(p.b0 + b) * p.D + (j - 1);
   const float *U = p.U + row * p.r;
   const float *pv = p.pbuf + static_cast<size_t>(slot) * p.r;
-  for (int q = lane; q < p.r; q += 32) hbuf[q] = siluf_(__ldg(U + q) + ldcg(pv + q));
-  __syncwarp();
+  const int nq = p.r / 8;
   const int32_t *cid = p.cand_id + row * p.M;
   const float *cval = p.cand_val + row * p.M;
-  const float ninf = -__int_as_float(0x7f800000);
-  uint64_t key[SLOTS];
-  float Lv[SLOTS];
-  float mx = ninf;
+  int my_id[SLOTS];
+  float my_base[SLOTS];
 #pragma unroll
   for (int s = 0; s < SLOTS; ++s) {
     const int c = s * 32 + lane;
+    my_id[s] = (c < p.M) ? __ldg(cid + c) : -1;
+    my_base[s] = (c < p.M) ? __ldg(cval + c) : 0.f;
+  }
+  float h[8];
+  if (SMALL_R) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      h[i] = (lane < nq) ? siluf_(__ldg(U + 8 * lane + i) + ldcg(pv + 8 * lane + i)) : 0.f;
+  } else {
+    for (int q = lane; q < p.r; q += 32) hbuf[q] = siluf_(__ldg(U + q) + ldcg(pv + q));
+    __syncwarp();
+  }
+  const float ninf = -__int_as_float(0x7f800000);
+  uint64_t key[SLOTS];
+  float Lv[SLOTS];
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) {
     key[s] = 0ull;
     Lv[s] = ninf;
-    if (c < p.M) {
-      const int id = __ldg(cid + c);
-      const size_t w0 = static_cast<size_t>(id) * p.r;
-      float acc = 0.f;
-      for (int q = 0; q < p.r; q += 8) {
-        float wf[8];
-        load8<WDT>(p.W2, w0 + q, wf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc = fmaf(wf[i], hbuf[q + i], acc);
+    for (int c8 = 0; c8 < 4; ++c8) {
+      const int c0 = s * 32 + c8 * 8;
+      if (c0 < p.M) {                        // warp-uniform
+        constexpr int G = 8;
+        float acc[G];
+        int ids[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          ids[g] = __shfl_sync(kFull, my_id[s], c8 * 8 + g);
+          acc[g] = 0.f;
+        }
+        if (SMALL_R) {
+          float wf[G][8];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            if (ids[g] >= 0 && lane < nq) {
+              load8<WDT>(p.W2, static_cast<size_t>(ids[g]) * p.r + 8 * lane, wf[g]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) wf[g][i] = 0.f;
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[g] = fmaf(wf[g][i], h[i], acc[g]);
+        } else {
+#pragma unroll 1
+          for (int q = lane; q - lane < nq; q += 32) {
+            if (q < nq) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) h[i] = hbuf[8 * q + i];
+#pragma unroll
+              for (int g = 0; g < G; ++g) {
+                if (ids[g] >= 0) {
+                  float wf[8];
+                  load8<WDT>(p.W2, static_cast<size_t>(ids[g]) * p.r + 8 * q, wf);
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) acc[g] = fmaf(wf[i], h[i], acc[g]);
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float dl = warp_sum(acc[g]);
+          if (c8 * 8 + g == lane && ids[g] >= 0) {
+            const float L = __fdiv_rn(my_base[s] + dl, T);
+            Lv[s] = L;
+            key[s] = make_key(L, static_cast<uint32_t>(ids[g]));
+          }
+        }
       }
-      const float L = __fdiv_rn(__ldg(cval + c) + acc, T);
-      Lv[s] = L;
-      key[s] = make_key(L, static_cast<uint32_t>(id));
-      mx = fmaxf(mx, L);
     }
   }
+  float mx = ninf;
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) mx = fmaxf(mx, Lv[s]);
   mx = warp_max(mx);
   float sum = 0.f;
 #pragma unroll
@@ -517,6 +852,21 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
     }
     __syncwarp();
   }
+  // warm L2 with the prepared rows of the frontier nodes most likely to be
+  // expanded at the next step (the next 2P unexpanded entries in order)
+  for (int extra = 0; extra < 2 * p.P;) {
+    const int r = best_run(p, t, t.vhead, n_runs, lane);
+    if (r < 0) break;
+    const int h = t.vhead[r], er = t.run_e[r];
+    if (t.exp_depth[er] + 1 < p.D && t.child_exp[er * p.k + h] < 0) {
+      if (lane == 0)
+        prefetch_l2(p.G + static_cast<size_t>(t.child_tok[er * p.k + h]) * 3 * p.d_s,
+                    static_cast<uint32_t>(12u * p.d_s));
+      ++extra;
+    }
+    if (lane == 0) t.vhead[r] = static_cast<uint8_t>(h + 1);
+    __syncwarp();
+  }
   if (lane == 0) {
     ts.count = count;
     ts.n_runs = n_runs;
@@ -524,6 +874,7 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
     ts.n_sel = nsel;
     ts.spec_used += nspec;
     p.col_count[b] = nsel;
+    atomicAdd(&p.ctrl->expansions, static_cast<unsigned>(nsel));
   }
   __syncwarp();
 }
@@ -547,12 +898,23 @@ __device__ void tail_init(const ChainParams &p, const Tables &t, TailState &ts, 
   if (p.N == 0) { finalize(p, t, ts, b, false); return; }
   // first GEMM column: the initial state, for W_hh state0 + b_hh
   const float *s0 = p.state0 + static_cast<size_t>(p.b0 + b) * p.d_s;
-  float *col = p.gin + static_cast<size_t>(b) * p.P * p.d_s;
-  for (int u = threadIdx.x; u < p.d_s; u += kThreads) col[u] = s0[u];
+  for (int u = threadIdx.x; u < p.d_s; u += kThreads) write_column(p, b * p.P, u, s0[u]);
   if (threadIdx.x == 0) {
     p.colexp[b * p.P] = kState0;
     p.col_count[b] = 1;
     atomicAdd(&p.ctrl->active, 1);
+  }
+  // warm L2 with the W2 rows of every candidate of this request (scored by the
+  // expansions to come) when the whole wave's rows fit comfortably in L2
+  const size_t row_bytes = static_cast<size_t>(p.r) * (p.umma ? 2 : 4);
+  if (static_cast<size_t>(p.nb) * p.D * p.M * row_bytes <= (48u << 20)) {
+    const int32_t *cid = p.cand_id + static_cast<size_t>(p.b0 + b) * p.D * p.M;
+    for (int i = threadIdx.x; i < p.D * p.M; i += kThreads) {
+      const int id = cid[i];
+      if (id >= 0)
+        prefetch_l2(static_cast<const char *>(p.W2) + static_cast<size_t>(id) * row_bytes,
+                    static_cast<uint32_t>(row_bytes));
+    }
   }
   __syncthreads();
 }
@@ -565,13 +927,21 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
   if (ts.e_count == 0) {
     // the root: S_0 = GRU(state0, E[anchor]); its recurrent half came from the state0 column
     const int anchor = p.anchor[p.b0 + b];
-    gru_node(p, b, anchor, p.gh_store + (ebase + p.e_cap) * 3 * p.d_s,
-             p.state0 + static_cast<size_t>(p.b0 + b) * p.d_s, p.S_store + ebase * p.d_s,
-             p.gin + static_cast<size_t>(b) * p.P * p.d_s);
+    if (threadIdx.x == 0) {
+      GruJob &J = ts.jobs[0];
+      J.tok = anchor;
+      J.slot = b * p.P;
+      J.gh = p.gh_store + (ebase + p.e_cap) * 3 * p.d_s;
+      J.sp = p.state0 + static_cast<size_t>(p.b0 + b) * p.d_s;
+      J.s_out = p.S_store + ebase * p.d_s;
+    }
+    __syncthreads();
+    gru_jobs(p, ts.jobs, 1);
     if (threadIdx.x == 0) {
       t.exp_depth[0] = 0; t.exp_parent[0] = -1; t.exp_score[0] = 0.0f; t.exp_tok[0] = anchor;
       ts.e_count = 1;
       ts.n_sel = 1;
+      atomicAdd(&p.ctrl->expansions, 1u);
       ts.sel_e[0] = 0;
       p.colexp[b * p.P] = 0;
       p.col_count[b] = 1;
@@ -580,9 +950,13 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
     return;
   }
   // 1. children of the nodes expanded by the last GEMM (one warp per node)
-  float *hbuf = t.scratch + warp * p.r;
-  for (int i = warp; i < ncols; i += kWarps)
-    score_node<WDT, SLOTS>(p, t, ts.T, b, b * p.P + i, ts.sel_e[i], hbuf, lane);
+  float *hbuf = t.scratch + warp * p.r;   // used only when r > 256
+  for (int i = warp; i < ncols; i += kWarps) {
+    if (p.r <= 256)
+      score_node<WDT, SLOTS, true>(p, t, ts.T, b, b * p.P + i, ts.sel_e[i], lane, hbuf);
+    else
+      score_node<WDT, SLOTS, false>(p, t, ts.T, b, b * p.P + i, ts.sel_e[i], lane, hbuf);
+  }
   __syncthreads();
   if (threadIdx.x == 0 && ts.n_runs == 0) {  // the root's children form the first run
     t.run_e[0] = 0; t.run_head[0] = 0; t.run_pos[0] = 0;
@@ -594,35 +968,85 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
   __syncthreads();
   if (ts.done == 2) { finalize(p, t, ts, b, true); return; }
   // 3. GRU states of the chosen nodes
-  for (int i = 0; i < ts.n_sel; ++i) {
-    const int e = ts.sel_e[i];
-    const int pe = t.exp_parent[e];
-    gru_node(p, b, t.exp_tok[e], p.gh_store + (ebase + pe) * 3 * p.d_s,
-             p.S_store + (ebase + pe) * p.d_s, p.S_store + (ebase + e) * p.d_s,
-             p.gin + (static_cast<size_t>(b) * p.P + i) * p.d_s);
+  if (threadIdx.x < ts.n_sel) {
+    const int i = threadIdx.x, e = ts.sel_e[i], pe = t.exp_parent[e];
+    GruJob &J = ts.jobs[i];
+    J.tok = t.exp_tok[e];
+    J.slot = b * p.P + i;
+    J.gh = p.gh_store + (ebase + pe) * 3 * p.d_s;
+    J.sp = p.S_store + (ebase + pe) * p.d_s;
+    J.s_out = p.S_store + (ebase + e) * p.d_s;
   }
+  __syncthreads();
+  gru_jobs(p, ts.jobs, ts.n_sel);
   __syncthreads();
 }
 
 template <int WDT, int SLOTS>
 __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ TailState ts;
   __shared__ int s_active;
   const Tables t = tables(p, smem);
   const int b = blockIdx.x;
   const bool tail = b < p.nb;
+  // tensor-core blocks: stationary A tile, two mbarriers, 256 TMEM columns
+  const bool mma_block = p.umma && blockIdx.x < p.n_mt * p.ks;
+  UmmaState u;
+  u.tmem = 0;
+  u.uses[0] = u.uses[1] = 0;
+  if (mma_block) {
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + p.sm_tmem);
+    if (threadIdx.x == 0) {
+      mbar_init(&mbar[0], 1);
+      mbar_init(&mbar[1], 1);
+    }
+    load_a_tile(p, smem + p.sm_A);
+    if ((threadIdx.x >> 5) == 0) tmem_alloc(tslot, kTmemCols);
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    u.tmem = *tslot;
+  }
   if (tail) tail_init(p, t, ts, b);
   bool ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
                          p.limit_ns);
+  // block 0 accounts its time per phase (for profiling; a few timer reads a step)
+  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
+  uint64_t t_prev = clock_me ? global_ns() : 0;
+  auto lap = [&](int k) {
+    if (clock_me) {
+      const uint64_t now = global_ns();
+      p.ctrl->t_ns[k] += now - t_prev;
+      t_prev = now;
+    }
+  };
   for (int step = 0; ok && step < p.N + 3; ++step) {
-    gemm_phase<WDT>(p, smem + p.sm_scratch);
+    if (clock_me) p.ctrl->steps = static_cast<unsigned>(step + 1);
+    if (p.umma) {
+      if (!gemm_phase_umma(p, smem, smem + p.sm_scratch, u) && threadIdx.x == 0)
+        atomicExch(&p.ctrl->abort, 1);
+      lap(0);
+      ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
+                        p.limit_ns);
+      lap(1);
+      if (!ok) break;
+      reduce_phase(p, smem + p.sm_scratch);
+      lap(2);
+    } else {
+      gemm_phase<WDT>(p, smem + p.sm_scratch);
+      lap(0);
+    }
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
                       p.limit_ns);
+    lap(3);
     if (!ok) break;
     if (tail && !ts.done) tail_step<WDT, SLOTS>(p, t, ts, b);
+    lap(4);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
                       p.limit_ns);
+    lap(5);
     if (!ok) break;
     if (threadIdx.x == 0) s_active = ld_acquire_s32(&p.ctrl->active);
     __syncthreads();
@@ -631,6 +1055,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
   if (tail && !ts.done) {
     if (threadIdx.x == 0) ts.status = DT_ERR_TIMEOUT;
     finalize(p, t, ts, b, true);
+  }
+  if (mma_block) {  // every MMA of this block has completed (waited in its phase)
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    if ((threadIdx.x >> 5) == 0) tmem_dealloc(u.tmem, kTmemCols);
   }
 }
 
@@ -654,9 +1084,16 @@ static int chain_smem_layout(const Plan &pl, int e_cap, int wave, ChainParams *c
   cp->sm_run_pos = off;     off = al(off + n1 * 2, 16);
   cp->sm_vhead = off;       off = al(off + n1, 16);
   cp->sm_par = off;         off = al(off + n1 * 2, 16);
+  cp->sm_A = cp->sm_B = cp->sm_mbar = cp->sm_tmem = 0;
+  if (pl.umma) {
+    cp->sm_A = off = al(off, 128);    off += 128 * pl.kc * 2;
+    cp->sm_B = off = al(off, 128);    off += 2 * 3 * kUmmaN * pl.kc * 2;
+    cp->sm_mbar = off = al(off, 16);  off += 16;
+    cp->sm_tmem = off;                off += 16;
+  }
   cp->sm_scratch = off;
-  const int gemm_scratch = al(wave * pl.spec * 4, 16) + kGemmCols * kGemmKC * 4;
-  const int tail_scratch = kWarps * d.r * 4;
+  const int gemm_scratch = al(wave * pl.spec * 4, 16) + (pl.umma ? 0 : kGemmCols * kGemmKC * 4);
+  const int tail_scratch = d.r > 256 ? kWarps * d.r * 4 : 16;
   off += gemm_scratch > tail_scratch ? gemm_scratch : tail_scratch;
   cp->sm_total = off;
   return off;
@@ -709,6 +1146,10 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.gin = reinterpret_cast<float *>(w + pl.off_gin);
   cp.pbuf = reinterpret_cast<float *>(w + pl.off_p);
   cp.colexp = reinterpret_cast<int *>(w + pl.off_colexp);
+  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc;
+  cp.cols_cap = pl.wave * pl.spec;
+  cp.partial = pl.umma ? reinterpret_cast<float *>(w + pl.off_partial) : nullptr;
+  cp.gin16 = pl.umma ? reinterpret_cast<uint16_t *>(w + pl.off_gin16) : nullptr;
   cp.col_count = cp.colexp + static_cast<size_t>(pl.wave) * pl.spec;
   cp.ctrl = reinterpret_cast<Ctrl *>(w + pl.off_ctrl);
   cp.req_flags = reinterpret_cast<const int *>(w + pl.off_ctrl + kCtrlHeader +

@@ -105,7 +105,14 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return DT_ERR_CUDA;
   const int smem_max = smem_optin - static_cast<int>(fa.sharedSizeBytes);
   int e_cap = d.N + 1 + (p->spec > 1 ? d.N + 1 : 0);
-  int smem = chain_smem_bytes(*p, e_cap, wave);
+  // widest MMA column block (fewer B-load round trips) that fits
+  p->umma_n = 32;
+  int smem = 0;
+  for (int un : {64, 48, 32}) {
+    p->umma_n = un;
+    smem = chain_smem_bytes(*p, e_cap, wave);
+    if (smem <= smem_max) break;
+  }
   while (smem > smem_max && e_cap > d.N + 1) {
     e_cap = d.N + 1 + (e_cap - d.N - 1) / 2;
     smem = chain_smem_bytes(*p, e_cap, wave);
@@ -123,12 +130,12 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   p->e_cap = e_cap;
   p->chain_smem = static_cast<size_t>(smem);
 
-  // projection GEMM: split K until about two blocks per SM
+  // projection GEMM: split K so that the tiles x chunks fill every SM once
   {
     const int tiles = gemm_tiles(static_cast<int>(rows), d.r);
-    int ks = (2 * p->num_sms + tiles - 1) / tiles;
+    int ks = p->num_sms / tiles;
     const int kmax = (d.d + 15) / 16;
-    p->proj_ksplit = ks < 1 ? 1 : (ks > 16 ? 16 : (ks > kmax ? kmax : ks));
+    p->proj_ksplit = ks < 1 ? 1 : (ks > 32 ? 32 : (ks > kmax ? kmax : ks));
   }
   // workspace carve-up
   size_t off = 0;
@@ -208,9 +215,7 @@ int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const f
   float *U = reinterpret_cast<float *>(wsb + pl.off_U);
   if (dt::launch_gemm_nt(d.batch * d.D, d.r, d.d, H, DT_F32, d.d, w->W1, w->wdtype,
                          static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r, pl.proj_ksplit,
-                         reinterpret_cast<float *>(wsb + pl.off_upart),
-                         reinterpret_cast<unsigned *>(wsb + pl.off_ctrl + pl.off_gemm_tickets),
-                         st) != cudaSuccess)
+                         reinterpret_cast<float *>(wsb + pl.off_upart), st) != cudaSuccess)
     return DT_ERR_CUDA;
   rc = record(opt, 2, st);
   if (rc) return rc;
@@ -292,8 +297,7 @@ int dt_prepare_weights(const dt_dims *dims, const dt_weights *w, void *prepared,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dt::launch_gemm_nt(dims->V, 3 * dims->d_s, dims->d, w->E, w->wdtype, dims->d, w->W_ih,
                          w->wdtype, dims->d, w->b_ih, static_cast<float *>(prepared),
-                         3 * static_cast<size_t>(dims->d_s), 1, nullptr, nullptr,
-                         st) != cudaSuccess)
+                         3 * static_cast<size_t>(dims->d_s), 1, nullptr, st) != cudaSuccess)
     return DT_ERR_CUDA;
   return DT_OK;
 }

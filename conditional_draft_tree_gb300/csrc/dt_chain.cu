@@ -74,7 +74,7 @@ struct ChainParams {
   int *colexp, *col_count;
   // tensor-core GEMM path (bf16 weights): A tiles of 128 rows x kc K stay in
   // shared memory; the input columns arrive as three bf16 terms per state
-  int umma, n_mt, ks, kc, cols_cap;
+  int umma, n_mt, ks, kc, un, cols_cap;   // un: columns per MMA (one B buffer)
   float *partial;      // [ks][cols_cap][R] per-K-chunk partial products
   uint16_t *gin16;     // [cols_cap][3][d_s]
   Ctrl *ctrl;
@@ -87,7 +87,7 @@ struct ChainParams {
   // dynamic shared memory carve-up (byte offsets)
   int sm_child_score, sm_child_tok, sm_child_exp, sm_exp_depth, sm_exp_parent, sm_exp_score,
       sm_exp_tok, sm_run_e, sm_run_head, sm_run_pos, sm_vhead, sm_par, sm_scratch, sm_total;
-  int sm_A, sm_B, sm_mbar, sm_tmem;
+  int sm_A, sm_B, sm_mbar, sm_tmem, sm_run_hs, sm_vhs;
 };
 
 // One GRU cell to evaluate: input row G[tok], recurrent half gh, previous state
@@ -303,9 +303,7 @@ __device__ void gemm_phase(const ChainParams &p, unsigned char *smem) {
 
 // ------------------------------------------------- tensor-core GEMM phase
 
-constexpr int kUmmaN = 32;        // columns per MMA (one B buffer)
-constexpr int kUmmaPass = 256;    // TMEM columns (fp32 accumulators) per pass
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 256;   // fp32 accumulator columns per block
 
 // Rows [mt*128, mt*128+128) of [W_hh; W1_S] and K columns [kz*kc, kz*kc+kc) as
 // bf16 into the A tile (zero beyond R rows or d_s columns). Once per launch.
@@ -330,21 +328,27 @@ __device__ void load_a_tile(const ChainParams &p, unsigned char *sA) {
   }
 }
 
-// B chunk: columns [c0, c0 + 32) of the active list, three bf16 terms, K range
+// B chunk: columns [c0, c0 + un) of the active list, three bf16 terms, K range
 // of this block, into one buffer (zero for missing columns and k >= d_s), with
 // asynchronous 16-byte copies so that all of them are in flight at once.
 __device__ void load_b_chunk(const ChainParams &p, const int *slots, int total, int c0,
                              unsigned char *sB) {
-  const int kz = blockIdx.x % p.ks, k0 = kz * p.kc;
+  const int k0 = (blockIdx.x % p.ks) * p.kc;
   const int kg = p.kc / 8;
-  const int per_split = kUmmaN * p.kc * 2;
-  for (int i = threadIdx.x; i < 3 * kUmmaN * kg; i += kThreads) {
-    const int q = i % kg, n = (i / kg) % kUmmaN, sp = i / (kg * kUmmaN);
-    const int c = c0 + n, k = k0 + q * 8;
-    const bool live = c < total && k < p.d_s;
-    const uint16_t *src =
-        live ? p.gin16 + (static_cast<size_t>(slots[c]) * 3 + sp) * p.d_s + k : p.gin16;
-    cp_async16(sB + sp * per_split + umma_offset(n, q * 8, p.kc), src, live ? 16u : 0u);
+  const int per_split = p.un * p.kc * 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int sp = 0; sp < 3; ++sp) {
+    for (int n = warp; n < p.un; n += kWarps) {
+      const int c = c0 + n;
+      const uint16_t *rowp =
+          (c < total) ? p.gin16 + (static_cast<size_t>(slots[c]) * 3 + sp) * p.d_s : p.gin16;
+      unsigned char *dst = sB + sp * per_split + umma_offset(n, 0, p.kc);
+      for (int q = lane; q < kg; q += 32) {
+        const int k = k0 + q * 8;
+        const bool live = c < total && k < p.d_s;
+        cp_async16(dst + q * 128, live ? rowp + k : p.gin16, live ? 16u : 0u);
+      }
+    }
   }
   cp_async_commit();
 }
@@ -377,33 +381,43 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
   unsigned char *sA = smem + p.sm_A;
   unsigned char *sB = smem + p.sm_B;
   uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
-  const int buf_bytes = 3 * kUmmaN * p.kc * 2;
-  const uint32_t idesc = umma_idesc_bf16(128, kUmmaN);
+  const int buf_bytes = 3 * p.un * p.kc * 2;
+  const uint32_t idesc = umma_idesc_bf16(128, p.un);
+  const int pass_max = (static_cast<int>(kTmemCols) / p.un) * p.un;
   const uint32_t sbo = 16u * p.kc;
   const int nkb = p.kc / 16;
   bool ok = true;
-  for (int pass0 = 0; pass0 < total; pass0 += kUmmaPass) {
-    const int pass_cols = min(kUmmaPass, total - pass0);
-    const int nch = (pass_cols + kUmmaN - 1) / kUmmaN;
+  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
+  uint64_t t_mma0 = global_ns();
+  for (int pass0 = 0; pass0 < total; pass0 += pass_max) {
+    const int pass_cols = min(pass_max, total - pass0);
+    const int nch = (pass_cols + p.un - 1) / p.un;
     uint32_t wait0 = 0u, wait1 = 0u;   // commit numbers awaited on buffers 0 / 1
     bool pend0 = false, pend1 = false;
     load_b_chunk(p, slots, total, pass0, sB);
     for (int c = 0; c < nch; ++c) {
       const int bi = c & 1;
+      const uint64_t tw0 = clock_me ? global_ns() : 0;
       cp_async_wait_all();
       fence_async_smem();
       tmem_fence_before();
       __syncthreads();
       tmem_fence_after();
+      if (clock_me) p.ctrl->t_ns[11] += global_ns() - tw0;
       if (threadIdx.x == 0) {
-        const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + bi * buf_bytes);
+        // descriptors once; a K step of 16 moves the start address by 256 bytes
+        // (16 in the encoded field, which never carries: addresses < 256 KB)
+        const uint64_t ad0 = umma_desc(smem_u32(sA), 128, sbo);
+        const uint32_t b0 = smem_u32(sB + bi * buf_bytes);
+        const uint64_t bd0 = umma_desc(b0, 128, sbo);
+        const uint64_t bd1 = umma_desc(b0 + p.un * p.kc * 2, 128, sbo);
+        const uint64_t bd2 = umma_desc(b0 + 2 * p.un * p.kc * 2, 128, sbo);
+        const uint32_t dcol = u.tmem + c * p.un;
         for (int kb = 0; kb < nkb; ++kb) {
-          const uint64_t ad = umma_desc(a0 + kb * 256, 128, sbo);
-#pragma unroll
-          for (int sp = 0; sp < 3; ++sp) {
-            const uint64_t bd = umma_desc(b0 + sp * (kUmmaN * p.kc * 2) + kb * 256, 128, sbo);
-            umma_bf16(u.tmem + c * kUmmaN, ad, bd, idesc, kb > 0 || sp > 0);
-          }
+          const uint64_t step = static_cast<uint64_t>(kb) * 16u;
+          umma_bf16(dcol, ad0 + step, bd0 + step, idesc, kb > 0);
+          umma_bf16(dcol, ad0 + step, bd1 + step, idesc, true);
+          umma_bf16(dcol, ad0 + step, bd2 + step, idesc, true);
         }
         umma_commit(&mbar[bi]);
       }
@@ -411,32 +425,40 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
       else { wait1 = u.uses[1]++; pend1 = true; }
       if (c + 1 < nch) {
         // the MMAs of chunk c-1 may still read the other buffer
+        const uint64_t tm0 = clock_me ? global_ns() : 0;
         if (bi == 0 && pend1) { ok &= wait_mma(&mbar[1], wait1, p.limit_ns); pend1 = false; }
         if (bi == 1 && pend0) { ok &= wait_mma(&mbar[0], wait0, p.limit_ns); pend0 = false; }
-        load_b_chunk(p, slots, total, pass0 + (c + 1) * kUmmaN, sB + (bi ^ 1) * buf_bytes);
+        if (clock_me) p.ctrl->t_ns[12] += global_ns() - tm0;
+        load_b_chunk(p, slots, total, pass0 + (c + 1) * p.un, sB + (bi ^ 1) * buf_bytes);
       }
     }
+    const uint64_t tm1 = clock_me ? global_ns() : 0;
     if (pend0) ok &= wait_mma(&mbar[0], wait0, p.limit_ns);
     if (pend1) ok &= wait_mma(&mbar[1], wait1, p.limit_ns);
+    if (clock_me) p.ctrl->t_ns[12] += global_ns() - tm1;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      const uint64_t n = global_ns();
+      p.ctrl->t_ns[9] += n - t_mma0;
+      t_mma0 = n;
+    }
     tmem_fence_after();
     // epilogue: TMEM lane = row of the tile; warps w and w+4 share a lane quarter
     const int quarter = warp & 3;
     const int row = mt * 128 + quarter * 32 + lane;
-    for (int grp = warp >> 2; grp * 8 < pass_cols; grp += 2) {
-      float v[8];
-      tmem_ld8(u.tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * 8, v);
+    for (int grp = warp >> 2; grp * 32 < pass_cols; grp += 2) {
+      float v[32];
+      tmem_ld32(u.tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * 32, v);
       tmem_wait_ld();
       if (row < R) {
+        float *dst = p.partial + (static_cast<size_t>(kz) * p.cols_cap + pass0 + grp * 32) * R + row;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int col = pass0 + grp * 8 + j;
-          if (col < total)
-            p.partial[(static_cast<size_t>(kz) * p.cols_cap + col) * R + row] = v[j];
-        }
+        for (int j = 0; j < 32; ++j)
+          if (pass0 + grp * 32 + j < total) dst[static_cast<size_t>(j) * R] = v[j];
       }
     }
     tmem_fence_before();
     __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x == 0) p.ctrl->t_ns[10] += global_ns() - t_mma0;
   }
   return ok;
 }
@@ -486,6 +508,8 @@ struct Tables {
   uint8_t *run_head;     // [N+1]
   int16_t *run_pos;      // [N+1]
   uint8_t *vhead;        // [N+1]
+  float *run_hs;         // [N+1] score of each run's head (NaN: exhausted)
+  float *vhs;            // [N+1] the same for the virtual walk
   int16_t *par;          // [N+1] parents of the output rows
   float *scratch;
 };
@@ -503,23 +527,22 @@ __device__ Tables tables(const ChainParams &p, unsigned char *smem) {
   t.run_head = reinterpret_cast<uint8_t *>(smem + p.sm_run_head);
   t.run_pos = reinterpret_cast<int16_t *>(smem + p.sm_run_pos);
   t.vhead = reinterpret_cast<uint8_t *>(smem + p.sm_vhead);
+  t.run_hs = reinterpret_cast<float *>(smem + p.sm_run_hs);
+  t.vhs = reinterpret_cast<float *>(smem + p.sm_vhs);
   t.par = reinterpret_cast<int16_t *>(smem + p.sm_par);
   t.scratch = reinterpret_cast<float *>(smem + p.sm_scratch);
   return t;
 }
 
-// Warp-wide best run head under (score desc, run index asc) using heads `hd`.
-// Returns the run index or -1 when every run is exhausted.
-__device__ __forceinline__ int best_run(const ChainParams &p, const Tables &t, const uint8_t *hd,
-                                        int n_runs, int lane) {
+// Warp-wide best run head under (score desc, run index asc). hs[r] is the
+// score of run r's current head, NaN once the run is exhausted. Returns the run
+// index or -1 when every run is exhausted.
+__device__ __forceinline__ int best_run(const float *hs, int n_runs, int lane) {
   float best = 0.f;
   int br = -1;
   for (int r = lane; r < n_runs; r += 32) {
-    const int h = hd[r];
-    if (h < p.k) {
-      const float s = t.child_score[t.run_e[r] * p.k + h];
-      if (br < 0 || s > best) { best = s; br = r; }   // r ascending within a lane
-    }
+    const float s = hs[r];
+    if (s == s && (br < 0 || s > best)) { best = s; br = r; }   // r ascending within a lane
   }
 #pragma unroll
   for (int m = 16; m; m >>= 1) {
@@ -529,6 +552,11 @@ __device__ __forceinline__ int best_run(const ChainParams &p, const Tables &t, c
     if (take) { best = ob; br = orr; }
   }
   return br;
+}
+
+// score of entry h of run r's children, NaN past the last child
+__device__ __forceinline__ float head_score(const ChainParams &p, const Tables &t, int er, int h) {
+  return (h < p.k) ? t.child_score[er * p.k + h] : __int_as_float(0x7fc00000);
 }
 
 // The GEMM input column of a state: fp32 (CUDA-core path) or three bf16 terms
@@ -642,6 +670,7 @@ __device__ void score_node(const ChainParams &p, const Tables &t, float T, int b
   const int nq = p.r / 8;
   const int32_t *cid = p.cand_id + row * p.M;
   const float *cval = p.cand_val + row * p.M;
+  const uint64_t t_in = (blockIdx.x == 0 && threadIdx.x == 0) ? global_ns() : 0;
   int my_id[SLOTS];
   float my_base[SLOTS];
 #pragma unroll
@@ -659,6 +688,15 @@ __device__ void score_node(const ChainParams &p, const Tables &t, float T, int b
     for (int q = lane; q < p.r; q += 32) hbuf[q] = siluf_(__ldg(U + q) + ldcg(pv + q));
     __syncwarp();
   }
+  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
+  uint64_t tc = 0;
+  if (clock_me) {
+    // consume the loads above before reading the clock
+    volatile float sink = h[0] + my_base[0] + static_cast<float>(my_id[0]);
+    (void)sink;
+    tc = global_ns();
+    p.ctrl->t_ns[13] += tc - t_in;
+  }
   const float ninf = -__int_as_float(0x7f800000);
   uint64_t key[SLOTS];
   float Lv[SLOTS];
@@ -666,19 +704,38 @@ __device__ void score_node(const ChainParams &p, const Tables &t, float T, int b
   for (int s = 0; s < SLOTS; ++s) {
     key[s] = 0ull;
     Lv[s] = ninf;
+    float my_dl = 0.f;   // correction of candidate s*32 + lane
+    constexpr int G = WDT == 1 ? 16 : 8;   // candidate rows in flight
 #pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {
-      const int c0 = s * 32 + c8 * 8;
+    for (int cg = 0; cg < 32 / G; ++cg) {
+      const int c0 = s * 32 + cg * G;
       if (c0 < p.M) {                        // warp-uniform
-        constexpr int G = 8;
         float acc[G];
         int ids[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          ids[g] = __shfl_sync(kFull, my_id[s], c8 * 8 + g);
+          ids[g] = __shfl_sync(kFull, my_id[s], cg * G + g);
           acc[g] = 0.f;
         }
-        if (SMALL_R) {
+        if (SMALL_R && WDT == 1) {
+          uint4 raw[G];                      // eight bf16 weights per row and lane
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            raw[g] = (ids[g] >= 0 && lane < nq)
+                         ? __ldg(reinterpret_cast<const uint4 *>(
+                               static_cast<const uint16_t *>(p.W2) +
+                               static_cast<size_t>(ids[g]) * p.r + 8 * lane))
+                         : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const uint32_t w4[4] = {raw[g].x, raw[g].y, raw[g].z, raw[g].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc[g] = fmaf(__uint_as_float(w4[i] << 16), h[2 * i], acc[g]);
+              acc[g] = fmaf(__uint_as_float(w4[i] & 0xffff0000u), h[2 * i + 1], acc[g]);
+            }
+          }
+        } else if (SMALL_R) {
           float wf[G][8];
 #pragma unroll
           for (int g = 0; g < G; ++g) {
@@ -714,14 +771,19 @@ __device__ void score_node(const ChainParams &p, const Tables &t, float T, int b
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float dl = warp_sum(acc[g]);
-          if (c8 * 8 + g == lane && ids[g] >= 0) {
-            const float L = __fdiv_rn(my_base[s] + dl, T);
-            Lv[s] = L;
-            key[s] = make_key(L, static_cast<uint32_t>(ids[g]));
-          }
+          if (cg * G + g == lane) my_dl = dl;
         }
       }
     }
+    if (my_id[s] >= 0) {
+      Lv[s] = __fdiv_rn(my_base[s] + my_dl, T);
+      key[s] = make_key(Lv[s], static_cast<uint32_t>(my_id[s]));
+    }
+  }
+  if (clock_me) {
+    const uint64_t n = global_ns();
+    p.ctrl->t_ns[14] += n - tc;
+    tc = n;
   }
   float mx = ninf;
 #pragma unroll
@@ -746,6 +808,7 @@ __device__ void score_node(const ChainParams &p, const Tables &t, float T, int b
       t.child_exp[e * p.k + i] = -1;
     }
   }
+  if (clock_me) p.ctrl->t_ns[15] += global_ns() - tc;
 }
 
 __device__ void write_row(const ChainParams &p, int b, int pos, int tok, int par, int dep,
@@ -791,7 +854,7 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
   bool done = false;
   while (true) {
     if (count >= p.N) { done = true; break; }
-    const int r = best_run(p, t, t.run_head, n_runs, lane);
+    const int r = best_run(t.run_hs, n_runs, lane);
     if (r < 0) { done = true; break; }
     const int h = t.run_head[r], er = t.run_e[r];
     const int dep = t.exp_depth[er] + 1, pos = count + 1;
@@ -803,9 +866,11 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
                 t.child_score[er * p.k + h]);
       t.par[pos] = t.run_pos[r];
       t.run_head[r] = static_cast<uint8_t>(h + 1);
+      t.run_hs[r] = head_score(p, t, er, h + 1);
       if (need) {
         t.run_e[n_runs] = static_cast<int16_t>(ce);
         t.run_head[n_runs] = 0;
+        t.run_hs[n_runs] = head_score(p, t, ce, 0);
         t.run_pos[n_runs] = static_cast<int16_t>(pos);
       }
     }
@@ -820,12 +885,15 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
   }
   // choose the stalled node plus up to P-1 of the next frontier nodes in order
   const int spec_left = p.e_cap - p.N - ts.spec_used;
-  for (int r = lane; r < n_runs; r += 32) t.vhead[r] = t.run_head[r];
+  for (int r = lane; r < n_runs; r += 32) {
+    t.vhead[r] = t.run_head[r];
+    t.vhs[r] = t.run_hs[r];
+  }
   __syncwarp();
   int nsel = 0, nspec = 0, i = 0;
   int e_count = ts.e_count;
   while (nsel < p.P) {
-    const int r = best_run(p, t, t.vhead, n_runs, lane);
+    const int r = best_run(t.vhs, n_runs, lane);
     if (r < 0) break;
     ++i;
     if (count + i >= p.N) break;
@@ -835,6 +903,7 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
     const bool take = fresh && (nsel == 0 || nspec < spec_left);
     if (lane == 0) {
       t.vhead[r] = static_cast<uint8_t>(h + 1);
+      t.vhs[r] = head_score(p, t, er, h + 1);
       if (take) {
         const int e = e_count + nsel;
         t.child_exp[er * p.k + h] = static_cast<int16_t>(e);
@@ -855,7 +924,7 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
   // warm L2 with the prepared rows of the frontier nodes most likely to be
   // expanded at the next step (the next 2P unexpanded entries in order)
   for (int extra = 0; extra < 2 * p.P;) {
-    const int r = best_run(p, t, t.vhead, n_runs, lane);
+    const int r = best_run(t.vhs, n_runs, lane);
     if (r < 0) break;
     const int h = t.vhead[r], er = t.run_e[r];
     if (t.exp_depth[er] + 1 < p.D && t.child_exp[er * p.k + h] < 0) {
@@ -864,7 +933,10 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
                     static_cast<uint32_t>(12u * p.d_s));
       ++extra;
     }
-    if (lane == 0) t.vhead[r] = static_cast<uint8_t>(h + 1);
+    if (lane == 0) {
+      t.vhead[r] = static_cast<uint8_t>(h + 1);
+      t.vhs[r] = head_score(p, t, er, h + 1);
+    }
     __syncwarp();
   }
   if (lane == 0) {
@@ -949,6 +1021,8 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
     __syncthreads();
     return;
   }
+  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
+  uint64_t t0 = clock_me ? global_ns() : 0;
   // 1. children of the nodes expanded by the last GEMM (one warp per node)
   float *hbuf = t.scratch + warp * p.r;   // used only when r > 256
   for (int i = warp; i < ncols; i += kWarps) {
@@ -960,12 +1034,15 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
   __syncthreads();
   if (threadIdx.x == 0 && ts.n_runs == 0) {  // the root's children form the first run
     t.run_e[0] = 0; t.run_head[0] = 0; t.run_pos[0] = 0;
+    t.run_hs[0] = head_score(p, t, 0, 0);
     ts.n_runs = 1;
   }
   __syncthreads();
+  if (clock_me) { const uint64_t n = global_ns(); p.ctrl->t_ns[6] += n - t0; t0 = n; }
   // 2. canonical pops, then the next expansions
   if (warp == 0) replay_and_select(p, t, ts, b, lane);
   __syncthreads();
+  if (clock_me) { const uint64_t n = global_ns(); p.ctrl->t_ns[7] += n - t0; t0 = n; }
   if (ts.done == 2) { finalize(p, t, ts, b, true); return; }
   // 3. GRU states of the chosen nodes
   if (threadIdx.x < ts.n_sel) {
@@ -980,6 +1057,7 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
   __syncthreads();
   gru_jobs(p, ts.jobs, ts.n_sel);
   __syncthreads();
+  if (clock_me) p.ctrl->t_ns[8] += global_ns() - t0;
 }
 
 template <int WDT, int SLOTS>
@@ -1084,10 +1162,12 @@ static int chain_smem_layout(const Plan &pl, int e_cap, int wave, ChainParams *c
   cp->sm_run_pos = off;     off = al(off + n1 * 2, 16);
   cp->sm_vhead = off;       off = al(off + n1, 16);
   cp->sm_par = off;         off = al(off + n1 * 2, 16);
+  cp->sm_run_hs = off;      off = al(off + n1 * 4, 16);
+  cp->sm_vhs = off;         off = al(off + n1 * 4, 16);
   cp->sm_A = cp->sm_B = cp->sm_mbar = cp->sm_tmem = 0;
   if (pl.umma) {
     cp->sm_A = off = al(off, 128);    off += 128 * pl.kc * 2;
-    cp->sm_B = off = al(off, 128);    off += 2 * 3 * kUmmaN * pl.kc * 2;
+    cp->sm_B = off = al(off, 128);    off += 2 * 3 * pl.umma_n * pl.kc * 2;
     cp->sm_mbar = off = al(off, 16);  off += 16;
     cp->sm_tmem = off;                off += 16;
   }
@@ -1146,7 +1226,7 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.gin = reinterpret_cast<float *>(w + pl.off_gin);
   cp.pbuf = reinterpret_cast<float *>(w + pl.off_p);
   cp.colexp = reinterpret_cast<int *>(w + pl.off_colexp);
-  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc;
+  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc; cp.un = pl.umma_n;
   cp.cols_cap = pl.wave * pl.spec;
   cp.partial = pl.umma ? reinterpret_cast<float *>(w + pl.off_partial) : nullptr;
   cp.gin16 = pl.umma ? reinterpret_cast<uint16_t *>(w + pl.off_gin16) : nullptr;

@@ -35,18 +35,17 @@ __device__ __forceinline__ void load_tile_row8(const void *base, size_t ld, int 
   }
 }
 
-// Split K: blockIdx.z takes one K chunk; with ksplit > 1 every block writes its
-// partial tile and the last block of the tile (atomic ticket, no waiting) adds
-// the partials in chunk order, so the result does not depend on timing.
+// Split K: blockIdx.z takes one K chunk. With ksplit == 1 the block writes C;
+// otherwise it writes its partial tile and splitk_reduce_kernel adds the
+// partials in chunk order (deterministic). The next K tile is loaded into
+// registers while the current one is multiplied (double-buffered tiles).
 template <int ADT, int BDT>
 __global__ void __launch_bounds__(kThreads)
 gemm_nt_kernel(int M, int N, int K, const void *__restrict__ A, size_t lda,
                const void *__restrict__ B, size_t ldb, const float *__restrict__ bias,
-               float *__restrict__ C, size_t ldc, int ksplit, float *__restrict__ partial,
-               unsigned *__restrict__ tickets) {
-  __shared__ int s_last;
-  __shared__ __align__(16) float As[BK][BM + 4];
-  __shared__ __align__(16) float Bs[BK][BN + 4];
+               float *__restrict__ C, size_t ldc, int ksplit, float *__restrict__ partial) {
+  __shared__ __align__(16) float As[2][BK][BM + 4];
+  __shared__ __align__(16) float Bs[2][BK][BN + 4];
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
@@ -60,24 +59,31 @@ gemm_nt_kernel(int M, int N, int K, const void *__restrict__ A, size_t lda,
 
   const int kchunk = ((K + ksplit - 1) / ksplit + BK - 1) / BK * BK;
   const int kbeg = blockIdx.z * kchunk, kend = min(K, kbeg + kchunk);
-  for (int k0 = kbeg; k0 < kend; k0 += BK) {
-    float fa[8], fb[8];
-    load_tile_row8<ADT>(A, lda, m0 + lr, M, k0 + lk, kend, fa);
-    load_tile_row8<BDT>(B, ldb, n0 + lr, N, k0 + lk, kend, fb);
-    __syncthreads();
+  float fa[8], fb[8];
+  if (kbeg < kend) {
+    load_tile_row8<ADT>(A, lda, m0 + lr, M, kbeg + lk, kend, fa);
+    load_tile_row8<BDT>(B, ldb, n0 + lr, N, kbeg + lk, kend, fb);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      As[lk + i][lr] = fa[i];
-      Bs[lk + i][lr] = fb[i];
+      As[0][lk + i][lr] = fa[i];
+      Bs[0][lk + i][lr] = fb[i];
     }
-    __syncthreads();
+  }
+  __syncthreads();
+  int buf = 0;
+  for (int k0 = kbeg; k0 < kend; k0 += BK) {
+    const bool more = k0 + BK < kend;
+    if (more) {
+      load_tile_row8<ADT>(A, lda, m0 + lr, M, k0 + BK + lk, kend, fa);
+      load_tile_row8<BDT>(B, ldb, n0 + lr, N, k0 + BK + lk, kend, fb);
+    }
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float a[8], b[8];
-      float4 a0 = *reinterpret_cast<const float4 *>(&As[kk][ty * 4]);
-      float4 a1 = *reinterpret_cast<const float4 *>(&As[kk][64 + ty * 4]);
-      float4 b0 = *reinterpret_cast<const float4 *>(&Bs[kk][tx * 4]);
-      float4 b1 = *reinterpret_cast<const float4 *>(&Bs[kk][64 + tx * 4]);
+      float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][kk][ty * 4]);
+      float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][kk][64 + ty * 4]);
+      float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][tx * 4]);
+      float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][64 + tx * 4]);
       a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
       a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
       b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
@@ -87,66 +93,64 @@ gemm_nt_kernel(int M, int N, int K, const void *__restrict__ A, size_t lda,
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
-  }
-  if (ksplit == 1) {
+    if (more) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
-      if (m >= M) continue;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int n = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
-        if (n < N) C[static_cast<size_t>(m) * ldc + n] = acc[i][j] + (bias ? bias[n] : 0.f);
+      for (int i = 0; i < 8; ++i) {
+        As[buf ^ 1][lk + i][lr] = fa[i];
+        Bs[buf ^ 1][lk + i][lr] = fb[i];
       }
     }
-    return;
+    __syncthreads();
+    buf ^= 1;
   }
+  float *out = C;
+  size_t ldo = ldc;
+  if (ksplit > 1) {
+    out = partial + blockIdx.z * static_cast<size_t>(M) * N;
+    ldo = N;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int n = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+      if (n < N)
+        out[static_cast<size_t>(m) * ldo + n] =
+            acc[i][j] + ((ksplit == 1 && bias) ? bias[n] : 0.f);
+    }
+  }
+}
+
+// C = sum_z partial[z] (+ bias), four outputs per thread, chunks in order.
+__global__ void splitk_reduce_kernel(const float *__restrict__ partial, int ksplit, int M, int N,
+                                     const float *__restrict__ bias, float *__restrict__ C,
+                                     size_t ldc) {
   const size_t plane = static_cast<size_t>(M) * N;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
-    if (m >= M) continue;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int n = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
-      if (n < N) partial[blockIdx.z * plane + static_cast<size_t>(m) * N + n] = acc[i][j];
-    }
+  const size_t i4 = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i4 >= plane) return;
+  const int m = static_cast<int>(i4 / N), n = static_cast<int>(i4 % N);
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int z = 0; z < ksplit; ++z) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(partial + z * plane + i4));
+    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
   }
-  __threadfence();
-  __syncthreads();
-  const unsigned tile = blockIdx.y * gridDim.x + blockIdx.x;
-  if (threadIdx.x == 0) s_last = atomicAdd(tickets + tile, 1u) == static_cast<unsigned>(ksplit - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
-    if (m >= M) continue;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int n = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
-      if (n >= N) continue;
-      float sum = 0.f;
-      for (int z = 0; z < ksplit; ++z)
-        sum += __ldcg(partial + z * plane + static_cast<size_t>(m) * N + n);
-      C[static_cast<size_t>(m) * ldc + n] = sum + (bias ? bias[n] : 0.f);
-    }
-  }
-  if (threadIdx.x == 0) tickets[tile] = 0u;
+  if (bias) { s.x += bias[n]; s.y += bias[n + 1]; s.z += bias[n + 2]; s.w += bias[n + 3]; }
+  float *c = C + static_cast<size_t>(m) * ldc + n;
+  c[0] = s.x; c[1] = s.y; c[2] = s.z; c[3] = s.w;
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_nt(int M, int N, int K, const void *A, int a_dtype, size_t lda,
                            const void *B, int b_dtype, size_t ldb, const float *bias, float *C,
-                           size_t ldc, int ksplit, float *partial, unsigned *tickets,
-                           cudaStream_t st) {
+                           size_t ldc, int ksplit, float *partial, cudaStream_t st) {
   if (M <= 0 || N <= 0) return cudaSuccess;
-  if (ksplit < 1) ksplit = 1;
+  if (ksplit < 1 || N % 4) ksplit = 1;
   dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM, ksplit);
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-#define DT_GEMM_ARGS M, N, K, A, lda, B, ldb, bias, C, ldc, ksplit, partial, tickets
+#define DT_GEMM_ARGS M, N, K, A, lda, B, ldb, bias, C, ldc, ksplit, partial
   if (a_dtype == DT_F32 && b_dtype == DT_F32)
     gemm_nt_kernel<0, 0><<<grid, kThreads, 0, st>>>(DT_GEMM_ARGS);
   else if (a_dtype == DT_F32 && b_dtype == DT_BF16)
@@ -156,6 +160,11 @@ cudaError_t launch_gemm_nt(int M, int N, int K, const void *A, int a_dtype, size
   else
     gemm_nt_kernel<1, 1><<<grid, kThreads, 0, st>>>(DT_GEMM_ARGS);
 #undef DT_GEMM_ARGS
+  if (ksplit > 1) {
+    const size_t n4 = (static_cast<size_t>(M) * N + 3) / 4;
+    splitk_reduce_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(
+        partial, ksplit, M, N, bias, C, ldc);
+  }
   return cudaGetLastError();
 }
 

@@ -20,6 +20,7 @@ struct Plan {
   int proj_ksplit;     // K split of the projection GEMM
   int umma;            // search GEMM on tcgen05 (bf16 weights)
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
+  int umma_n;          // columns per MMA (B buffer width)
   int num_sms;
   int chain_grid;      // co-resident blocks of the search kernel
   int wave;            // requests per search launch (<= chain_grid)
@@ -39,9 +40,12 @@ struct Ctrl {
   unsigned int steps;      // lockstep steps of the last search launch
   unsigned int expansions; // expansions of the last search launch
   unsigned int pad[2];
-  // block 0 of the last search launch: ns spent in GEMM, barrier, reduction,
-  // barrier, tail, barrier (summed over steps)
-  unsigned long long t_ns[6];
+  // block 0 of the last search launch, ns summed over steps: GEMM, barrier,
+  // reduction, barrier, tail, barrier; tail parts: scoring, pops and
+  // selection, GRU; GEMM parts: MMA loop, epilogue
+  // then: GEMM waits for B copies, GEMM waits for MMA completion; scoring of
+  // one node (warp 0): operand loads, candidate loop, softmax + sort + write
+  unsigned long long t_ns[16];
   // followed by: unsigned row_ticket[batch * D]; int req_flags[batch]; gemm tickets
 };
 
@@ -57,12 +61,11 @@ cudaError_t launch_topm(const Plan &p, const float *base_logits, void *ws, int32
 
 // C[m][n] = sum_k A[m][k] * B[n][k] (+ bias[n]); fp32 accumulation.
 // a_dtype/b_dtype: DT_F32 or DT_BF16.
-// ksplit > 1 splits K over blockIdx.z; partial: ksplit*M*N floats, tickets:
-// gemm_tiles(M, N) zeroed counters (left zeroed on return).
+// ksplit > 1 splits K over blockIdx.z (partial: ksplit*M*N floats) and adds a
+// reduction launch; requires N % 4 == 0 (else ksplit is forced to 1).
 cudaError_t launch_gemm_nt(int M, int N, int K, const void *A, int a_dtype, size_t lda,
                            const void *B, int b_dtype, size_t ldb, const float *bias, float *C,
-                           size_t ldc, int ksplit, float *partial, unsigned *tickets,
-                           cudaStream_t st);
+                           size_t ldc, int ksplit, float *partial, cudaStream_t st);
 int gemm_tiles(int M, int N);
 
 // The best-first search for requests [b0, b0 + nb).

@@ -105,14 +105,7 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return DT_ERR_CUDA;
   const int smem_max = smem_optin - static_cast<int>(fa.sharedSizeBytes);
   int e_cap = d.N + 1 + (p->spec > 1 ? d.N + 1 : 0);
-  // widest MMA column block (fewer B-load round trips) that fits
-  p->umma_n = 32;
-  int smem = 0;
-  for (int un : {64, 48, 32}) {
-    p->umma_n = un;
-    smem = chain_smem_bytes(*p, e_cap, wave);
-    if (smem <= smem_max) break;
-  }
+  int smem = chain_smem_bytes(*p, e_cap, wave);
   while (smem > smem_max && e_cap > d.N + 1) {
     e_cap = d.N + 1 + (e_cap - d.N - 1) / 2;
     smem = chain_smem_bytes(*p, e_cap, wave);
@@ -160,7 +153,9 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   p->off_partial = off;
   off = al(off + (p->umma ? sizeof(float) * p->ks * cols * (3 * d.d_s + d.r) : 0));
   p->off_gin16 = off;
-  off = al(off + (p->umma ? sizeof(uint16_t) * cols * 3 * d.d_s : 0));
+  // B operand of the tensor-core GEMM: passes of 256 columns, K padded to ks * kc
+  const size_t cols256 = (cols + 255) / 256 * 256;
+  off = al(off + (p->umma ? sizeof(uint16_t) * cols256 * 3 * p->ks * p->kc : 0));
   p->off_end = off;
   return DT_OK;
 }

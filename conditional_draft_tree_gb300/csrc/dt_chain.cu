@@ -74,9 +74,9 @@ struct ChainParams {
   int *colexp, *col_count;
   // tensor-core GEMM path (bf16 weights): A tiles of 128 rows x kc K stay in
   // shared memory; the input columns arrive as three bf16 terms per state
-  int umma, n_mt, ks, kc, un, cols_cap;   // un: columns per MMA (one B buffer)
-  float *partial;      // [ks][cols_cap][R] per-K-chunk partial products
-  uint16_t *gin16;     // [cols_cap][3][d_s]
+  int umma, n_mt, ks, kc, cols_cap;
+  float *partial;      // [ks][cols_cap][R] per-K-chunk partial products, by slot
+  uint16_t *gin16;     // B operand in tile layout (bcol_index)
   Ctrl *ctrl;
   const int *req_flags;
   int32_t *tokens, *parents, *depths;
@@ -328,169 +328,206 @@ __device__ void load_a_tile(const ChainParams &p, unsigned char *sA) {
   }
 }
 
-// B chunk: columns [c0, c0 + un) of the active list, three bf16 terms, K range
-// of this block, into one buffer (zero for missing columns and k >= d_s), with
-// asynchronous 16-byte copies so that all of them are in flight at once.
-__device__ void load_b_chunk(const ChainParams &p, const int *slots, int total, int c0,
-                             unsigned char *sB) {
-  const int k0 = (blockIdx.x % p.ks) * p.kc;
-  const int kg = p.kc / 8;
-  const int per_split = p.un * p.kc * 2;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int sp = 0; sp < 3; ++sp) {
-    for (int n = warp; n < p.un; n += kWarps) {
-      const int c = c0 + n;
-      const uint16_t *rowp =
-          (c < total) ? p.gin16 + (static_cast<size_t>(slots[c]) * 3 + sp) * p.d_s : p.gin16;
-      unsigned char *dst = sB + sp * per_split + umma_offset(n, 0, p.kc);
-      for (int q = lane; q < kg; q += 32) {
-        const int k = k0 + q * 8;
-        const bool live = c < total && k < p.d_s;
-        cp_async16(dst + q * 128, live ? rowp + k : p.gin16, live ? 16u : 0u);
-      }
-    }
-  }
-  cp_async_commit();
-}
+// B operand in global memory, already in the tensor cores' tile layout. Node
+// column `slot` lives in pass slot / 256 at column c = slot % 256; K index k in
+// chunk kz = k / kc at slice (k % kc) / 16. For each (pass, chunk, slice) the
+// three bf16 terms follow one another, each a K-major no-swizzle tile of 256
+// columns x 16 K (8 KB), so that one slice of a term is a single contiguous
+// block whose first 32 * n bytes hold columns [0, n).
+constexpr int kTermBytes = 256 * 16 * 2;
+constexpr int kSliceBytes = 3 * kTermBytes;
+constexpr int kBufs = 4;                       // B slices in flight
 
-// Completion of MMA batch number `use` of a buffer; an expired wait is retried
-// once so that no MMA is left in flight, and reported as failure.
-__device__ __forceinline__ bool wait_mma(uint64_t *mbar, uint32_t use, uint64_t limit_ns) {
-  if (mbar_wait(mbar, use & 1u, limit_ns)) return true;
-  mbar_wait(mbar, use & 1u, limit_ns);
-  return false;
+__device__ __forceinline__ size_t bcol_index(const ChainParams &p, int slot, int k) {
+  const int kz = k / p.kc, kk = k - kz * p.kc;
+  const int c = slot & 255;
+  const size_t blk = (static_cast<size_t>((slot >> 8) * p.ks + kz) * (p.kc >> 4) + (kk >> 4)) * 3;
+  return blk * (kTermBytes / 2) +
+         static_cast<size_t>(((c >> 3) * 256 + ((kk >> 3) & 1) * 128 + (c & 7) * 16) / 2 + (kk & 7));
 }
 
 struct UmmaState {
   uint32_t tmem;      // TMEM base column address
-  uint32_t uses[2];   // commits issued on each B-buffer mbarrier
+  uint32_t next;      // global index of the next B slice (buffer = next % kBufs)
 };
 
 // Partial products of this block's (M tile, K chunk) for every active column,
-// written to p.partial[kz][column][row]. D = A B^T with A = 128 weight rows
-// (K-major, resident) and B = 32 columns of hi / mid / lo terms accumulated into
-// the same fp32 TMEM tile. Returns false if an MMA completion wait expired.
+// written to p.partial[kz][slot][row]. D (TMEM, 128 rows x up to 256 node
+// columns) = A B^T, A = 128 weight rows (K-major, resident), B = the node
+// columns as hi / mid / lo bf16 terms; one MMA per (K step, term) covers a
+// whole pass of 256 columns, since an MMA costs about the same for any N up to
+// 256. Thread 0 runs the pipeline (bulk copies into kBufs slice buffers, MMAs,
+// commits); all warps read the accumulators back.
 __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsigned char *scratch,
                                 UmmaState &u) {
+  __shared__ int s_hi[16];           // per pass: last active column + 1
+  __shared__ uint32_t s_mask[16][8]; // per pass: active columns
   int *slots = reinterpret_cast<int *>(scratch);
   const int total = compact_slots(p, slots);
   if (total == 0 || blockIdx.x >= p.n_mt * p.ks) return true;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int mt = blockIdx.x / p.ks, kz = blockIdx.x % p.ks;
   const int R = 3 * p.d_s + p.r;
+  const int n_pass = (p.cols_cap + 255) >> 8;
+  if (threadIdx.x < 16 * 9) {
+    if (threadIdx.x < 16) s_hi[threadIdx.x] = 0;
+    else (&s_mask[0][0])[threadIdx.x - 16] = 0u;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < total; i += kThreads) {
+    const int slot = slots[i], c = slot & 255;
+    atomicMax(&s_hi[slot >> 8], c + 1);
+    atomicOr(&s_mask[slot >> 8][c >> 5], 1u << (c & 31));
+  }
+  __syncthreads();
   unsigned char *sA = smem + p.sm_A;
   unsigned char *sB = smem + p.sm_B;
-  uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
-  const int buf_bytes = 3 * p.un * p.kc * 2;
-  const uint32_t idesc = umma_idesc_bf16(128, p.un);
-  const int pass_max = (static_cast<int>(kTmemCols) / p.un) * p.un;
-  const uint32_t sbo = 16u * p.kc;
-  const int nkb = p.kc / 16;
-  bool ok = true;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
+  uint64_t *empty = full + kBufs;
+  const int nkb = p.kc >> 4;
   const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
-  uint64_t t_mma0 = global_ns();
-  for (int pass0 = 0; pass0 < total; pass0 += pass_max) {
-    const int pass_cols = min(pass_max, total - pass0);
-    const int nch = (pass_cols + p.un - 1) / p.un;
-    uint32_t wait0 = 0u, wait1 = 0u;   // commit numbers awaited on buffers 0 / 1
-    bool pend0 = false, pend1 = false;
-    load_b_chunk(p, slots, total, pass0, sB);
-    for (int c = 0; c < nch; ++c) {
-      const int bi = c & 1;
-      const uint64_t tw0 = clock_me ? global_ns() : 0;
-      cp_async_wait_all();
-      fence_async_smem();
-      tmem_fence_before();
-      __syncthreads();
-      tmem_fence_after();
-      if (clock_me) p.ctrl->t_ns[11] += global_ns() - tw0;
-      if (threadIdx.x == 0) {
-        // descriptors once; a K step of 16 moves the start address by 256 bytes
-        // (16 in the encoded field, which never carries: addresses < 256 KB)
-        const uint64_t ad0 = umma_desc(smem_u32(sA), 128, sbo);
-        const uint32_t b0 = smem_u32(sB + bi * buf_bytes);
-        const uint64_t bd0 = umma_desc(b0, 128, sbo);
-        const uint64_t bd1 = umma_desc(b0 + p.un * p.kc * 2, 128, sbo);
-        const uint64_t bd2 = umma_desc(b0 + 2 * p.un * p.kc * 2, 128, sbo);
-        const uint32_t dcol = u.tmem + c * p.un;
-        for (int kb = 0; kb < nkb; ++kb) {
-          const uint64_t step = static_cast<uint64_t>(kb) * 16u;
-          umma_bf16(dcol, ad0 + step, bd0 + step, idesc, kb > 0);
-          umma_bf16(dcol, ad0 + step, bd1 + step, idesc, true);
-          umma_bf16(dcol, ad0 + step, bd2 + step, idesc, true);
-        }
-        umma_commit(&mbar[bi]);
-      }
-      if (bi == 0) { wait0 = u.uses[0]++; pend0 = true; }
-      else { wait1 = u.uses[1]++; pend1 = true; }
-      if (c + 1 < nch) {
-        // the MMAs of chunk c-1 may still read the other buffer
-        const uint64_t tm0 = clock_me ? global_ns() : 0;
-        if (bi == 0 && pend1) { ok &= wait_mma(&mbar[1], wait1, p.limit_ns); pend1 = false; }
-        if (bi == 1 && pend0) { ok &= wait_mma(&mbar[0], wait0, p.limit_ns); pend0 = false; }
-        if (clock_me) p.ctrl->t_ns[12] += global_ns() - tm0;
-        load_b_chunk(p, slots, total, pass0 + (c + 1) * p.un, sB + (bi ^ 1) * buf_bytes);
-      }
-    }
-    const uint64_t tm1 = clock_me ? global_ns() : 0;
-    if (pend0) ok &= wait_mma(&mbar[0], wait0, p.limit_ns);
-    if (pend1) ok &= wait_mma(&mbar[1], wait1, p.limit_ns);
-    if (clock_me) p.ctrl->t_ns[12] += global_ns() - tm1;
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-      const uint64_t n = global_ns();
-      p.ctrl->t_ns[9] += n - t_mma0;
-      t_mma0 = n;
-    }
-    tmem_fence_after();
-    // epilogue: TMEM lane = row of the tile; warps w and w+4 share a lane quarter
-    const int quarter = warp & 3;
-    const int row = mt * 128 + quarter * 32 + lane;
-    for (int grp = warp >> 2; grp * 32 < pass_cols; grp += 2) {
-      float v[32];
-      tmem_ld32(u.tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * 32, v);
-      tmem_wait_ld();
-      if (row < R) {
-        float *dst = p.partial + (static_cast<size_t>(kz) * p.cols_cap + pass0 + grp * 32) * R + row;
+  bool ok = true;
+  for (int pass = 0; pass < n_pass; ++pass) {
+    const int hi = s_hi[pass];
+    if (hi == 0) continue;
+    const uint64_t t0 = clock_me ? global_ns() : 0;
+    if (threadIdx.x == 0) {
+      const int npad = (hi + 15) & ~15;
+      const uint32_t bytes = static_cast<uint32_t>(npad) * 32;
+      const uint32_t idesc = umma_idesc_bf16(128, npad);
+      const unsigned char *src = reinterpret_cast<const unsigned char *>(p.gin16) +
+                                 static_cast<size_t>(pass * p.ks + kz) * nkb * kSliceBytes;
+      const uint32_t g0 = u.next;
+      fence_async_global();   // columns written before the grid barrier -> bulk reads
+      auto issue = [&](int s) {
+        const uint32_t g = g0 + s, buf = g % kBufs;
+        // the buffer's previous slice must be consumed by its MMAs
+        if (g >= kBufs) ok &= mbar_wait(&empty[buf], ((g / kBufs) - 1) & 1u, p.limit_ns);
+        mbar_expect_tx(&full[buf], 3 * bytes);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (pass0 + grp * 32 + j < total) dst[static_cast<size_t>(j) * R] = v[j];
+        for (int sp = 0; sp < 3; ++sp)
+          bulk_g2s(sB + buf * kSliceBytes + sp * kTermBytes,
+                   src + static_cast<size_t>(s) * kSliceBytes + sp * kTermBytes, bytes,
+                   &full[buf]);
+      };
+      for (int s = 0; s < kBufs && s < nkb; ++s) issue(s);
+      uint64_t t_wait = 0;
+      for (int s = 0; s < nkb; ++s) {
+        const uint32_t g = g0 + s, buf = g % kBufs;
+        const uint64_t tw = clock_me ? global_ns() : 0;
+        ok &= mbar_wait(&full[buf], (g / kBufs) & 1u, p.limit_ns);
+        if (clock_me) t_wait += global_ns() - tw;
+        tmem_fence_after();
+        const uint64_t ad = umma_desc(smem_u32(sA) + s * 256, 128, 16u * p.kc);
+        const uint32_t b0 = smem_u32(sB + buf * kSliceBytes);
+#pragma unroll
+        for (int sp = 0; sp < 3; ++sp)
+          umma_bf16(u.tmem, ad, umma_desc(b0 + sp * kTermBytes, 128, 256), idesc, s > 0 || sp > 0);
+        umma_commit(&empty[buf]);
+        // refill the buffer of the previous slice (its MMAs were issued one slice ago)
+        if (s >= 1 && s + kBufs - 1 < nkb) issue(s + kBufs - 1);
+      }
+      u.next = g0 + nkb;
+      const uint32_t last = u.next - 1;
+      const uint64_t tm = clock_me ? global_ns() : 0;
+      ok &= mbar_wait(&empty[last % kBufs], (last / kBufs) & 1u, p.limit_ns);
+      if (clock_me) {
+        p.ctrl->t_ns[11] += t_wait;
+        p.ctrl->t_ns[12] += global_ns() - tm;
       }
     }
     tmem_fence_before();
     __syncthreads();
-    if (blockIdx.x == 0 && threadIdx.x == 0) p.ctrl->t_ns[10] += global_ns() - t_mma0;
+    tmem_fence_after();
+    const uint64_t t1 = clock_me ? global_ns() : 0;
+    if (clock_me) p.ctrl->t_ns[9] += t1 - t0;
+    // epilogue: TMEM lane = row of the tile; warps w and w+4 share a lane quarter
+    const int quarter = warp & 3;
+    const int row = mt * 128 + quarter * 32 + lane;
+    for (int grp = warp >> 2; grp * 32 < hi; grp += 2) {
+      const uint32_t m = s_mask[pass][grp];
+      if (m == 0u) continue;
+      float v[32];
+      tmem_ld32(u.tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * 32, v);
+      tmem_wait_ld();
+      if (row < R) {
+        float *dst = p.partial +
+                     (static_cast<size_t>(kz) * p.cols_cap + pass * 256 + grp * 32) * R + row;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if ((m >> j) & 1u) dst[static_cast<size_t>(j) * R] = v[j];
+      }
+    }
+    tmem_fence_before();
+    __syncthreads();
+    if (clock_me) p.ctrl->t_ns[10] += global_ns() - t1;
   }
   return ok;
 }
 
-// Sum of the K-chunk partials (fixed order) + b_hh into gh_store / pbuf.
+// Sum of the K-chunk partials (fixed order) + b_hh into gh_store / pbuf. Each
+// thread takes kRI float4 items at a time and, for up to kRZ chunks, issues all
+// their loads before adding, so that the L2 latency is paid about once.
+constexpr int kRI = 3;
+constexpr int kRZ = 6;
+
+__device__ __forceinline__ void store_reduced(const ChainParams &p, int slot, int row, float4 acc) {
+  const int ds = p.d_s;
+  if (row < 3 * ds) {
+    const int b = slot / p.P;
+    const int e = __ldcg(p.colexp + slot);
+    const int e_slot = (e == kState0) ? p.e_cap : e;
+    if (p.b_hh) {
+      acc.x += p.b_hh[row]; acc.y += p.b_hh[row + 1];
+      acc.z += p.b_hh[row + 2]; acc.w += p.b_hh[row + 3];
+    }
+    *reinterpret_cast<float4 *>(
+        p.gh_store + (static_cast<size_t>(b) * (p.e_cap + 1) + e_slot) * 3 * ds + row) = acc;
+  } else {
+    *reinterpret_cast<float4 *>(p.pbuf + static_cast<size_t>(slot) * p.r + (row - 3 * ds)) = acc;
+  }
+}
+
 __device__ void reduce_phase(const ChainParams &p, unsigned char *scratch) {
   int *slots = reinterpret_cast<int *>(scratch);
   const int total = compact_slots(p, slots);
-  const int ds = p.d_s, R = 3 * ds + p.r, R4 = R / 4;
+  const int R = 3 * p.d_s + p.r, R4 = R / 4;
   const size_t plane = static_cast<size_t>(p.cols_cap) * R;
-  for (int i = blockIdx.x * kThreads + threadIdx.x; i < total * R4; i += gridDim.x * kThreads) {
-    const int col = i / R4, row = (i % R4) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int z = 0; z < p.ks; ++z) {
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-          p.partial + z * plane + static_cast<size_t>(col) * R + row));
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  const int n = total * R4;
+  const int stride = gridDim.x * kThreads;
+  for (int i0 = blockIdx.x * kThreads + threadIdx.x; i0 < n; i0 += kRI * stride) {
+    int slot[kRI], row[kRI];
+    const float *src[kRI];
+    float4 acc[kRI];
+#pragma unroll
+    for (int q = 0; q < kRI; ++q) {
+      const int i = min(i0 + q * stride, n - 1);   // clamped: duplicates are not stored
+      const int col = i / R4;
+      row[q] = (i - col * R4) * 4;
+      slot[q] = slots[col];
+      src[q] = p.partial + static_cast<size_t>(slot[q]) * R + row[q];
+      acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const int slot = slots[col];
-    const int b = slot / p.P;
-    if (row < 3 * ds) {
-      const int e = __ldcg(p.colexp + slot);
-      const int e_slot = (e == kState0) ? p.e_cap : e;
-      if (p.b_hh) {
-        acc.x += p.b_hh[row]; acc.y += p.b_hh[row + 1];
-        acc.z += p.b_hh[row + 2]; acc.w += p.b_hh[row + 3];
-      }
-      *reinterpret_cast<float4 *>(
-          p.gh_store + (static_cast<size_t>(b) * (p.e_cap + 1) + e_slot) * 3 * ds + row) = acc;
-    } else {
-      *reinterpret_cast<float4 *>(p.pbuf + static_cast<size_t>(slot) * p.r + (row - 3 * ds)) = acc;
+    for (int z0 = 0; z0 < p.ks; z0 += kRZ) {
+      float4 v[kRZ][kRI];
+#pragma unroll
+      for (int z = 0; z < kRZ; ++z)
+#pragma unroll
+        for (int q = 0; q < kRI; ++q)
+          v[z][q] = (z0 + z < p.ks) ? __ldcg(reinterpret_cast<const float4 *>(
+                                          src[q] + static_cast<size_t>(z0 + z) * plane))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int z = 0; z < kRZ; ++z)
+#pragma unroll
+        for (int q = 0; q < kRI; ++q) {
+          acc[q].x += v[z][q].x; acc[q].y += v[z][q].y;
+          acc[q].z += v[z][q].z; acc[q].w += v[z][q].w;
+        }
     }
+#pragma unroll
+    for (int q = 0; q < kRI; ++q)
+      if (i0 + q * stride < n) store_reduced(p, slot[q], row[q], acc[q]);
   }
 }
 
@@ -534,24 +571,33 @@ __device__ Tables tables(const ChainParams &p, unsigned char *smem) {
   return t;
 }
 
-// Warp-wide best run head under (score desc, run index asc). hs[r] is the
-// score of run r's current head, NaN once the run is exhausted. Returns the run
-// index or -1 when every run is exhausted.
-__device__ __forceinline__ int best_run(const float *hs, int n_runs, int lane) {
-  float best = 0.f;
-  int br = -1;
+// Frontier argmax, warp-level. Run r belongs to lane r % 32; every lane keeps,
+// in registers, the best of its own runs as (key, run) with key = order image
+// of the head score (0: exhausted). The warp's best run under (score desc, run
+// index asc) is then one max-reduction, one vote and one min-reduction.
+struct LaneBest {
+  uint32_t key;
+  int run;
+};
+
+__device__ __forceinline__ uint32_t hs_key(float s) { return s == s ? float_order_bits(s) : 0u; }
+
+// this lane's best among runs lane, lane + 32, ... < n_runs (ascending, so ties keep the lowest)
+__device__ __forceinline__ LaneBest lane_scan(const float *hs, int n_runs, int lane) {
+  LaneBest lb{0u, -1};
   for (int r = lane; r < n_runs; r += 32) {
-    const float s = hs[r];
-    if (s == s && (br < 0 || s > best)) { best = s; br = r; }   // r ascending within a lane
+    const uint32_t k = hs_key(hs[r]);
+    if (k > lb.key) { lb.key = k; lb.run = r; }
   }
-#pragma unroll
-  for (int m = 16; m; m >>= 1) {
-    const float ob = __shfl_xor_sync(kFull, best, m);
-    const int orr = __shfl_xor_sync(kFull, br, m);
-    const bool take = orr >= 0 && (br < 0 || ob > best || (ob == best && orr < br));
-    if (take) { best = ob; br = orr; }
-  }
-  return br;
+  return lb;
+}
+
+// the warp's best run, or -1 when every run is exhausted
+__device__ __forceinline__ int warp_best(const LaneBest &lb) {
+  const uint32_t kmax = __reduce_max_sync(kFull, lb.key);
+  if (kmax == 0u) return -1;
+  const uint32_t r = (lb.key == kmax) ? static_cast<uint32_t>(lb.run) : 0xffffffffu;
+  return static_cast<int>(__reduce_min_sync(kFull, r));
 }
 
 // score of entry h of run r's children, NaN past the last child
@@ -568,10 +614,10 @@ __device__ __forceinline__ void write_column(const ChainParams &p, int slot, int
     const float r1 = s - __bfloat162float(hi);
     const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
     const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-    uint16_t *c = p.gin16 + static_cast<size_t>(slot) * 3 * p.d_s + u;
+    uint16_t *c = p.gin16 + bcol_index(p, slot, u);
     c[0] = __bfloat16_as_ushort(hi);
-    c[p.d_s] = __bfloat16_as_ushort(mid);
-    c[2 * p.d_s] = __bfloat16_as_ushort(lo);
+    c[kTermBytes / 2] = __bfloat16_as_ushort(mid);
+    c[kTermBytes] = __bfloat16_as_ushort(lo);
   } else {
     p.gin[static_cast<size_t>(slot) * p.d_s + u] = s;
   }
@@ -591,11 +637,11 @@ __device__ __forceinline__ void write_column4(const ChainParams &p, int slot, in
       mb[i] = __bfloat16_as_ushort(mid);
       lb[i] = __bfloat16_as_ushort(lo);
     }
-    uint16_t *c = p.gin16 + static_cast<size_t>(slot) * 3 * p.d_s + u;
+    uint16_t *c = p.gin16 + bcol_index(p, slot, u);
     *reinterpret_cast<uint2 *>(c) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
-    *reinterpret_cast<uint2 *>(c + p.d_s) =
+    *reinterpret_cast<uint2 *>(c + kTermBytes / 2) =
         make_uint2(mb[0] | (mb[1] << 16), mb[2] | (mb[3] << 16));
-    *reinterpret_cast<uint2 *>(c + 2 * p.d_s) =
+    *reinterpret_cast<uint2 *>(c + kTermBytes) =
         make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
   } else {
     *reinterpret_cast<float4 *>(p.gin + static_cast<size_t>(slot) * p.d_s + u) = s;
@@ -651,6 +697,7 @@ __device__ void gru_jobs(const ChainParams &p, const GruJob *jobs, int njobs) {
       write_column4(p, J.slot, u[k], s);
     }
   }
+  if (p.umma) fence_async_global();   // the columns are read by bulk copies next
 }
 
 // Children of expansion e (warp-level): h = SiLU(U_j + p), L over the M
@@ -847,32 +894,41 @@ __device__ void finalize(const ChainParams &p, const Tables &t, TailState &ts, i
 }
 
 // Pop in canonical order until done or until a popped node needs children that
-// are not known yet; then choose the next nodes to expand. Warp 0 only.
+// are not known yet; then choose the next nodes to expand. Warp 0 only. Shared
+// tables are read by every lane (broadcast); a run's entries are written by the
+// lane that owns it.
 __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailState &ts, int b,
                                   int lane) {
   int count = ts.count, n_runs = ts.n_runs;
+  LaneBest lb = lane_scan(t.run_hs, n_runs, lane);
   bool done = false;
   while (true) {
     if (count >= p.N) { done = true; break; }
-    const int r = best_run(t.run_hs, n_runs, lane);
+    const int r = warp_best(lb);
     if (r < 0) { done = true; break; }
     const int h = t.run_head[r], er = t.run_e[r];
     const int dep = t.exp_depth[er] + 1, pos = count + 1;
     const int ce = t.child_exp[er * p.k + h];
     const bool need = dep < p.D && pos < p.N;
     if (need && ce < 0) break;  // stall: this node's children are not known yet
+    const int rpos = t.run_pos[r];
     if (lane == 0) {
-      write_row(p, b, pos, t.child_tok[er * p.k + h], t.run_pos[r], dep,
-                t.child_score[er * p.k + h]);
-      t.par[pos] = t.run_pos[r];
+      write_row(p, b, pos, t.child_tok[er * p.k + h], rpos, dep, t.child_score[er * p.k + h]);
+      t.par[pos] = static_cast<int16_t>(rpos);
+    }
+    if (lane == (r & 31)) {
       t.run_head[r] = static_cast<uint8_t>(h + 1);
       t.run_hs[r] = head_score(p, t, er, h + 1);
-      if (need) {
-        t.run_e[n_runs] = static_cast<int16_t>(ce);
-        t.run_head[n_runs] = 0;
-        t.run_hs[n_runs] = head_score(p, t, ce, 0);
-        t.run_pos[n_runs] = static_cast<int16_t>(pos);
-      }
+      lb = lane_scan(t.run_hs, n_runs, lane);
+    }
+    if (need && lane == (n_runs & 31)) {
+      const float hs0 = head_score(p, t, ce, 0);
+      t.run_e[n_runs] = static_cast<int16_t>(ce);
+      t.run_head[n_runs] = 0;
+      t.run_hs[n_runs] = hs0;
+      t.run_pos[n_runs] = static_cast<int16_t>(pos);
+      const uint32_t k0 = hs_key(hs0);
+      if (k0 > lb.key) { lb.key = k0; lb.run = n_runs; }
     }
     n_runs += need ? 1 : 0;
     count = pos;
@@ -883,7 +939,8 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
     __syncwarp();
     return;
   }
-  // choose the stalled node plus up to P-1 of the next frontier nodes in order
+  // choose the stalled node plus up to P-1 of the next frontier nodes in order,
+  // walking a copy of the run heads (vhead / vhs)
   const int spec_left = p.e_cap - p.N - ts.spec_used;
   for (int r = lane; r < n_runs; r += 32) {
     t.vhead[r] = t.run_head[r];
@@ -891,29 +948,31 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
   }
   __syncwarp();
   int nsel = 0, nspec = 0, i = 0;
-  int e_count = ts.e_count;
+  const int e_count = ts.e_count;
   while (nsel < p.P) {
-    const int r = best_run(t.vhs, n_runs, lane);
+    const int r = warp_best(lb);
     if (r < 0) break;
     ++i;
     if (count + i >= p.N) break;
     const int h = t.vhead[r], er = t.run_e[r];
     const int dep = t.exp_depth[er] + 1;
-    const bool fresh = dep < p.D && t.child_exp[er * p.k + h] < 0;
+    const int slot_c = er * p.k + h;
+    const bool fresh = dep < p.D && t.child_exp[slot_c] < 0;
     const bool take = fresh && (nsel == 0 || nspec < spec_left);
-    if (lane == 0) {
+    if (take && lane == 0) {
+      const int e = e_count + nsel;
+      t.child_exp[slot_c] = static_cast<int16_t>(e);
+      t.exp_depth[e] = static_cast<int8_t>(dep);
+      t.exp_parent[e] = static_cast<int16_t>(er);
+      t.exp_score[e] = t.child_score[slot_c];
+      t.exp_tok[e] = t.child_tok[slot_c];
+      ts.sel_e[nsel] = e;
+      p.colexp[b * p.P + nsel] = e;
+    }
+    if (lane == (r & 31)) {
       t.vhead[r] = static_cast<uint8_t>(h + 1);
       t.vhs[r] = head_score(p, t, er, h + 1);
-      if (take) {
-        const int e = e_count + nsel;
-        t.child_exp[er * p.k + h] = static_cast<int16_t>(e);
-        t.exp_depth[e] = static_cast<int8_t>(dep);
-        t.exp_parent[e] = static_cast<int16_t>(er);
-        t.exp_score[e] = t.child_score[er * p.k + h];
-        t.exp_tok[e] = t.child_tok[er * p.k + h];
-        ts.sel_e[nsel] = e;
-        p.colexp[b * p.P + nsel] = e;
-      }
+      lb = lane_scan(t.vhs, n_runs, lane);
     }
     if (take) {
       nspec += (nsel > 0) ? 1 : 0;
@@ -924,7 +983,7 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
   // warm L2 with the prepared rows of the frontier nodes most likely to be
   // expanded at the next step (the next 2P unexpanded entries in order)
   for (int extra = 0; extra < 2 * p.P;) {
-    const int r = best_run(t.vhs, n_runs, lane);
+    const int r = warp_best(lb);
     if (r < 0) break;
     const int h = t.vhead[r], er = t.run_e[r];
     if (t.exp_depth[er] + 1 < p.D && t.child_exp[er * p.k + h] < 0) {
@@ -933,9 +992,10 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
                     static_cast<uint32_t>(12u * p.d_s));
       ++extra;
     }
-    if (lane == 0) {
+    if (lane == (r & 31)) {
       t.vhead[r] = static_cast<uint8_t>(h + 1);
       t.vhs[r] = head_score(p, t, er, h + 1);
+      lb = lane_scan(t.vhs, n_runs, lane);
     }
     __syncwarp();
   }
@@ -971,6 +1031,7 @@ __device__ void tail_init(const ChainParams &p, const Tables &t, TailState &ts, 
   // first GEMM column: the initial state, for W_hh state0 + b_hh
   const float *s0 = p.state0 + static_cast<size_t>(p.b0 + b) * p.d_s;
   for (int u = threadIdx.x; u < p.d_s; u += kThreads) write_column(p, b * p.P, u, s0[u]);
+  if (p.umma) fence_async_global();
   if (threadIdx.x == 0) {
     p.colexp[b * p.P] = kState0;
     p.col_count[b] = 1;
@@ -1072,20 +1133,30 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
   const bool mma_block = p.umma && blockIdx.x < p.n_mt * p.ks;
   UmmaState u;
   u.tmem = 0;
-  u.uses[0] = u.uses[1] = 0;
+  u.next = 0;
   if (mma_block) {
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + p.sm_tmem);
-    if (threadIdx.x == 0) {
-      mbar_init(&mbar[0], 1);
-      mbar_init(&mbar[1], 1);
-    }
+    if (threadIdx.x == 0)
+      for (int i = 0; i < 2 * kBufs; ++i) mbar_init(&mbar[i], 1);
     load_a_tile(p, smem + p.sm_A);
+    fence_async_smem();   // generic stores of the A tile -> tensor-core reads
     if ((threadIdx.x >> 5) == 0) tmem_alloc(tslot, kTmemCols);
     tmem_fence_before();
     __syncthreads();
     tmem_fence_after();
     u.tmem = *tslot;
+  }
+  if (p.umma && p.ks * p.kc > p.d_s) {
+    // K padding of every B column: zero once (A is zero there too, and 0 * NaN
+    // from stale bytes must not reach an accumulator)
+    const int pad = p.ks * p.kc - p.d_s;
+    const int ncol = ((p.cols_cap + 255) >> 8) << 8;
+    for (int i = blockIdx.x * kThreads + threadIdx.x; i < ncol * pad; i += gridDim.x * kThreads) {
+      uint16_t *c = p.gin16 + bcol_index(p, i / pad, p.d_s + i % pad);
+      c[0] = 0; c[kTermBytes / 2] = 0; c[kTermBytes] = 0;
+    }
+    fence_async_global();
   }
   if (tail) tail_init(p, t, ts, b);
   bool ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
@@ -1167,8 +1238,8 @@ static int chain_smem_layout(const Plan &pl, int e_cap, int wave, ChainParams *c
   cp->sm_A = cp->sm_B = cp->sm_mbar = cp->sm_tmem = 0;
   if (pl.umma) {
     cp->sm_A = off = al(off, 128);    off += 128 * pl.kc * 2;
-    cp->sm_B = off = al(off, 128);    off += 2 * 3 * pl.umma_n * pl.kc * 2;
-    cp->sm_mbar = off = al(off, 16);  off += 16;
+    cp->sm_B = off = al(off, 128);    off += kBufs * kSliceBytes;
+    cp->sm_mbar = off = al(off, 16);  off += 16 * kBufs;
     cp->sm_tmem = off;                off += 16;
   }
   cp->sm_scratch = off;
@@ -1226,7 +1297,7 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.gin = reinterpret_cast<float *>(w + pl.off_gin);
   cp.pbuf = reinterpret_cast<float *>(w + pl.off_p);
   cp.colexp = reinterpret_cast<int *>(w + pl.off_colexp);
-  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc; cp.un = pl.umma_n;
+  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc;
   cp.cols_cap = pl.wave * pl.spec;
   cp.partial = pl.umma ? reinterpret_cast<float *>(w + pl.off_partial) : nullptr;
   cp.gin16 = pl.umma ? reinterpret_cast<uint16_t *>(w + pl.off_gin16) : nullptr;

@@ -20,7 +20,6 @@ struct Plan {
   int proj_ksplit;     // K split of the projection GEMM
   int umma;            // search GEMM on tcgen05 (bf16 weights)
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
-  int umma_n;          // columns per MMA (B buffer width)
   int num_sms;
   int chain_grid;      // co-resident blocks of the search kernel
   int wave;            // requests per search launch (<= chain_grid)

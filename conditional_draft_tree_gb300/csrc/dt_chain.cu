@@ -72,6 +72,12 @@ struct ChainParams {
   const float *U;
   float *S_store, *gh_store, *gin, *pbuf;
   int *colexp, *col_count;
+  // per GEMM column (slot): depth of the children and score of the expanded
+  // node (written with the selection); its k children once scored
+  int *col_dep;
+  float *col_score;
+  float *kid_score;
+  int32_t *kid_tok;
   // tensor-core GEMM path (bf16 weights): A tiles of 128 rows x kc K stay in
   // shared memory; the input columns arrive as three bf16 terms per state
   int umma, n_mt, ks, kc, cols_cap;
@@ -465,7 +471,7 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
   return ok;
 }
 
-// Sum of the K-chunk partials (fixed order) + b_hh into gh_store / pbuf. Each
+// Sum of the K-chunk partials (fixed order) + b_hh into gh_store. Each
 // thread takes kRI float4 items at a time and, for up to kRZ chunks, issues all
 // their loads before adding, so that the L2 latency is paid about once.
 constexpr int kRI = 3;
@@ -488,10 +494,8 @@ __device__ __forceinline__ void store_reduced(const ChainParams &p, int slot, in
   }
 }
 
-__device__ void reduce_phase(const ChainParams &p, unsigned char *scratch) {
-  int *slots = reinterpret_cast<int *>(scratch);
-  const int total = compact_slots(p, slots);
-  const int R = 3 * p.d_s + p.r, R4 = R / 4;
+__device__ void reduce_phase(const ChainParams &p, const int *slots, int total) {
+  const int R = 3 * p.d_s + p.r, R4 = 3 * p.d_s / 4;   // the gh rows (p is summed by the scorers)
   const size_t plane = static_cast<size_t>(p.cols_cap) * R;
   const int n = total * R4;
   const int stride = gridDim.x * kThreads;
@@ -700,68 +704,111 @@ __device__ void gru_jobs(const ChainParams &p, const GruJob *jobs, int njobs) {
   if (p.umma) fence_async_global();   // the columns are read by bulk copies next
 }
 
-// Children of expansion e (warp-level): h = SiLU(U_j + p), L over the M
-// candidates of depth j, log-sum-exp over them, the k best by (L desc, id asc).
-// The lanes split the rank dimension into 8-wide chunks: a candidate's W2 row
-// is read by the whole warp in one coalesced access, candidate ids and base
-// logits are loaded up front, and eight rows are in flight at a time; lane
-// c % 32 keeps candidate c for the sort. With r <= 256 each lane's h chunk
-// stays in registers; larger ranks read h from a per-warp shared buffer.
+// Children of every node expanded by the last GEMM, spread over the grid. A
+// node (GEMM column `slot`, children at depth j, request b) gets kWPN warps of
+// one block: each forms h = SiLU(U_j + p) (p summed over the K-chunk partials
+// in fixed order) and the corrected logits L_c = (L_base^j[c] + W2[c,:] h) / T
+// of its share of the M candidates; then one of them takes the log-sum-exp
+// over the M values and the k best (L desc, id asc) as the children, with
+// scores col_score + L_c - lse, and warms L2 with the prepared rows of the two
+// best (the likeliest next expansions).
+constexpr int kWPN = 4;                // warps per node
+constexpr int kNPB = kWarps / kWPN;    // nodes per block and round
+
 template <int WDT, int SLOTS, bool SMALL_R>
-__device__ void score_node(const ChainParams &p, const Tables &t, float T, int b, int slot, int e,
-                           int lane, float *hbuf) {
-  const int j = t.exp_depth[e] + 1;
-  const size_t row = static_cast<size_t>(p.b0 + b) * p.D + (j - 1);
-  const float *U = p.U + row * p.r;
-  const float *pv = p.pbuf + static_cast<size_t>(slot) * p.r;
+__device__ void score_phase(const ChainParams &p, const int *slots, int total, float *sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int node_in_block = warp / kWPN, wq = warp % kWPN;
+  float *Lsm = sm + node_in_block * p.M;
+  float *hbuf = sm + kNPB * p.M + warp * p.r;   // used only when r > 256
   const int nq = p.r / 8;
-  const int32_t *cid = p.cand_id + row * p.M;
-  const float *cval = p.cand_val + row * p.M;
-  const uint64_t t_in = (blockIdx.x == 0 && threadIdx.x == 0) ? global_ns() : 0;
-  int my_id[SLOTS];
-  float my_base[SLOTS];
-#pragma unroll
-  for (int s = 0; s < SLOTS; ++s) {
-    const int c = s * 32 + lane;
-    my_id[s] = (c < p.M) ? __ldg(cid + c) : -1;
-    my_base[s] = (c < p.M) ? __ldg(cval + c) : 0.f;
-  }
-  float h[8];
-  if (SMALL_R) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      h[i] = (lane < nq) ? siluf_(__ldg(U + 8 * lane + i) + ldcg(pv + 8 * lane + i)) : 0.f;
-  } else {
-    for (int q = lane; q < p.r; q += 32) hbuf[q] = siluf_(__ldg(U + q) + ldcg(pv + q));
-    __syncwarp();
-  }
-  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
-  uint64_t tc = 0;
-  if (clock_me) {
-    // consume the loads above before reading the clock
-    volatile float sink = h[0] + my_base[0] + static_cast<float>(my_id[0]);
-    (void)sink;
-    tc = global_ns();
-    p.ctrl->t_ns[13] += tc - t_in;
-  }
+  const int R = 3 * p.d_s + p.r;
+  const size_t plane = static_cast<size_t>(p.cols_cap) * R;
   const float ninf = -__int_as_float(0x7f800000);
-  uint64_t key[SLOTS];
-  float Lv[SLOTS];
+  const int mq = (p.M + kWPN - 1) / kWPN;
+  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
+  for (int n0 = blockIdx.x * kNPB; n0 < total; n0 += gridDim.x * kNPB) {
+    const int n = n0 + node_in_block;
+    const int slot = n < total ? slots[n] : 0;
+    const bool live = n < total && __ldcg(p.colexp + slot) >= 0;
+    const int b = slot / p.P;
+    const int j = live ? __ldcg(p.col_dep + slot) : 1;
+    const size_t row = static_cast<size_t>(p.b0 + b) * p.D + (j - 1);
+    const int32_t *cid = p.cand_id + row * p.M;
+    const float *cval = p.cand_val + row * p.M;
+    float T = p.temperature ? p.temperature[p.b0 + b] : 1.0f;
+    T = (T == 0.0f) ? 1.0f : T;
+    uint64_t t_in = clock_me ? global_ns() : 0;
+    if (live) {
+      const float *U = p.U + row * p.r;
+      // h = SiLU(U_j + p): p from the partials (tensor-core path) or pbuf
+      float h[8];
+      if (SMALL_R) {
+        if (lane < nq) {
+          float a[8];
+          if (p.umma) {
 #pragma unroll
-  for (int s = 0; s < SLOTS; ++s) {
-    key[s] = 0ull;
-    Lv[s] = ninf;
-    float my_dl = 0.f;   // correction of candidate s*32 + lane
-    constexpr int G = WDT == 1 ? 16 : 8;   // candidate rows in flight
+            for (int i = 0; i < 8; ++i) a[i] = 0.f;
+            const float *src = p.partial + static_cast<size_t>(slot) * R + 3 * p.d_s + 8 * lane;
+            for (int z0 = 0; z0 < p.ks; z0 += 4) {
+              float4 v[4][2];
 #pragma unroll
-    for (int cg = 0; cg < 32 / G; ++cg) {
-      const int c0 = s * 32 + cg * G;
-      if (c0 < p.M) {                        // warp-uniform
+              for (int z = 0; z < 4; ++z) {
+                const bool ok = z0 + z < p.ks;
+                const float4 *q = reinterpret_cast<const float4 *>(src + (z0 + z) * plane);
+                v[z][0] = ok ? __ldcg(q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[z][1] = ok ? __ldcg(q + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+              for (int z = 0; z < 4; ++z) {
+                a[0] += v[z][0].x; a[1] += v[z][0].y; a[2] += v[z][0].z; a[3] += v[z][0].w;
+                a[4] += v[z][1].x; a[5] += v[z][1].y; a[6] += v[z][1].z; a[7] += v[z][1].w;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              a[i] = ldcg(p.pbuf + static_cast<size_t>(slot) * p.r + 8 * lane + i);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) h[i] = siluf_(__ldg(U + 8 * lane + i) + a[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) h[i] = 0.f;
+        }
+      } else {
+        for (int q = lane; q < p.r; q += 32) {
+          float a = 0.f;
+          if (p.umma) {
+            for (int z = 0; z < p.ks; ++z)
+              a += ldcg(p.partial + z * plane + static_cast<size_t>(slot) * R + 3 * p.d_s + q);
+          } else {
+            a = ldcg(p.pbuf + static_cast<size_t>(slot) * p.r + q);
+          }
+          hbuf[q] = siluf_(__ldg(U + q) + a);
+        }
+        __syncwarp();
+      }
+      if (clock_me) {
+        volatile float sink = h[0];
+        (void)sink;
+        const uint64_t now = global_ns();
+        p.ctrl->t_ns[13] += now - t_in;
+        t_in = now;
+      }
+      // this warp's candidates [c_beg, c_end), G rows in flight
+      constexpr int G = WDT == 1 ? 16 : 8;
+      const int c_beg = wq * mq, c_end = min(p.M, c_beg + mq);
+      for (int c0 = c_beg; c0 < c_end; c0 += G) {
+        const int my_c = c0 + lane;
+        const bool mine = lane < G && my_c < c_end;
+        const int my_id = mine ? __ldg(cid + my_c) : -1;
+        const float my_base = mine ? __ldg(cval + my_c) : 0.f;
         float acc[G];
         int ids[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          ids[g] = __shfl_sync(kFull, my_id[s], cg * G + g);
+          ids[g] = __shfl_sync(kFull, my_id, g);
           acc[g] = 0.f;
         }
         if (SMALL_R && WDT == 1) {
@@ -801,61 +848,81 @@ __device__ void score_node(const ChainParams &p, const Tables &t, float T, int b
 #pragma unroll 1
           for (int q = lane; q - lane < nq; q += 32) {
             if (q < nq) {
+              float hq[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) h[i] = hbuf[8 * q + i];
+              for (int i = 0; i < 8; ++i) hq[i] = hbuf[8 * q + i];
 #pragma unroll
               for (int g = 0; g < G; ++g) {
                 if (ids[g] >= 0) {
                   float wf[8];
                   load8<WDT>(p.W2, static_cast<size_t>(ids[g]) * p.r + 8 * q, wf);
 #pragma unroll
-                  for (int i = 0; i < 8; ++i) acc[g] = fmaf(wf[i], h[i], acc[g]);
+                  for (int i = 0; i < 8; ++i) acc[g] = fmaf(wf[i], hq[i], acc[g]);
                 }
               }
             }
           }
         }
+        float my_dl = 0.f;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float dl = warp_sum(acc[g]);
-          if (cg * G + g == lane) my_dl = dl;
+          if (g == lane) my_dl = dl;
         }
+        if (mine) Lsm[my_c] = my_id >= 0 ? __fdiv_rn(my_base + my_dl, T) : ninf;
       }
     }
-    if (my_id[s] >= 0) {
-      Lv[s] = __fdiv_rn(my_base[s] + my_dl, T);
-      key[s] = make_key(Lv[s], static_cast<uint32_t>(my_id[s]));
+    __syncthreads();
+    if (clock_me && live) {
+      const uint64_t now = global_ns();
+      p.ctrl->t_ns[14] += now - t_in;
+      t_in = now;
     }
-  }
-  if (clock_me) {
-    const uint64_t n = global_ns();
-    p.ctrl->t_ns[14] += n - tc;
-    tc = n;
-  }
-  float mx = ninf;
+    if (live && wq == 0) {
+      uint64_t key[SLOTS];
+      float Lv[SLOTS];
+      float mx = ninf;
 #pragma unroll
-  for (int s = 0; s < SLOTS; ++s) mx = fmaxf(mx, Lv[s]);
-  mx = warp_max(mx);
-  float sum = 0.f;
+      for (int s = 0; s < SLOTS; ++s) {
+        const int c = s * 32 + lane;
+        key[s] = 0ull;
+        Lv[s] = ninf;
+        if (c < p.M) {
+          const int id = __ldg(cid + c);
+          if (id >= 0) {
+            Lv[s] = Lsm[c];
+            key[s] = make_key(Lv[s], static_cast<uint32_t>(id));
+          }
+        }
+        mx = fmaxf(mx, Lv[s]);
+      }
+      mx = warp_max(mx);
+      float sum = 0.f;
 #pragma unroll
-  for (int s = 0; s < SLOTS; ++s)
-    if (s * 32 + lane < p.M) sum += expf(Lv[s] - mx);
-  sum = warp_sum(sum);
-  const float lse = (mx == ninf) ? ninf : mx + logf(sum);
-  warp_sort_desc<SLOTS>(key, lane);
-  const float base_score = t.exp_score[e];
+      for (int s = 0; s < SLOTS; ++s)
+        if (s * 32 + lane < p.M) sum += expf(Lv[s] - mx);
+      sum = warp_sum(sum);
+      const float lse = (mx == ninf) ? ninf : mx + logf(sum);
+      warp_sort_desc<SLOTS>(key, lane);
+      const float base_score = __ldcg(p.col_score + slot);
 #pragma unroll
-  for (int s = 0; s < SLOTS; ++s) {
-    const int i = s * 32 + lane;
-    if (i < p.k) {
-      const float L = key_value(key[s]);
-      const float lp = (lse == ninf) ? ninf : L - lse;
-      t.child_score[e * p.k + i] = base_score + lp;
-      t.child_tok[e * p.k + i] = static_cast<int32_t>(key_id(key[s]));
-      t.child_exp[e * p.k + i] = -1;
+      for (int s = 0; s < SLOTS; ++s) {
+        const int i = s * 32 + lane;
+        if (i < p.k) {
+          const float L = key_value(key[s]);
+          const float lp = (lse == ninf) ? ninf : L - lse;
+          const int tok = static_cast<int32_t>(key_id(key[s]));
+          p.kid_score[static_cast<size_t>(slot) * p.k + i] = base_score + lp;
+          p.kid_tok[static_cast<size_t>(slot) * p.k + i] = tok;
+          if (i < 2 && j < p.D)
+            prefetch_l2(p.G + static_cast<size_t>(tok) * 3 * p.d_s,
+                        static_cast<uint32_t>(12u * p.d_s));
+        }
+      }
+      if (clock_me) p.ctrl->t_ns[15] += global_ns() - t_in;
     }
+    __syncthreads();
   }
-  if (clock_me) p.ctrl->t_ns[15] += global_ns() - tc;
 }
 
 __device__ void write_row(const ChainParams &p, int b, int pos, int tok, int par, int dep,
@@ -968,6 +1035,8 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
       t.exp_tok[e] = t.child_tok[slot_c];
       ts.sel_e[nsel] = e;
       p.colexp[b * p.P + nsel] = e;
+      p.col_dep[b * p.P + nsel] = dep + 1;   // the children's depth
+      p.col_score[b * p.P + nsel] = t.child_score[slot_c];
     }
     if (lane == (r & 31)) {
       t.vhead[r] = static_cast<uint8_t>(h + 1);
@@ -977,25 +1046,6 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
     if (take) {
       nspec += (nsel > 0) ? 1 : 0;
       ++nsel;
-    }
-    __syncwarp();
-  }
-  // warm L2 with the prepared rows of the frontier nodes most likely to be
-  // expanded at the next step (the next 2P unexpanded entries in order)
-  for (int extra = 0; extra < 2 * p.P;) {
-    const int r = warp_best(lb);
-    if (r < 0) break;
-    const int h = t.vhead[r], er = t.run_e[r];
-    if (t.exp_depth[er] + 1 < p.D && t.child_exp[er * p.k + h] < 0) {
-      if (lane == 0)
-        prefetch_l2(p.G + static_cast<size_t>(t.child_tok[er * p.k + h]) * 3 * p.d_s,
-                    static_cast<uint32_t>(12u * p.d_s));
-      ++extra;
-    }
-    if (lane == (r & 31)) {
-      t.vhead[r] = static_cast<uint8_t>(h + 1);
-      t.vhs[r] = head_score(p, t, er, h + 1);
-      lb = lane_scan(t.vhs, n_runs, lane);
     }
     __syncwarp();
   }
@@ -1077,6 +1127,8 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
       atomicAdd(&p.ctrl->expansions, 1u);
       ts.sel_e[0] = 0;
       p.colexp[b * p.P] = 0;
+      p.col_dep[b * p.P] = 1;
+      p.col_score[b * p.P] = 0.0f;
       p.col_count[b] = 1;
     }
     __syncthreads();
@@ -1084,13 +1136,14 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
   }
   const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
   uint64_t t0 = clock_me ? global_ns() : 0;
-  // 1. children of the nodes expanded by the last GEMM (one warp per node)
-  float *hbuf = t.scratch + warp * p.r;   // used only when r > 256
-  for (int i = warp; i < ncols; i += kWarps) {
-    if (p.r <= 256)
-      score_node<WDT, SLOTS, true>(p, t, ts.T, b, b * p.P + i, ts.sel_e[i], lane, hbuf);
-    else
-      score_node<WDT, SLOTS, false>(p, t, ts.T, b, b * p.P + i, ts.sel_e[i], lane, hbuf);
+  // 1. children of the nodes expanded by the last GEMM (scored grid-wide)
+  for (int i = threadIdx.x; i < ncols * p.k; i += kThreads) {
+    const int c = i / p.k, rank = i - c * p.k;
+    const int e = ts.sel_e[c];
+    const size_t src = static_cast<size_t>(b * p.P + c) * p.k + rank;
+    t.child_score[e * p.k + rank] = __ldcg(p.kid_score + src);
+    t.child_tok[e * p.k + rank] = __ldcg(p.kid_tok + src);
+    t.child_exp[e * p.k + rank] = -1;
   }
   __syncthreads();
   if (threadIdx.x == 0 && ts.n_runs == 0) {  // the root's children form the first run
@@ -1176,17 +1229,24 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     if (p.umma) {
       if (!gemm_phase_umma(p, smem, smem + p.sm_scratch, u) && threadIdx.x == 0)
         atomicExch(&p.ctrl->abort, 1);
-      lap(0);
-      ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
-                        p.limit_ns);
-      lap(1);
-      if (!ok) break;
-      reduce_phase(p, smem + p.sm_scratch);
-      lap(2);
     } else {
       gemm_phase<WDT>(p, smem + p.sm_scratch);
-      lap(0);
     }
+    lap(0);
+    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
+                      p.limit_ns);
+    lap(1);
+    if (!ok) break;
+    {
+      // children of the new expansions (p summed here), then the gh rows
+      int *slots = reinterpret_cast<int *>(smem + p.sm_scratch);
+      const int total = compact_slots(p, slots);
+      float *sc = reinterpret_cast<float *>(smem + p.sm_scratch + ((p.cols_cap * 4 + 15) & ~15));
+      if (p.r <= 256) score_phase<WDT, SLOTS, true>(p, slots, total, sc);
+      else score_phase<WDT, SLOTS, false>(p, slots, total, sc);
+      if (p.umma) reduce_phase(p, slots, total);
+    }
+    lap(2);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
                       p.limit_ns);
     lap(3);
@@ -1244,8 +1304,9 @@ static int chain_smem_layout(const Plan &pl, int e_cap, int wave, ChainParams *c
   }
   cp->sm_scratch = off;
   const int gemm_scratch = al(wave * pl.spec * 4, 16) + (pl.umma ? 0 : kGemmCols * kGemmKC * 4);
-  const int tail_scratch = d.r > 256 ? kWarps * d.r * 4 : 16;
-  off += gemm_scratch > tail_scratch ? gemm_scratch : tail_scratch;
+  const int score_scratch =
+      al(wave * pl.spec * 4, 16) + kNPB * d.M * 4 + (d.r > 256 ? kWarps * d.r * 4 : 0);
+  off += gemm_scratch > score_scratch ? gemm_scratch : score_scratch;
   cp->sm_total = off;
   return off;
 }
@@ -1302,6 +1363,11 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.partial = pl.umma ? reinterpret_cast<float *>(w + pl.off_partial) : nullptr;
   cp.gin16 = pl.umma ? reinterpret_cast<uint16_t *>(w + pl.off_gin16) : nullptr;
   cp.col_count = cp.colexp + static_cast<size_t>(pl.wave) * pl.spec;
+  cp.col_dep = reinterpret_cast<int *>(w + pl.off_colinfo);
+  cp.col_score = reinterpret_cast<float *>(cp.col_dep + static_cast<size_t>(pl.wave) * pl.spec);
+  cp.kid_score = reinterpret_cast<float *>(w + pl.off_kids);
+  cp.kid_tok = reinterpret_cast<int32_t *>(cp.kid_score +
+                                           static_cast<size_t>(pl.wave) * pl.spec * d.k);
   cp.ctrl = reinterpret_cast<Ctrl *>(w + pl.off_ctrl);
   cp.req_flags = reinterpret_cast<const int *>(w + pl.off_ctrl + kCtrlHeader +
                                                sizeof(unsigned) * static_cast<size_t>(d.batch) * d.D);

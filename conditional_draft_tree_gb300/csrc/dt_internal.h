@@ -26,7 +26,7 @@ struct Plan {
   size_t chain_smem;   // dynamic shared memory of the search kernel
   // workspace carve-up (byte offsets)
   size_t off_ctrl, off_part, off_cand_id, off_cand_val, off_U, off_S, off_gh, off_gin, off_p,
-      off_colexp, off_upart, off_partial, off_gin16, off_end;
+      off_colexp, off_colinfo, off_kids, off_upart, off_partial, off_gin16, off_end;
   size_t off_gemm_tickets;  // inside the control region
 };
 
@@ -40,10 +40,10 @@ struct Ctrl {
   unsigned int expansions; // expansions of the last search launch
   unsigned int pad[2];
   // block 0 of the last search launch, ns summed over steps: GEMM, barrier,
-  // reduction, barrier, tail, barrier; tail parts: scoring, pops and
-  // selection, GRU; GEMM parts: MMA loop, epilogue
+  // scoring + reduction, barrier, tail, barrier; tail parts: reading the
+  // children, pops and selection, GRU; GEMM parts: MMA loop, epilogue
   // then: GEMM waits for B copies, GEMM waits for MMA completion; scoring of
-  // one node (warp 0): operand loads, candidate loop, softmax + sort + write
+  // block 0's first node: h, candidate loop (incl. block sync), softmax + sort + write
   unsigned long long t_ns[16];
   // followed by: unsigned row_ticket[batch * D]; int req_flags[batch]; gemm tickets
 };

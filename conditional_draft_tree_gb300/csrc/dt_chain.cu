@@ -1212,8 +1212,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     fence_async_global();
   }
   if (tail) tail_init(p, t, ts, b);
-  bool ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
-                         p.limit_ns);
+  unsigned bar_target = 0;
+  bool ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
+                         false);
   // block 0 accounts its time per phase (for profiling; a few timer reads a step)
   const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
   uint64_t t_prev = clock_me ? global_ns() : 0;
@@ -1226,15 +1227,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
   };
   for (int step = 0; ok && step < p.N + 3; ++step) {
     if (clock_me) p.ctrl->steps = static_cast<unsigned>(step + 1);
-    if (p.umma) {
-      if (!gemm_phase_umma(p, smem, smem + p.sm_scratch, u) && threadIdx.x == 0)
-        atomicExch(&p.ctrl->abort, 1);
-    } else {
-      gemm_phase<WDT>(p, smem + p.sm_scratch);
-    }
+    bool gemm_ok = true;
+    if (p.umma) gemm_ok = gemm_phase_umma(p, smem, smem + p.sm_scratch, u);
+    else gemm_phase<WDT>(p, smem + p.sm_scratch);
     lap(0);
-    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
-                      p.limit_ns);
+    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
+                      !gemm_ok);
     lap(1);
     if (!ok) break;
     {
@@ -1247,14 +1245,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
       if (p.umma) reduce_phase(p, slots, total);
     }
     lap(2);
-    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
-                      p.limit_ns);
+    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
+                      false);
     lap(3);
     if (!ok) break;
     if (tail && !ts.done) tail_step<WDT, SLOTS>(p, t, ts, b);
     lap(4);
-    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->bar_gen, &p.ctrl->abort, gridDim.x,
-                      p.limit_ns);
+    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
+                      false);
     lap(5);
     if (!ok) break;
     if (threadIdx.x == 0) s_active = ld_acquire_s32(&p.ctrl->active);

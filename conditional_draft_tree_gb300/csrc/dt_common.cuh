@@ -102,36 +102,43 @@ __device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Bounded grid-wide barrier for a cooperative launch of `nblocks` blocks.
-// A wait that exceeds `limit_ns` (or sees *abort set) sets *abort and returns
-// false; the caller then leaves its step loop. Never traps or spins forever.
-__device__ __forceinline__ bool grid_barrier(unsigned *count, unsigned *gen, int *abort,
-                                             unsigned nblocks, uint64_t limit_ns) {
+__device__ __forceinline__ void red_release_add_u32(unsigned *p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded grid-wide barrier for a cooperative launch of `nblocks` blocks. The
+// counter only grows: barrier number i completes when it reaches i * nblocks
+// (`target`, advanced by every call, wrap-safe). A block that failed locally
+// (`fail`) raises *abort and does not arrive; a wait longer than `limit_ns`, or
+// one that sees *abort, returns false. Never traps or spins forever.
+__device__ __forceinline__ bool grid_barrier(unsigned *count, int *abort, unsigned nblocks,
+                                             uint64_t limit_ns, unsigned &target, bool fail) {
   __shared__ int s_ok;
+  target += nblocks;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    unsigned g = ld_acquire_u32(gen);
-    __threadfence();
-    unsigned arrived = atomicAdd(count, 1u);
-    if (arrived == nblocks - 1) {
-      atomicExch(count, 0u);
-      __threadfence();
-      st_release_u32(gen, g + 1);
+    if (fail) {
+      atomicExch(abort, 1);
+      ok = 0;
     } else {
-      uint64_t t0 = global_ns();
-      unsigned spins = 0;
-      while (ld_acquire_u32(gen) == g) {
-        if (ld_acquire_s32(abort)) { ok = 0; break; }
-        if ((++spins & 63u) == 0 && global_ns() - t0 > limit_ns) {
-          atomicExch(abort, 1);
-          ok = 0;
-          break;
+      red_release_add_u32(count, 1u);
+      uint64_t t0 = 0;
+      for (unsigned spins = 0;; ++spins) {
+        if (static_cast<int>(ld_acquire_u32(count) - target) >= 0) break;
+        if ((spins & 31u) == 31u) {
+          if (ld_acquire_s32(abort)) { ok = 0; break; }
+          const uint64_t now = global_ns();
+          if (spins == 31u) {
+            t0 = now;
+          } else if (now - t0 > limit_ns) {
+            atomicExch(abort, 1);
+            ok = 0;
+            break;
+          }
         }
-        __nanosleep(20);
       }
     }
-    if (ok && ld_acquire_s32(abort)) ok = 0;
     s_ok = ok;
   }
   __syncthreads();

@@ -32,8 +32,8 @@ struct Plan {
 
 // Control block at the start of the workspace; zeroed by every call.
 struct Ctrl {
-  unsigned int bar_count;
-  unsigned int bar_gen;
+  unsigned int bar_count;  // grid barrier arrivals (monotonic within a launch)
+  unsigned int bar_spare;
   int abort;           // set when a bounded wait expired
   int active;          // requests of the current wave still searching
   unsigned int steps;      // lockstep steps of the last search launch

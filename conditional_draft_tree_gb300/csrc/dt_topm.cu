@@ -97,6 +97,36 @@ struct WarpList {
   }
 };
 
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// element `bit` (0..15) of four float4 registers, without local memory
+__device__ __forceinline__ float pick16(const float4 c[kQ], int bit) {
+  const float4 a = (bit & 8) ? ((bit & 4) ? c[3] : c[2]) : ((bit & 4) ? c[1] : c[0]);
+  return (bit & 2) ? ((bit & 1) ? a.w : a.z) : ((bit & 1) ? a.y : a.x);
+}
+
+// The (k+1)-th largest of the 32 lane values (k < 32; NaN lanes count as -inf).
+__device__ __forceinline__ float warp_kth_largest(float v, int k, int lane) {
+  if (k >= 32) return -__int_as_float(0x7f800000);
+  v = (v == v) ? v : -__int_as_float(0x7f800000);
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride >= 1; stride >>= 1) {
+      const float o = __shfl_xor_sync(kFull, v, stride);
+      const bool desc = (lane & size) == 0 || size == 32;
+      const bool low = (lane & stride) == 0;
+      const float mx = fmaxf(v, o), mn = fminf(v, o);
+      v = (low == desc) ? mx : mn;
+    }
+  }
+  return __shfl_sync(kFull, v, k);
+}
+
 // Descending bitonic sort of one key per lane.
 __device__ __forceinline__ uint64_t sort32_desc(uint64_t v, int lane) {
 #pragma unroll
@@ -115,9 +145,14 @@ __device__ __forceinline__ uint64_t sort32_desc(uint64_t v, int lane) {
 
 // Streaming top-M of one warp. Candidates above the current threshold are
 // appended to a per-warp shared-memory buffer; every 32 buffered keys are
-// sorted and merged into the register-resident list in one bitonic merge. The
-// threshold is the larger of this warp's M-th key and the block-wide maximum of
-// all warps' M-th keys (each is a lower bound of the block's M-th key).
+// sorted and merged into the register-resident list in one bitonic merge.
+//
+// Threshold: any value below the M-th largest key seen so far by the whole
+// block can be dropped. Two lower bounds of that key are kept in a block-shared
+// maximum: each warp's own M-th key, and the smallest of the warps' q-th keys,
+// q = ceil(M / warps) (every warp holds at least q keys at or above it, so the
+// block holds at least M). The second tracks the block's M-th key about as if
+// one warp had seen the whole segment, so few elements pass after a short start.
 template <int SLOTS>
 struct Select {
   WarpList<SLOTS> L;
@@ -125,7 +160,8 @@ struct Select {
   float tau_v;
   uint64_t *buf;                 // [kBuf] per warp
   unsigned long long *s_tau;     // block-wide threshold
-  int cnt, M, lane;
+  unsigned long long *s_wq;      // [warps] each warp's q-th key
+  int cnt, M, qi, lane, warp;
   bool bad;
 
   __device__ __forceinline__ void set_tau(uint64_t t) {
@@ -142,9 +178,21 @@ struct Select {
     b.v[0] = sort32_desc(k, lane);
     L.merge(b, lane);
     const uint64_t own = L.at(M - 1);
-    if (own != 0ull) {
-      if (lane == 0) atomicMax(s_tau, static_cast<unsigned long long>(own));
-      if (own > tau) set_tau(own);
+    const uint64_t qk = L.at(qi);
+    if (lane == 0) reinterpret_cast<volatile unsigned long long *>(s_wq)[warp] = qk;
+    __syncwarp();
+    uint64_t mn = (lane < kTopmWarps) ? reinterpret_cast<volatile unsigned long long *>(s_wq)[lane]
+                                      : ~0ull;
+#pragma unroll
+    for (int o = 4; o; o >>= 1) {
+      const uint64_t y = shfl64_xor(mn, o);
+      mn = y < mn ? y : mn;
+    }
+    mn = shfl64(mn, 0);
+    const uint64_t best = own > mn ? own : mn;
+    if (best != 0ull) {
+      if (lane == 0) atomicMax(s_tau, static_cast<unsigned long long>(best));
+      if (best > tau) set_tau(best);
     }
   }
   // one candidate per lane: keys above the threshold are appended to the
@@ -207,12 +255,14 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
   __shared__ uint64_t lists[kTopmWarps * MP];
   __shared__ uint64_t bufs[kTopmWarps * kBuf];
   __shared__ unsigned long long s_tau;
+  __shared__ unsigned long long s_wq[kTopmWarps];
   __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int row = blockIdx.y, split = blockIdx.x;
   const size_t row_base = static_cast<size_t>(row) * V;
   const float *rowp = logits + row_base;
   if (threadIdx.x == 0) s_tau = 0ull;
+  if (threadIdx.x < kTopmWarps) s_wq[threadIdx.x] = 0ull;
   __syncthreads();
 
   // vector part [a0, a0 + 4 nv) is 16-byte aligned; scalar head [0, a0), tail
@@ -227,7 +277,10 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
   Select<SLOTS> st;
   st.L.clear();
   st.M = M;
+  st.qi = (M + kTopmWarps - 1) / kTopmWarps - 1;
   st.lane = lane;
+  st.warp = warp;
+  st.s_wq = s_wq;
   st.bad = false;
   st.cnt = 0;
   st.buf = bufs + warp * kBuf;
@@ -242,6 +295,31 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
     const int u = w0 + q * 32 + lane;
     cur[q] = (u < w1) ? __ldcs(vec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  // starting threshold from the first tile of every warp: the q-th largest of
+  // a warp's lane maxima is a value that at least q of its elements reach, so
+  // the smallest such value over the warps is reached by at least M elements
+  // of the block and nothing below it can be among the block's top M
+  {
+    const float ninf = -__int_as_float(0x7f800000);
+    float lm = ninf;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      if (w0 + q * 32 + lane < w1)
+        lm = fmaxf(lm, fmaxf(fmaxf(cur[q].x, cur[q].y), fmaxf(cur[q].z, cur[q].w)));
+    }
+    const float t = warp_kth_largest(lm, st.qi, lane);
+    if (lane == 0) s_wq[warp] = static_cast<unsigned long long>(__float_as_uint(t));
+    __syncthreads();
+    float t0 = __uint_as_float(static_cast<uint32_t>(s_wq[0]));
+#pragma unroll
+    for (int w = 1; w < kTopmWarps; ++w)
+      t0 = fminf(t0, __uint_as_float(static_cast<uint32_t>(s_wq[w])));
+    __syncthreads();
+    if (threadIdx.x < kTopmWarps) s_wq[threadIdx.x] = 0ull;
+    // key of (t0, largest id): every element of value t0 or more passes
+    if (t0 > ninf && st.qi < 32) st.set_tau(make_key(t0, 0xffffffffu));
+    __syncthreads();
+  }
   for (int base = w0; base < w1; base += kQ * 32) {
 #pragma unroll
     for (int q = 0; q < kQ; ++q) {
@@ -249,29 +327,37 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
       nxt[q] = (u < w1) ? __ldcs(vec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     st.sync_tau();
+    // NaN-propagating maximum: a NaN (or +inf) forces the slow path, where
+    // push() flags it; -inf is an ordinary (masked) value
     bool any = false;
 #pragma unroll
     for (int q = 0; q < kQ; ++q) {
       const bool ok = base + q * 32 + lane < w1;
-      any |= ok && (cur[q].x >= st.tau_v || cur[q].y >= st.tau_v || cur[q].z >= st.tau_v ||
-                    cur[q].w >= st.tau_v);
-      st.bad |= ok && !(cur[q].x < __int_as_float(0x7f800000) &&
-                        cur[q].y < __int_as_float(0x7f800000) &&
-                        cur[q].z < __int_as_float(0x7f800000) &&
-                        cur[q].w < __int_as_float(0x7f800000));
+      const float m4 = fmax_nan(fmax_nan(cur[q].x, cur[q].y), fmax_nan(cur[q].z, cur[q].w));
+      any |= ok && !(m4 < st.tau_v);
     }
     if (__any_sync(kFull, any)) {
+      // only the elements at or above the threshold (or NaN): one push round
+      // per element of the busiest lane, usually one or two
+      uint32_t mask = 0u;
 #pragma unroll
       for (int q = 0; q < kQ; ++q) {
-        const int u = base + q * 32 + lane;
-        const bool ok = u < w1;
-        const uint32_t id = static_cast<uint32_t>(a0 + 4 * u);
-        st.push(cur[q].x, id + 0, ok);
-        st.push(cur[q].y, id + 1, ok);
-        st.push(cur[q].z, id + 2, ok);
-        st.push(cur[q].w, id + 3, ok);
-        st.drain();
+        if (base + q * 32 + lane < w1) {
+          mask |= (!(cur[q].x < st.tau_v) ? 1u : 0u) << (4 * q + 0);
+          mask |= (!(cur[q].y < st.tau_v) ? 1u : 0u) << (4 * q + 1);
+          mask |= (!(cur[q].z < st.tau_v) ? 1u : 0u) << (4 * q + 2);
+          mask |= (!(cur[q].w < st.tau_v) ? 1u : 0u) << (4 * q + 3);
+        }
       }
+      while (__any_sync(kFull, mask != 0u)) {
+        const bool has = mask != 0u;
+        const int bit = has ? __ffs(mask) - 1 : 0;
+        mask &= mask - 1u;
+        const int u = base + (bit >> 2) * 32 + lane;
+        st.push(pick16(cur, bit), static_cast<uint32_t>(a0 + 4 * u + (bit & 3)), has);
+        if (st.cnt > kBuf - 32) st.drain();
+      }
+      st.drain();
     }
 #pragma unroll
     for (int q = 0; q < kQ; ++q) cur[q] = nxt[q];

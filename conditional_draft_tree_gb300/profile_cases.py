@@ -1,0 +1,84 @@
+"""Fixed single-GPU workloads for kernel profiling and timing.
+
+    python -m conditional_draft_tree_gb300.profile_cases topm  [--reps R] [--cfg C]
+        top-M of a workload's base logits (Qwen3-8B batch 32 by default:
+        480 rows x 151936 fp32, 292 MB) through dt_select_topm_noalloc, whose
+        top-M kernel and launch shape are those of dt_build_trees. Only the
+        logits and the outputs live on the device.
+    python -m conditional_draft_tree_gb300.profile_cases round [--reps R] [--cfg C]
+        R whole dt_build_trees rounds of the workload (weights, prepared table
+        and workspace on the device: about 3.5 GB for the default workload).
+
+Each case does one untimed launch first, then R timed ones (CUDA events on the
+current stream, L2 flushed by a 256 MB write before each), and prints one line
+with the mean time. Run it under ncu with -k / -s / -c to capture one launch.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+import conditional_draft_tree_gb300 as dt
+import dt_workloads as W
+
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _timed(fn, reps, dev):
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    fn()
+    torch.cuda.synchronize()
+    ms = []
+    for i in range(reps):
+        flush.fill_(i & 0xff)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    return sum(ms) / len(ms)
+
+
+def case_topm(cfg, reps, dev):
+    wl = W.make_workload(cfg)
+    logits = torch.from_numpy(wl.base_logits).to(dev)
+    topm = torch.empty(wl.batch, wl.D, wl.M, dtype=torch.int32, device=dev)
+    status = torch.empty(wl.batch, dtype=torch.int32, device=dev)
+
+    def run():
+        rc = dt.select_topm_noalloc(logits, wl.M, topm, status)
+        if rc != dt.OK:
+            raise dt.DtError(dt.status_string(rc))
+
+    ms = _timed(run, reps, dev)
+    gbs = logits.numel() * 4 / (ms * 1e-3) / 1e9
+    print(f"topm {wl.name}: rows={wl.batch * wl.D} V={wl.V} M={wl.M} "
+          f"mean_us={1000 * ms:.1f} GB/s={gbs:.0f}")
+
+
+def case_round(cfg, reps, dev):
+    wl = W.make_workload(cfg)
+    tb = dt.TreeBuilder.from_numpy(wl, device=dev)
+    inp = tb.inputs_to_device(wl)
+    out = dt.alloc_outputs(tb.dims, dev)
+    ms = _timed(lambda: tb.run(**inp, out=out), reps, dev)
+    print(f"round {wl.name}: batch={wl.batch} mean_us={1000 * ms:.1f} "
+          f"trees/s={wl.batch / (ms * 1e-3):.0f}")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["topm", "round"])
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--cfg", type=int, default=3)
+    args = ap.parse_args()
+    dev = torch.device("cuda", 0)
+    from conditional_draft_tree_gb300 import build
+    build.build()
+    {"topm": case_topm, "round": case_round}[args.case](args.cfg, args.reps, dev)
+
+
+if __name__ == "__main__":
+    main()

@@ -269,11 +269,12 @@ def main():
     clocks = clk.stop()
     ctrl = tb.workspace[:32].view(torch.int32).cpu().tolist()   # search counters of the last round
     search_steps, search_expansions = ctrl[4], ctrl[5]
-    t_ns = tb.workspace[32:32 + 128].view(torch.int64).cpu().tolist()
-    search_split_us = dict(zip(["gemm", "barrier1", "reduce", "barrier2", "tail", "barrier3",
-                                "tail_score", "tail_pop_select", "tail_gru", "gemm_mma",
-                                "gemm_epilogue", "gemm_wait_copies", "gemm_wait_mma",
-                                "score1_loads", "score1_candidates", "score1_softmax_sort"],
+    t_ns = tb.workspace[32:32 + 8 * 24].view(torch.int64).cpu().tolist()
+    search_split_us = dict(zip(["gemm", "barrier1", "score_reduce", "barrier2", "tail",
+                                "barrier3", "tail_children", "tail_pop_select", "gru",
+                                "gemm_mma", "gemm_epilogue", "gemm_wait_copies", "gemm_wait_mma",
+                                "score1_h", "score1_candidates", "score1_softmax_sort",
+                                "barrier4"],
                                [x / 1000.0 for x in t_ns]))
     per = [ph[i][0].elapsed_time(ph[i][3]) for i in range(K)]
     topm_ms = [ph[i][0].elapsed_time(ph[i][1]) for i in range(K)]

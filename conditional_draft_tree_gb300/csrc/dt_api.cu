@@ -148,7 +148,7 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   p->off_gin = off;       off = al(off + sizeof(float) * cols * d.d_s);
   p->off_p = off;         off = al(off + sizeof(float) * cols * d.r);
   p->off_colexp = off;    off = al(off + sizeof(int) * (cols + wave));
-  p->off_colinfo = off;   off = al(off + (sizeof(int) + sizeof(float)) * cols);
+  p->off_colinfo = off;   off = al(off + (3 * sizeof(int) + sizeof(float)) * cols);
   p->off_kids = off;      off = al(off + (sizeof(float) + sizeof(int32_t)) * cols * d.k);
   p->off_upart = off;
   off = al(off + (p->proj_ksplit > 1 ? sizeof(float) * p->proj_ksplit * rows * d.r : 0));

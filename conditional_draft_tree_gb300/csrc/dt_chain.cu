@@ -76,6 +76,7 @@ struct ChainParams {
   // node (written with the selection); its k children once scored
   int *col_dep;
   float *col_score;
+  int *col_tok, *col_par;   // GRU input token and parent expansion (-1: state0) per slot
   float *kid_score;
   int32_t *kid_tok;
   // tensor-core GEMM path (bf16 weights): A tiles of 128 rows x kc K stay in
@@ -96,14 +97,6 @@ struct ChainParams {
   int sm_A, sm_B, sm_mbar, sm_tmem, sm_run_hs, sm_vhs;
 };
 
-// One GRU cell to evaluate: input row G[tok], recurrent half gh, previous state
-// sp; the new state goes to s_out and to GEMM input column `slot`.
-struct GruJob {
-  int tok, slot;
-  const float *gh, *sp;
-  float *s_out;
-};
-
 struct TailState {
   int count;      // nodes popped so far (root excluded)
   int n_runs;
@@ -112,7 +105,6 @@ struct TailState {
   int n_sel;
   int spec_used;  // speculative (non-stall) expansions made so far
   int sel_e[DT_MAX_SPEC];
-  GruJob jobs[DT_MAX_SPEC];
   float T;
   int status;
 };
@@ -652,11 +644,12 @@ __device__ __forceinline__ void write_column4(const ChainParams &p, int slot, in
   }
 }
 
-// GRU cells of the chosen nodes: S_e = GRU(S_parent, x = E[tok]) with the input
-// half taken from the prepared table row G[tok] (= W_ih E[tok] + b_ih) and the
-// recurrent half gh_parent (= W_hh S_parent + b_hh) from an earlier GEMM. All
-// nodes are processed together, four units per item and two items per thread
-// in flight, so that the gathers of G rows overlap.
+// GRU cells of the nodes chosen for expansion, spread over the grid:
+// S_e = GRU(S_parent, x = E[tok]) with the input half taken from the prepared
+// table row G[tok] (= W_ih E[tok] + b_ih) and the recurrent half gh_parent
+// (= W_hh S_parent + b_hh) from an earlier GEMM (the root: state0 and the gh of
+// the state0 column). Four units per item, two items per thread in flight; the
+// new state goes to S_store and, as the next GEMM's input, to its column.
 __device__ __forceinline__ float gru_unit(float gir, float giz, float gin, float ghr, float ghz,
                                           float ghn, float sp) {
   const float r = sigmoidf_(gir + ghr);
@@ -665,40 +658,51 @@ __device__ __forceinline__ float gru_unit(float gir, float giz, float gin, float
   return (1.f - z) * n + z * sp;
 }
 
-__device__ void gru_jobs(const ChainParams &p, const GruJob *jobs, int njobs) {
+__device__ void gru_phase(const ChainParams &p, const int *slots, int total) {
   const int ds = p.d_s, q4 = ds / 4;
-  const int items = njobs * q4;
+  const int items = total * q4;
+  const int stride = gridDim.x * kThreads;
   constexpr int IT = 2;
-  for (int i0 = threadIdx.x; i0 < items; i0 += IT * kThreads) {
+  for (int i0 = blockIdx.x * kThreads + threadIdx.x; i0 < items; i0 += IT * stride) {
     float4 gi[IT][3], gh[IT][3], sp[IT];
-    int jn[IT], u[IT];
+    int slot[IT], u[IT];
+    size_t so[IT];
 #pragma unroll
     for (int k = 0; k < IT; ++k) {
-      const int i = i0 + k * kThreads;
-      jn[k] = (i < items) ? i / q4 : -1;
-      u[k] = (i % q4) * 4;
-      if (jn[k] >= 0) {
-        const GruJob &J = jobs[jn[k]];
-        const float *g = p.G + static_cast<size_t>(J.tok) * 3 * ds + u[k];
+      const int i = i0 + k * stride;
+      slot[k] = -1;
+      if (i < items) {
+        const int c = i / q4;
+        u[k] = (i - c * q4) * 4;
+        slot[k] = slots[c];
+        const int b = slot[k] / p.P;
+        const int e = __ldcg(p.colexp + slot[k]);
+        const int pe = __ldcg(p.col_par + slot[k]);
+        const int tok = __ldcg(p.col_tok + slot[k]);
+        const size_t ebase = static_cast<size_t>(b) * (p.e_cap + 1);
+        const float *g = p.G + static_cast<size_t>(tok) * 3 * ds + u[k];
+        const float *ghp = p.gh_store + (ebase + (pe < 0 ? p.e_cap : pe)) * 3 * ds + u[k];
+        const float *spp = pe < 0 ? p.state0 + static_cast<size_t>(p.b0 + b) * ds + u[k]
+                                  : p.S_store + (ebase + pe) * ds + u[k];
+        so[k] = (ebase + e) * ds + u[k];
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
           gi[k][q] = __ldg(reinterpret_cast<const float4 *>(g + q * ds));
-          gh[k][q] = __ldcg(reinterpret_cast<const float4 *>(J.gh + q * ds + u[k]));
+          gh[k][q] = __ldcg(reinterpret_cast<const float4 *>(ghp + q * ds));
         }
-        sp[k] = __ldcg(reinterpret_cast<const float4 *>(J.sp + u[k]));
+        sp[k] = __ldcg(reinterpret_cast<const float4 *>(spp));
       }
     }
 #pragma unroll
     for (int k = 0; k < IT; ++k) {
-      if (jn[k] < 0) continue;
-      const GruJob &J = jobs[jn[k]];
+      if (slot[k] < 0) continue;
       float4 s;
       s.x = gru_unit(gi[k][0].x, gi[k][1].x, gi[k][2].x, gh[k][0].x, gh[k][1].x, gh[k][2].x, sp[k].x);
       s.y = gru_unit(gi[k][0].y, gi[k][1].y, gi[k][2].y, gh[k][0].y, gh[k][1].y, gh[k][2].y, sp[k].y);
       s.z = gru_unit(gi[k][0].z, gi[k][1].z, gi[k][2].z, gh[k][0].z, gh[k][1].z, gh[k][2].z, sp[k].z);
       s.w = gru_unit(gi[k][0].w, gi[k][1].w, gi[k][2].w, gh[k][0].w, gh[k][1].w, gh[k][2].w, sp[k].w);
-      *reinterpret_cast<float4 *>(J.s_out + u[k]) = s;
-      write_column4(p, J.slot, u[k], s);
+      *reinterpret_cast<float4 *>(p.S_store + so[k]) = s;
+      write_column4(p, slot[k], u[k], s);
     }
   }
   if (p.umma) fence_async_global();   // the columns are read by bulk copies next
@@ -1002,7 +1006,10 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
     __syncwarp();
   }
   if (done) {
-    if (lane == 0) { ts.count = count; ts.n_runs = n_runs; ts.n_sel = 0; ts.done = 2; }
+    if (lane == 0) {
+      ts.count = count; ts.n_runs = n_runs; ts.n_sel = 0; ts.done = 2;
+      p.col_count[b] = 0;
+    }
     __syncwarp();
     return;
   }
@@ -1106,21 +1113,12 @@ template <int WDT, int SLOTS>
 __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, int b) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ncols = ts.n_sel;
-  const size_t ebase = static_cast<size_t>(b) * (p.e_cap + 1);
   if (ts.e_count == 0) {
     // the root: S_0 = GRU(state0, E[anchor]); its recurrent half came from the state0 column
     const int anchor = p.anchor[p.b0 + b];
     if (threadIdx.x == 0) {
-      GruJob &J = ts.jobs[0];
-      J.tok = anchor;
-      J.slot = b * p.P;
-      J.gh = p.gh_store + (ebase + p.e_cap) * 3 * p.d_s;
-      J.sp = p.state0 + static_cast<size_t>(p.b0 + b) * p.d_s;
-      J.s_out = p.S_store + ebase * p.d_s;
-    }
-    __syncthreads();
-    gru_jobs(p, ts.jobs, 1);
-    if (threadIdx.x == 0) {
+      p.col_tok[b * p.P] = anchor;
+      p.col_par[b * p.P] = -1;
       t.exp_depth[0] = 0; t.exp_parent[0] = -1; t.exp_score[0] = 0.0f; t.exp_tok[0] = anchor;
       ts.e_count = 1;
       ts.n_sel = 1;
@@ -1158,20 +1156,13 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
   __syncthreads();
   if (clock_me) { const uint64_t n = global_ns(); p.ctrl->t_ns[7] += n - t0; t0 = n; }
   if (ts.done == 2) { finalize(p, t, ts, b, true); return; }
-  // 3. GRU states of the chosen nodes
+  // 3. the GRU jobs of the chosen nodes (run grid-wide next)
   if (threadIdx.x < ts.n_sel) {
-    const int i = threadIdx.x, e = ts.sel_e[i], pe = t.exp_parent[e];
-    GruJob &J = ts.jobs[i];
-    J.tok = t.exp_tok[e];
-    J.slot = b * p.P + i;
-    J.gh = p.gh_store + (ebase + pe) * 3 * p.d_s;
-    J.sp = p.S_store + (ebase + pe) * p.d_s;
-    J.s_out = p.S_store + (ebase + e) * p.d_s;
+    const int i = threadIdx.x, e = ts.sel_e[i];
+    p.col_tok[b * p.P + i] = t.exp_tok[e];
+    p.col_par[b * p.P + i] = t.exp_parent[e];
   }
   __syncthreads();
-  gru_jobs(p, ts.jobs, ts.n_sel);
-  __syncthreads();
-  if (clock_me) p.ctrl->t_ns[8] += global_ns() - t0;
 }
 
 template <int WDT, int SLOTS>
@@ -1258,6 +1249,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     if (threadIdx.x == 0) s_active = ld_acquire_s32(&p.ctrl->active);
     __syncthreads();
     if (s_active == 0) break;
+    {
+      int *slots = reinterpret_cast<int *>(smem + p.sm_scratch);
+      gru_phase(p, slots, compact_slots(p, slots));
+    }
+    lap(8);
+    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
+                      false);
+    lap(16);
+    if (!ok) break;
   }
   if (tail && !ts.done) {
     if (threadIdx.x == 0) ts.status = DT_ERR_TIMEOUT;
@@ -1363,6 +1363,8 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.col_count = cp.colexp + static_cast<size_t>(pl.wave) * pl.spec;
   cp.col_dep = reinterpret_cast<int *>(w + pl.off_colinfo);
   cp.col_score = reinterpret_cast<float *>(cp.col_dep + static_cast<size_t>(pl.wave) * pl.spec);
+  cp.col_tok = reinterpret_cast<int *>(cp.col_score + static_cast<size_t>(pl.wave) * pl.spec);
+  cp.col_par = cp.col_tok + static_cast<size_t>(pl.wave) * pl.spec;
   cp.kid_score = reinterpret_cast<float *>(w + pl.off_kids);
   cp.kid_tok = reinterpret_cast<int32_t *>(cp.kid_score +
                                            static_cast<size_t>(pl.wave) * pl.spec * d.k);

@@ -39,12 +39,14 @@ struct Ctrl {
   unsigned int steps;      // lockstep steps of the last search launch
   unsigned int expansions; // expansions of the last search launch
   unsigned int pad[2];
-  // block 0 of the last search launch, ns summed over steps: GEMM, barrier,
-  // scoring + reduction, barrier, tail, barrier; tail parts: reading the
-  // children, pops and selection, GRU; GEMM parts: MMA loop, epilogue
-  // then: GEMM waits for B copies, GEMM waits for MMA completion; scoring of
-  // block 0's first node: h, candidate loop (incl. block sync), softmax + sort + write
-  unsigned long long t_ns[16];
+  // block 0 of the last search launch, ns summed over steps: [0] GEMM,
+  // [1] barrier, [2] scoring + reduction, [3] barrier, [4] tail, [5] barrier;
+  // tail parts: [6] reading the children, [7] pops and selection; [8] GRU
+  // phase; GEMM parts: [9] MMA loop, [10] epilogue, [11] waits for B copies,
+  // [12] waits for MMA completion; scoring of block 0's first node: [13] h,
+  // [14] candidate loop (incl. block sync), [15] softmax + sort + write;
+  // [16] barrier after the GRU phase
+  unsigned long long t_ns[24];
   // followed by: unsigned row_ticket[batch * D]; int req_flags[batch]; gemm tickets
 };
 

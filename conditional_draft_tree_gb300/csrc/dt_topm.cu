@@ -287,14 +287,59 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
   st.s_tau = &s_tau;
   st.set_tau(0ull);
 
-  // kQ float4 per lane per iteration, the next iteration's loads in flight
+  // kQ float4 per lane per tile; two register tiles alternate so that the next
+  // tile's loads are in flight while this one is filtered
   const float4 *vec = reinterpret_cast<const float4 *>(rowp + a0);
-  float4 cur[kQ], nxt[kQ];
+  auto load_tile = [&](float4 (&dst)[kQ], int b) {
+    if (b + kQ * 32 <= w1) {                     // warp-uniform: a full tile
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) {
-    const int u = w0 + q * 32 + lane;
-    cur[q] = (u < w1) ? __ldcs(vec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+      for (int q = 0; q < kQ; ++q) dst[q] = __ldcs(vec + b + q * 32 + lane);
+    } else {
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const int u = b + q * 32 + lane;
+        dst[q] = (u < w1) ? __ldcs(vec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  };
+  auto filter_tile = [&](const float4 (&c)[kQ], int b) {
+    const bool full = b + kQ * 32 <= w1;
+    st.sync_tau();
+    // NaN-propagating maximum: a NaN (or +inf) forces the slow path, where
+    // push() flags it; -inf is an ordinary (masked) value
+    bool any = false;
+#pragma unroll
+    for (int q = 0; q < kQ; ++q) {
+      const bool ok = full || b + q * 32 + lane < w1;
+      const float m4 = fmax_nan(fmax_nan(c[q].x, c[q].y), fmax_nan(c[q].z, c[q].w));
+      any |= ok && !(m4 < st.tau_v);
+    }
+    if (__any_sync(kFull, any)) {
+      // only the elements at or above the threshold (or NaN): one push round
+      // per element of the busiest lane, usually one or two
+      uint32_t mask = 0u;
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        if (full || b + q * 32 + lane < w1) {
+          mask |= (!(c[q].x < st.tau_v) ? 1u : 0u) << (4 * q + 0);
+          mask |= (!(c[q].y < st.tau_v) ? 1u : 0u) << (4 * q + 1);
+          mask |= (!(c[q].z < st.tau_v) ? 1u : 0u) << (4 * q + 2);
+          mask |= (!(c[q].w < st.tau_v) ? 1u : 0u) << (4 * q + 3);
+        }
+      }
+      while (__any_sync(kFull, mask != 0u)) {
+        const bool has = mask != 0u;
+        const int bit = has ? __ffs(mask) - 1 : 0;
+        mask &= mask - 1u;
+        const int u = b + (bit >> 2) * 32 + lane;
+        st.push(pick16(c, bit), static_cast<uint32_t>(a0 + 4 * u + (bit & 3)), has);
+        if (st.cnt > kBuf - 32) st.drain();
+      }
+      st.drain();
+    }
+  };
+  float4 ta[kQ], tb[kQ];
+  load_tile(ta, w0);
   // starting threshold from the first tile of every warp: the q-th largest of
   // a warp's lane maxima is a value that at least q of its elements reach, so
   // the smallest such value over the warps is reached by at least M elements
@@ -305,7 +350,7 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
 #pragma unroll
     for (int q = 0; q < kQ; ++q) {
       if (w0 + q * 32 + lane < w1)
-        lm = fmaxf(lm, fmaxf(fmaxf(cur[q].x, cur[q].y), fmaxf(cur[q].z, cur[q].w)));
+        lm = fmaxf(lm, fmaxf(fmaxf(ta[q].x, ta[q].y), fmaxf(ta[q].z, ta[q].w)));
     }
     const float t = warp_kth_largest(lm, st.qi, lane);
     if (lane == 0) s_wq[warp] = static_cast<unsigned long long>(__float_as_uint(t));
@@ -320,47 +365,13 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
     if (t0 > ninf && st.qi < 32) st.set_tau(make_key(t0, 0xffffffffu));
     __syncthreads();
   }
-  for (int base = w0; base < w1; base += kQ * 32) {
-#pragma unroll
-    for (int q = 0; q < kQ; ++q) {
-      const int u = base + kQ * 32 + q * 32 + lane;
-      nxt[q] = (u < w1) ? __ldcs(vec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    st.sync_tau();
-    // NaN-propagating maximum: a NaN (or +inf) forces the slow path, where
-    // push() flags it; -inf is an ordinary (masked) value
-    bool any = false;
-#pragma unroll
-    for (int q = 0; q < kQ; ++q) {
-      const bool ok = base + q * 32 + lane < w1;
-      const float m4 = fmax_nan(fmax_nan(cur[q].x, cur[q].y), fmax_nan(cur[q].z, cur[q].w));
-      any |= ok && !(m4 < st.tau_v);
-    }
-    if (__any_sync(kFull, any)) {
-      // only the elements at or above the threshold (or NaN): one push round
-      // per element of the busiest lane, usually one or two
-      uint32_t mask = 0u;
-#pragma unroll
-      for (int q = 0; q < kQ; ++q) {
-        if (base + q * 32 + lane < w1) {
-          mask |= (!(cur[q].x < st.tau_v) ? 1u : 0u) << (4 * q + 0);
-          mask |= (!(cur[q].y < st.tau_v) ? 1u : 0u) << (4 * q + 1);
-          mask |= (!(cur[q].z < st.tau_v) ? 1u : 0u) << (4 * q + 2);
-          mask |= (!(cur[q].w < st.tau_v) ? 1u : 0u) << (4 * q + 3);
-        }
-      }
-      while (__any_sync(kFull, mask != 0u)) {
-        const bool has = mask != 0u;
-        const int bit = has ? __ffs(mask) - 1 : 0;
-        mask &= mask - 1u;
-        const int u = base + (bit >> 2) * 32 + lane;
-        st.push(pick16(cur, bit), static_cast<uint32_t>(a0 + 4 * u + (bit & 3)), has);
-        if (st.cnt > kBuf - 32) st.drain();
-      }
-      st.drain();
-    }
-#pragma unroll
-    for (int q = 0; q < kQ; ++q) cur[q] = nxt[q];
+  for (int base = w0; base < w1; base += 2 * kQ * 32) {
+    const int b2 = base + kQ * 32;
+    if (b2 < w1) load_tile(tb, b2);
+    filter_tile(ta, base);
+    if (b2 >= w1) break;
+    if (b2 + kQ * 32 < w1) load_tile(ta, b2 + kQ * 32);
+    filter_tile(tb, b2);
   }
   // scalar head (split 0) and tail (last split), warp 0
   if (warp == 0) {

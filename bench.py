@@ -274,7 +274,8 @@ def main():
                                 "barrier3", "tail_children", "tail_pop_select", "gru",
                                 "gemm_mma", "gemm_epilogue", "gemm_wait_copies", "gemm_wait_mma",
                                 "score1_h", "score1_candidates", "score1_softmax_sort",
-                                "barrier4"],
+                                "barrier4", "csum_sync1", "csum_send", "csum_sync2",
+                                "csum_add"],
                                [x / 1000.0 for x in t_ns]))
     per = [ph[i][0].elapsed_time(ph[i][3]) for i in range(K)]
     topm_ms = [ph[i][0].elapsed_time(ph[i][1]) for i in range(K)]

@@ -21,6 +21,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, -1, -2, -3
 ERR_NONFINITE, ERR_TIMEOUT, ERR_BAD_TEMPERATURE = -4, -5, -6
 F32, BF16 = 0, 1
 NUM_PHASE_EVENTS = 4
+OPT_CLUSTER_SUM = 1          # dt_options.flags: K-chunk sums in distributed shared memory
 MAX_SPEC = 16
 
 # every symbol include/dt.h declares
@@ -46,7 +47,8 @@ class DtTreeOut(C.Structure):
 
 
 class DtOptions(C.Structure):
-    _fields_ = [("spec_width", C.c_int), ("phase_events", C.POINTER(C.c_void_p))]
+    _fields_ = [("spec_width", C.c_int), ("phase_events", C.POINTER(C.c_void_p)),
+                ("flags", C.c_int)]
 
 
 class DtError(RuntimeError):
@@ -111,9 +113,10 @@ def _stream(stream):
     return s.cuda_stream
 
 
-def options(spec_width: int = 0, events=None) -> DtOptions:
-    """Build a dt_options; ``events``: DT_NUM_PHASE_EVENTS torch.cuda.Event or None."""
-    o = DtOptions(spec_width, None)
+def options(spec_width: int = 0, events=None, flags: int = 0) -> DtOptions:
+    """Build a dt_options; ``events``: DT_NUM_PHASE_EVENTS torch.cuda.Event or None;
+    ``flags``: OPT_* bits."""
+    o = DtOptions(spec_width, None, flags)
     if events is not None:
         arr = (C.c_void_p * NUM_PHASE_EVENTS)(*[e.cuda_event for e in events])
         o.phase_events = C.cast(arr, C.POINTER(C.c_void_p))
@@ -224,11 +227,11 @@ class TreeBuilder:
     device and prepares them; ``run(...)`` builds one round on device tensors."""
 
     def __init__(self, dims: DtDims, weights: DeviceWeights, spec_width: int = 0,
-                 device="cuda"):
+                 device="cuda", flags: int = 0):
         self.dims = dims
         self.w = weights
         self.device = torch.device(device)
-        self.opt = options(spec_width)
+        self.opt = options(spec_width, flags=flags)
         nbytes = prepared_bytes(dims)
         if nbytes == 0:
             raise DtError("invalid dims")
@@ -254,10 +257,10 @@ class TreeBuilder:
                              W2=t(wl.W2), b_ih=t(wl.b_ih), b_hh=t(wl.b_hh))
 
     @classmethod
-    def from_numpy(cls, wl, spec_width: int = 0, device="cuda", batch=None):
+    def from_numpy(cls, wl, spec_width: int = 0, device="cuda", batch=None, flags: int = 0):
         dims = dims_of(wl.V, wl.d, wl.d_s, wl.r, wl.D, wl.M, wl.k, wl.N,
                        wl.batch if batch is None else batch)
-        return cls(dims, cls.weights_from_numpy(wl, device), spec_width, device)
+        return cls(dims, cls.weights_from_numpy(wl, device), spec_width, device, flags)
 
     def run(self, base_logits, H, state0, anchor_tok, temperature=None, out=None, stream=None,
             opt=None):

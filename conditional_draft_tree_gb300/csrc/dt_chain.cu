@@ -82,6 +82,7 @@ struct ChainParams {
   // tensor-core GEMM path (bf16 weights): A tiles of 128 rows x kc K stay in
   // shared memory; the input columns arrive as three bf16 terms per state
   int umma, n_mt, ks, kc, cols_cap;
+  int cluster;         // 0, or the cluster size (= ks): K chunks summed in distributed shared memory
   float *partial;      // [ks][cols_cap][R] per-K-chunk partial products, by slot
   uint16_t *gin16;     // B operand in tile layout (bcol_index)
   Ctrl *ctrl;
@@ -347,7 +348,112 @@ __device__ __forceinline__ size_t bcol_index(const ChainParams &p, int slot, int
 struct UmmaState {
   uint32_t tmem;      // TMEM base column address
   uint32_t next;      // global index of the next B slice (buffer = next % kBufs)
+  uint32_t cphase;    // uses of the cluster barrier so far
 };
+
+// Bounded barrier of the CTAs of one cluster: every CTA arrives on every CTA's
+// barrier (count = cluster size) and waits on its own, with a time limit.
+__device__ bool cluster_sync(uint64_t *cbar, int cs, uint32_t &phase, uint64_t limit_ns) {
+  __shared__ int s_cok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t a = smem_u32(cbar);
+    for (int q = 0; q < cs; ++q) mbar_arrive_remote(mapa_u32(a, q));
+    s_cok = mbar_wait_cluster(cbar, phase & 1u, limit_ns) ? 1 : 0;
+  }
+  ++phase;
+  __syncthreads();
+  return s_cok != 0;
+}
+
+// The K-chunk sum of one pass inside the cluster of an M tile, in rounds of 128
+// columns. CTA q owns the columns [q * owned, (q + 1) * owned) of a round.
+// Every CTA reads its accumulator columns from TMEM (one row per lane) and
+// stores them, four columns per 16-byte store, into the owner's receive
+// buffer [sender rank][row][column] in distributed shared memory; after a
+// cluster barrier each owner sums its columns over the senders in chunk order
+// (the order of the global-memory path) and writes [gh; p] (+ [b_hh; 0]).
+__device__ bool cluster_reduce(const ChainParams &p, unsigned char *sB, uint64_t *cbar,
+                               UmmaState &u, int pass, int hi, const uint32_t *mask, int mt,
+                               int rank) {
+  __shared__ long long s_ghoff[256];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cs = p.cluster, ds = p.d_s, R = 3 * ds + p.r;
+  const int owned = ((128 + cs - 1) / cs + 3) & ~3;   // columns per owner and round
+  float *recv = reinterpret_cast<float *>(sB);        // [cs][128][owned]
+  const uint32_t recv_a = smem_u32(recv);
+  for (int c = threadIdx.x; c < 256; c += kThreads) {
+    long long off = -1;
+    if (c < hi && ((mask[c >> 5] >> (c & 31)) & 1u)) {
+      const int slot = pass * 256 + c;
+      const int e = __ldcg(p.colexp + slot);
+      const int e_slot = (e == kState0) ? p.e_cap : e;
+      off = (static_cast<long long>(slot / p.P) * (p.e_cap + 1) + e_slot) * 3 * ds;
+    }
+    s_ghoff[c] = off;
+  }
+  bool ok = true;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int row_l = quarter * 32 + lane;              // this lane's TMEM lane = tile row
+  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
+  uint64_t tc = clock_me ? global_ns() : 0;
+  auto lap = [&](int k) {
+    if (clock_me) {
+      const uint64_t n = global_ns();
+      p.ctrl->t_ns[k] += n - tc;
+      tc = n;
+    }
+  };
+  for (int r0 = 0; r0 < hi; r0 += 128) {
+    // the receive buffers alias the B slices: every CTA's MMAs (round 0) and
+    // sums (later rounds) must be done before the stores
+    ok &= cluster_sync(cbar, cs, u.cphase, p.limit_ns);
+    lap(17);
+    // send: warp (quarter, half) covers columns r0 + 64 half + [0, 64)
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const int c32 = r0 + 64 * half + 32 * g;
+      if (c32 < hi && mask[c32 >> 5] != 0u) {
+        float v[32];
+        tmem_ld32(u.tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const int cl = c32 - r0 + j;                 // column within the round
+          const int owner = cl / owned, co = cl - owner * owned;
+          const uint32_t off = static_cast<uint32_t>(((rank * 128 + row_l) * owned + co) * 4);
+          st_cluster_f4(mapa_u32(recv_a + off, owner), v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+      }
+    }
+    lap(18);
+    ok &= cluster_sync(cbar, cs, u.cphase, p.limit_ns);
+    lap(19);
+    // sum: item = (column group of 4, row); lanes take consecutive rows
+    const int c_beg = r0 + rank * owned;
+    for (int it = threadIdx.x; it < (owned / 4) * 128; it += kThreads) {
+      const int g4 = it >> 7, rl = it & 127;
+      const int row = mt * 128 + rl;
+      if (row >= R) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int z = 0; z < cs; ++z) {
+        const float4 v = *reinterpret_cast<const float4 *>(recv + (z * 128 + rl) * owned + 4 * g4);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+      const float bias = (row < 3 * ds && p.b_hh) ? p.b_hh[row] : 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = c_beg + 4 * g4 + q;
+        if (c - r0 >= 128 || c >= hi || s_ghoff[c] < 0) continue;
+        if (row < 3 * ds) p.gh_store[s_ghoff[c] + row] = a4[q] + bias;
+        else p.pbuf[static_cast<size_t>(pass * 256 + c) * p.r + (row - 3 * ds)] = a4[q];
+      }
+    }
+    lap(20);
+  }
+  return ok;
+}
 
 // Partial products of this block's (M tile, K chunk) for every active column,
 // written to p.partial[kz][slot][row]. D (TMEM, 128 rows x up to 256 node
@@ -397,6 +503,7 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
                                  static_cast<size_t>(pass * p.ks + kz) * nkb * kSliceBytes;
       const uint32_t g0 = u.next;
       fence_async_global();   // columns written before the grid barrier -> bulk reads
+      fence_async_smem();     // earlier generic use of the stage buffers -> bulk writes
       auto issue = [&](int s) {
         const uint32_t g = g0 + s, buf = g % kBufs;
         // the buffer's previous slice must be consumed by its MMAs
@@ -439,6 +546,18 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
     tmem_fence_after();
     const uint64_t t1 = clock_me ? global_ns() : 0;
     if (clock_me) p.ctrl->t_ns[9] += t1 - t0;
+    if (p.cluster) {
+      fence_async_smem();
+      ok &= cluster_reduce(p, sB, full + 2 * kBufs, u, pass, hi, s_mask[pass], mt, kz);
+      bool more = false;
+      for (int q = pass + 1; q < n_pass; ++q) more |= s_hi[q] > 0;
+      // the next pass's copies overwrite the stages: every CTA must be done reading
+      if (more) ok &= cluster_sync(full + 2 * kBufs, p.cluster, u.cphase, p.limit_ns);
+      tmem_fence_before();
+      __syncthreads();
+      if (clock_me) p.ctrl->t_ns[10] += global_ns() - t1;
+      continue;
+    }
     // epilogue: TMEM lane = row of the tile; warps w and w+4 share a lane quarter
     const int quarter = warp & 3;
     const int row = mt * 128 + quarter * 32 + lane;
@@ -463,68 +582,67 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
   return ok;
 }
 
-// Sum of the K-chunk partials (fixed order) + b_hh into gh_store. Each
-// thread takes kRI float4 items at a time and, for up to kRZ chunks, issues all
-// their loads before adding, so that the L2 latency is paid about once.
-constexpr int kRI = 3;
-constexpr int kRZ = 6;
-
-__device__ __forceinline__ void store_reduced(const ChainParams &p, int slot, int row, float4 acc) {
-  const int ds = p.d_s;
-  if (row < 3 * ds) {
-    const int b = slot / p.P;
-    const int e = __ldcg(p.colexp + slot);
-    const int e_slot = (e == kState0) ? p.e_cap : e;
-    if (p.b_hh) {
-      acc.x += p.b_hh[row]; acc.y += p.b_hh[row + 1];
-      acc.z += p.b_hh[row + 2]; acc.w += p.b_hh[row + 3];
-    }
-    *reinterpret_cast<float4 *>(
-        p.gh_store + (static_cast<size_t>(b) * (p.e_cap + 1) + e_slot) * 3 * ds + row) = acc;
-  } else {
-    *reinterpret_cast<float4 *>(p.pbuf + static_cast<size_t>(slot) * p.r + (row - 3 * ds)) = acc;
-  }
-}
-
-__device__ void reduce_phase(const ChainParams &p, const int *slots, int total) {
-  const int R = 3 * p.d_s + p.r, R4 = 3 * p.d_s / 4;   // the gh rows (p is summed by the scorers)
+// Sum of the K-chunk partials (fixed order) + b_hh into gh_store, for the
+// columns of the last GEMM (`slots`, and `esl` their expansion slots, both
+// taken before the tails reassign the columns). It runs beside the tails: one
+// column per chunk, chunks handed out by a global counter, so that the blocks
+// without a request start at once and the tails join when they are done. Every
+// block calls this once per step and makes exactly one failing grab, so the
+// counter of the next step starts at base + columns + gridDim.
+__device__ void gh_reduce(const ChainParams &p, const int *slots, const int *esl, int total,
+                          unsigned &base) {
+  __shared__ int s_idx;
+  const int ds = p.d_s, R = 3 * ds + p.r, n4 = 3 * ds / 4;
   const size_t plane = static_cast<size_t>(p.cols_cap) * R;
-  const int n = total * R4;
-  const int stride = gridDim.x * kThreads;
-  for (int i0 = blockIdx.x * kThreads + threadIdx.x; i0 < n; i0 += kRI * stride) {
-    int slot[kRI], row[kRI];
-    const float *src[kRI];
-    float4 acc[kRI];
+  constexpr int IT = 3;
+  while (true) {
+    if (threadIdx.x == 0)
+      s_idx = static_cast<int>(atomicAdd(&p.ctrl->red_next, 1u) - base);
+    __syncthreads();
+    const int col = s_idx;
+    __syncthreads();
+    if (col >= total) break;
+    const int slot = slots[col];
+    float *dst = p.gh_store +
+                 (static_cast<size_t>(slot / p.P) * (p.e_cap + 1) + esl[col]) * 3 * ds;
+    const float *src = p.partial + static_cast<size_t>(slot) * R;
+    for (int i0 = threadIdx.x; i0 < n4; i0 += IT * kThreads) {
+      float4 acc[IT];
 #pragma unroll
-    for (int q = 0; q < kRI; ++q) {
-      const int i = min(i0 + q * stride, n - 1);   // clamped: duplicates are not stored
-      const int col = i / R4;
-      row[q] = (i - col * R4) * 4;
-      slot[q] = slots[col];
-      src[q] = p.partial + static_cast<size_t>(slot[q]) * R + row[q];
-      acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int z0 = 0; z0 < p.ks; z0 += kRZ) {
-      float4 v[kRZ][kRI];
+      for (int q = 0; q < IT; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int z0 = 0; z0 < p.ks; z0 += 4) {
+        float4 v[4][IT];
 #pragma unroll
-      for (int z = 0; z < kRZ; ++z)
+        for (int z = 0; z < 4; ++z)
 #pragma unroll
-        for (int q = 0; q < kRI; ++q)
-          v[z][q] = (z0 + z < p.ks) ? __ldcg(reinterpret_cast<const float4 *>(
-                                          src[q] + static_cast<size_t>(z0 + z) * plane))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q = 0; q < IT; ++q) {
+            const int i = i0 + q * kThreads;
+            v[z][q] = (z0 + z < p.ks && i < n4)
+                          ? __ldcg(reinterpret_cast<const float4 *>(src + (z0 + z) * plane) + i)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
 #pragma unroll
-      for (int z = 0; z < kRZ; ++z)
+        for (int z = 0; z < 4; ++z)
 #pragma unroll
-        for (int q = 0; q < kRI; ++q) {
-          acc[q].x += v[z][q].x; acc[q].y += v[z][q].y;
-          acc[q].z += v[z][q].z; acc[q].w += v[z][q].w;
+          for (int q = 0; q < IT; ++q) {
+            acc[q].x += v[z][q].x; acc[q].y += v[z][q].y;
+            acc[q].z += v[z][q].z; acc[q].w += v[z][q].w;
+          }
+      }
+#pragma unroll
+      for (int q = 0; q < IT; ++q) {
+        const int i = i0 + q * kThreads;
+        if (i >= n4) continue;
+        float4 a = acc[q];
+        if (p.b_hh) {   // 4-byte aligned only
+          a.x += p.b_hh[4 * i]; a.y += p.b_hh[4 * i + 1];
+          a.z += p.b_hh[4 * i + 2]; a.w += p.b_hh[4 * i + 3];
         }
+        reinterpret_cast<float4 *>(dst)[i] = a;
+      }
     }
-#pragma unroll
-    for (int q = 0; q < kRI; ++q)
-      if (i0 + q * stride < n) store_reduced(p, slot[q], row[q], acc[q]);
   }
+  base += static_cast<unsigned>(total) + gridDim.x;
 }
 
 // ---------------------------------------------------------------- tail phase
@@ -750,7 +868,7 @@ __device__ void score_phase(const ChainParams &p, const int *slots, int total, f
       if (SMALL_R) {
         if (lane < nq) {
           float a[8];
-          if (p.umma) {
+          if (p.umma && !p.cluster) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) a[i] = 0.f;
             const float *src = p.partial + static_cast<size_t>(slot) * R + 3 * p.d_s + 8 * lane;
@@ -783,7 +901,7 @@ __device__ void score_phase(const ChainParams &p, const int *slots, int total, f
       } else {
         for (int q = lane; q < p.r; q += 32) {
           float a = 0.f;
-          if (p.umma) {
+          if (p.umma && !p.cluster) {
             for (int z = 0; z < p.ks; ++z)
               a += ldcg(p.partial + z * plane + static_cast<size_t>(slot) * R + 3 * p.d_s + q);
           } else {
@@ -1178,11 +1296,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
   UmmaState u;
   u.tmem = 0;
   u.next = 0;
+  u.cphase = 0;
   if (mma_block) {
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + p.sm_tmem);
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
       for (int i = 0; i < 2 * kBufs; ++i) mbar_init(&mbar[i], 1);
+      if (p.cluster) mbar_init(&mbar[2 * kBufs], static_cast<uint32_t>(p.cluster));
+    }
     load_a_tile(p, smem + p.sm_A);
     fence_async_smem();   // generic stores of the A tile -> tensor-core reads
     if ((threadIdx.x >> 5) == 0) tmem_alloc(tslot, kTmemCols);
@@ -1202,8 +1323,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     }
     fence_async_global();
   }
+  // every CTA's cluster barrier is initialised before any CTA arrives on it
+  if (p.cluster) cluster_sync_all();
   if (tail) tail_init(p, t, ts, b);
-  unsigned bar_target = 0;
+  unsigned bar_target = 0, red_base = 0;
   bool ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
                          false);
   // block 0 accounts its time per phase (for profiling; a few timer reads a step)
@@ -1226,14 +1349,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
                       !gemm_ok);
     lap(1);
     if (!ok) break;
+    // children of the new expansions (their p summed by the scorers); the
+    // columns and their expansion slots are kept for the gh sums of the tail
+    // phase, since the tails reassign the columns
+    int *slots = reinterpret_cast<int *>(smem + p.sm_scratch);
+    int *esl = slots + p.cols_cap;
+    const int total = compact_slots(p, slots);
+    for (int c = threadIdx.x; c < total; c += kThreads) {
+      const int e = __ldcg(p.colexp + slots[c]);
+      esl[c] = (e == kState0) ? p.e_cap : e;
+    }
     {
-      // children of the new expansions (p summed here), then the gh rows
-      int *slots = reinterpret_cast<int *>(smem + p.sm_scratch);
-      const int total = compact_slots(p, slots);
-      float *sc = reinterpret_cast<float *>(smem + p.sm_scratch + ((p.cols_cap * 4 + 15) & ~15));
+      float *sc = reinterpret_cast<float *>(smem + p.sm_scratch + ((2 * p.cols_cap * 4 + 15) & ~15));
       if (p.r <= 256) score_phase<WDT, SLOTS, true>(p, slots, total, sc);
       else score_phase<WDT, SLOTS, false>(p, slots, total, sc);
-      if (p.umma) reduce_phase(p, slots, total);
     }
     lap(2);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
@@ -1241,6 +1370,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     lap(3);
     if (!ok) break;
     if (tail && !ts.done) tail_step<WDT, SLOTS>(p, t, ts, b);
+    if (p.umma && !p.cluster) gh_reduce(p, slots, esl, total, red_base);
     lap(4);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
                       false);
@@ -1269,6 +1399,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     tmem_fence_after();
     if ((threadIdx.x >> 5) == 0) tmem_dealloc(u.tmem, kTmemCols);
   }
+  // no CTA leaves while another CTA of its cluster may still address its memory
+  if (p.cluster) cluster_sync_all();
 }
 
 }  // namespace
@@ -1297,13 +1429,13 @@ static int chain_smem_layout(const Plan &pl, int e_cap, int wave, ChainParams *c
   if (pl.umma) {
     cp->sm_A = off = al(off, 128);    off += 128 * pl.kc * 2;
     cp->sm_B = off = al(off, 128);    off += kBufs * kSliceBytes;
-    cp->sm_mbar = off = al(off, 16);  off += 16 * kBufs;
+    cp->sm_mbar = off = al(off, 16);  off += 16 * kBufs + 8;
     cp->sm_tmem = off;                off += 16;
   }
   cp->sm_scratch = off;
   const int gemm_scratch = al(wave * pl.spec * 4, 16) + (pl.umma ? 0 : kGemmCols * kGemmKC * 4);
   const int score_scratch =
-      al(wave * pl.spec * 4, 16) + kNPB * d.M * 4 + (d.r > 256 ? kWarps * d.r * 4 : 0);
+      al(2 * wave * pl.spec * 4, 16) + kNPB * d.M * 4 + (d.r > 256 ? kWarps * d.r * 4 : 0);
   off += gemm_scratch > score_scratch ? gemm_scratch : score_scratch;
   cp->sm_total = off;
   return off;
@@ -1356,7 +1488,7 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.gin = reinterpret_cast<float *>(w + pl.off_gin);
   cp.pbuf = reinterpret_cast<float *>(w + pl.off_p);
   cp.colexp = reinterpret_cast<int *>(w + pl.off_colexp);
-  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc;
+  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc; cp.cluster = pl.cluster;
   cp.cols_cap = pl.wave * pl.spec;
   cp.partial = pl.umma ? reinterpret_cast<float *>(w + pl.off_partial) : nullptr;
   cp.gin16 = pl.umma ? reinterpret_cast<uint16_t *>(w + pl.off_gin16) : nullptr;
@@ -1381,9 +1513,28 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   // the barrier counters of the control block are re-zeroed for every wave
   e = cudaMemsetAsync(cp.ctrl, 0, sizeof(Ctrl), st);
   if (e != cudaSuccess) return e;
-  void *args[] = {&cp};
-  return cudaLaunchCooperativeKernel(fn, dim3(pl.chain_grid), dim3(kThreads), args,
-                                     pl.chain_smem, st);
+  if (!pl.cluster) {
+    void *args[] = {&cp};
+    return cudaLaunchCooperativeKernel(fn, dim3(pl.chain_grid), dim3(kThreads), args,
+                                       pl.chain_smem, st);
+  }
+  // cooperative (co-resident grid) and clustered: the K chunks of an M tile
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = static_cast<unsigned>(pl.cluster);
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeCooperative;
+  at[1].val.cooperative = 1;
+  cfg.gridDim = dim3(pl.chain_grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.chain_smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, reinterpret_cast<void (*)(ChainParams)>(const_cast<void *>(fn)),
+                            cp);
 }
 
 }  // namespace dt

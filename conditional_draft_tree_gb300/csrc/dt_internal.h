@@ -20,6 +20,7 @@ struct Plan {
   int proj_ksplit;     // K split of the projection GEMM
   int umma;            // search GEMM on tcgen05 (bf16 weights)
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
+  int cluster;         // 0, or the cluster size (= ks) of the search launch
   int num_sms;
   int chain_grid;      // co-resident blocks of the search kernel
   int wave;            // requests per search launch (<= chain_grid)
@@ -33,7 +34,7 @@ struct Plan {
 // Control block at the start of the workspace; zeroed by every call.
 struct Ctrl {
   unsigned int bar_count;  // grid barrier arrivals (monotonic within a launch)
-  unsigned int bar_spare;
+  unsigned int red_next;   // chunk counter of the gh sums (monotonic within a launch)
   int abort;           // set when a bounded wait expired
   int active;          // requests of the current wave still searching
   unsigned int steps;      // lockstep steps of the last search launch
@@ -45,7 +46,8 @@ struct Ctrl {
   // phase; GEMM parts: [9] MMA loop, [10] epilogue, [11] waits for B copies,
   // [12] waits for MMA completion; scoring of block 0's first node: [13] h,
   // [14] candidate loop (incl. block sync), [15] softmax + sort + write;
-  // [16] barrier after the GRU phase
+  // [16] barrier after the GRU phase; cluster sum of the GEMM: [17] barrier
+  // before the stores, [18] stores, [19] barrier after them, [20] sums
   unsigned long long t_ns[24];
   // followed by: unsigned row_ticket[batch * D]; int req_flags[batch]; gemm tickets
 };

@@ -108,7 +108,15 @@ typedef struct {
                          0 = library default. Any value yields the same trees. */
   void **phase_events;/* NULL, or DT_NUM_PHASE_EVENTS cudaEvent_t handles recorded on
                          the stream at phase boundaries (for timing) */
+  int flags;          /* DT_OPT_* bits; 0 = defaults */
 } dt_options;
+
+/* dt_options.flags: sum the K chunks of the search GEMM inside thread-block
+ * clusters, in distributed shared memory, instead of through global memory
+ * (used only when the clusters fit on the GPU at once; measured slower than
+ * the default at the shapes tested). The trees agree with the default path
+ * up to the rounding of a different K split. */
+#define DT_OPT_CLUSTER_SUM 1
 
 #define DT_NUM_PHASE_EVENTS 4 /* start, after top-M, after the projection, after the search */
 

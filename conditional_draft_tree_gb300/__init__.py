@@ -22,12 +22,13 @@ ERR_NONFINITE, ERR_TIMEOUT, ERR_BAD_TEMPERATURE = -4, -5, -6
 F32, BF16 = 0, 1
 NUM_PHASE_EVENTS = 4
 OPT_CLUSTER_SUM = 1          # dt_options.flags: K-chunk sums in distributed shared memory
+OPT_TEST_BARRIER_TIMEOUT = 2  # dt_options.flags: failure-detection test hook
 MAX_SPEC = 16
 
 # every symbol include/dt.h declares
 EXPORTS = ("dt_abi_version", "dt_status_string", "dt_prepared_bytes", "dt_prepare_weights",
            "dt_workspace_bytes", "dt_build_trees", "dt_host_workspace_bytes",
-           "dt_build_trees_host", "dt_select_topm_noalloc")
+           "dt_build_trees_host", "dt_select_topm_noalloc", "dt_kernel_launches")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -76,6 +77,8 @@ def lib():
         L.dt_workspace_bytes.argtypes = [C.POINTER(DtDims), C.POINTER(DtOptions)]
         L.dt_host_workspace_bytes.restype = C.c_size_t
         L.dt_host_workspace_bytes.argtypes = [C.POINTER(DtDims), C.POINTER(DtOptions)]
+        L.dt_kernel_launches.restype = C.c_int
+        L.dt_kernel_launches.argtypes = [C.POINTER(DtDims), C.c_int, C.POINTER(DtOptions)]
         sig = [C.POINTER(DtDims), C.POINTER(DtWeights), C.c_void_p, C.c_void_p, C.c_void_p,
                C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
                C.POINTER(DtTreeOut), C.POINTER(DtOptions), C.c_void_p]
@@ -157,6 +160,11 @@ def prepare_weights(dims: DtDims, w: DeviceWeights, prepared: torch.Tensor, stre
 
 def workspace_bytes(dims: DtDims, opt: DtOptions | None = None) -> int:
     return lib().dt_workspace_bytes(C.byref(dims), C.byref(opt) if opt else None)
+
+
+def kernel_launches(dims: DtDims, wdtype: int, opt: DtOptions | None = None) -> int:
+    """Kernels one build_trees call launches (see dt_kernel_launches)."""
+    return lib().dt_kernel_launches(C.byref(dims), int(wdtype), C.byref(opt) if opt else None)
 
 
 def host_workspace_bytes(dims: DtDims, opt: DtOptions | None = None) -> int:

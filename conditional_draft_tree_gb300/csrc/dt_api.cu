@@ -7,6 +7,7 @@
 // (Componenti Core 1, 4, 5). Nothing here allocates device memory.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -66,6 +67,7 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   if (rc) return rc;
   const dt_dims &d = *dims;
   p->spec = (opt && opt->spec_width > 0) ? opt->spec_width : 8;
+  p->test_timeout = (opt && (opt->flags & DT_OPT_TEST_BARRIER_TIMEOUT)) ? 1 : 0;
 
   // top-M segments: at most 64K elements per block, enough blocks to fill the GPU
   const long long rows = static_cast<long long>(d.batch) * d.D;
@@ -252,6 +254,34 @@ int record(const dt_options *opt, int i, cudaStream_t st) {
 }
 
 // The round on device buffers; `plan` is already made.
+// One library-owned non-blocking stream per device for the work that runs
+// beside the caller's stream; created on first use, kept for the process.
+cudaStream_t side_stream() {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+    streams[dev] = nullptr;
+  return streams[dev];
+}
+
+// fork/join events of one call (released when the call returns; the driver
+// frees them once the recorded work has completed)
+struct Events {
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ok = false;
+  Events() {
+    ok = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess;
+  }
+  ~Events() {
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+  }
+};
+
 int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const float *base_logits,
               const float *H, const float *state0, const int32_t *anchor_tok,
               const float *temperature, void *ws, const dt_tree_out *out, const dt_options *opt,
@@ -262,14 +292,24 @@ int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const f
   char *wsb = static_cast<char *>(ws);
   if (cudaMemsetAsync(wsb + pl.off_ctrl, 0, pl.off_part - pl.off_ctrl, st) != cudaSuccess)
     return DT_ERR_CUDA;
-  if (dt::launch_topm(pl, base_logits, ws, out->topm, st) != cudaSuccess) return DT_ERR_CUDA;
-  rc = record(opt, 1, st);
-  if (rc) return rc;
+  // the projection (compute bound) runs on a side stream beside the top-M
+  // selection (HBM bound); the two touch disjoint workspace regions
+  cudaStream_t side = side_stream();
+  if (!side) return DT_ERR_CUDA;
+  Events ev;
+  if (!ev.ok) return DT_ERR_CUDA;
+  if (cudaEventRecord(ev.fork, st) != cudaSuccess || cudaStreamWaitEvent(side, ev.fork, 0) != cudaSuccess)
+    return DT_ERR_CUDA;
   float *U = reinterpret_cast<float *>(wsb + pl.off_U);
   if (dt::launch_gemm_nt(d.batch * d.D, d.r, d.d, H, DT_F32, d.d, w->W1, w->wdtype,
                          static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r, pl.proj_ksplit,
-                         reinterpret_cast<float *>(wsb + pl.off_upart), st) != cudaSuccess)
+                         reinterpret_cast<float *>(wsb + pl.off_upart), side) != cudaSuccess)
     return DT_ERR_CUDA;
+  if (cudaEventRecord(ev.join, side) != cudaSuccess) return DT_ERR_CUDA;
+  if (dt::launch_topm(pl, base_logits, ws, out->topm, st) != cudaSuccess) return DT_ERR_CUDA;
+  rc = record(opt, 1, st);
+  if (rc) return rc;
+  if (cudaStreamWaitEvent(st, ev.join, 0) != cudaSuccess) return DT_ERR_CUDA;
   rc = record(opt, 2, st);
   if (rc) return rc;
   dt::ChainArgs a;
@@ -362,6 +402,14 @@ size_t dt_workspace_bytes(const dt_dims *dims, const dt_options *opt) {
   Plan pf;
   if (dt::make_plan(dims, DT_F32, opt, &pf)) return 0;
   return pl.off_end > pf.off_end ? pl.off_end : pf.off_end;
+}
+
+int dt_kernel_launches(const dt_dims *dims, int wdtype, const dt_options *opt) {
+  Plan pl;
+  if (!dims || (wdtype != DT_F32 && wdtype != DT_BF16)) return 0;
+  if (dt::make_plan(dims, wdtype, opt, &pl)) return 0;
+  const int waves = (dims->batch + pl.wave - 1) / pl.wave;
+  return 2 + (pl.proj_ksplit > 1 ? 1 : 0) + waves;
 }
 
 int dt_build_trees(const dt_dims *dims, const dt_weights *w, const void *prepared,

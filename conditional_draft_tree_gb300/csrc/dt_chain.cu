@@ -92,6 +92,7 @@ struct ChainParams {
   uint8_t *mask;
   int32_t *status;
   unsigned long long limit_ns;
+  int test_skip;       // failure-detection test: the last block skips its first arrival
   // dynamic shared memory carve-up (byte offsets)
   int sm_child_score, sm_child_tok, sm_child_exp, sm_exp_depth, sm_exp_parent, sm_exp_score,
       sm_exp_tok, sm_run_e, sm_run_head, sm_run_pos, sm_vhead, sm_par, sm_scratch, sm_total;
@@ -1328,7 +1329,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
   if (tail) tail_init(p, t, ts, b);
   unsigned bar_target = 0, red_base = 0;
   bool ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
-                         false);
+                         false, p.test_skip && blockIdx.x == gridDim.x - 1);
   // block 0 accounts its time per phase (for profiling; a few timer reads a step)
   const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
   uint64_t t_prev = clock_me ? global_ns() : 0;
@@ -1505,7 +1506,8 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
                                                sizeof(unsigned) * static_cast<size_t>(d.batch) * d.D);
   cp.tokens = a.out->tokens; cp.parents = a.out->parents; cp.depths = a.out->depths;
   cp.scores = a.out->scores; cp.mask = a.out->mask; cp.status = a.out->status;
-  cp.limit_ns = 10000000000ull;  // 10 s per grid barrier wait
+  cp.limit_ns = pl.test_timeout ? 2000000ull : 10000000000ull;  // per bounded wait
+  cp.test_skip = pl.test_timeout;
   const void *fn = chain_kernel_ptr(pl.wdtype, d.M);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(pl.chain_smem));

@@ -111,8 +111,10 @@ __device__ __forceinline__ void red_release_add_u32(unsigned *p, unsigned v) {
 // (`target`, advanced by every call, wrap-safe). A block that failed locally
 // (`fail`) raises *abort and does not arrive; a wait longer than `limit_ns`, or
 // one that sees *abort, returns false. Never traps or spins forever.
+// `skip_arrival` (failure-detection tests only) waits without arriving.
 __device__ __forceinline__ bool grid_barrier(unsigned *count, int *abort, unsigned nblocks,
-                                             uint64_t limit_ns, unsigned &target, bool fail) {
+                                             uint64_t limit_ns, unsigned &target, bool fail,
+                                             bool skip_arrival = false) {
   __shared__ int s_ok;
   target += nblocks;
   __syncthreads();
@@ -122,7 +124,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned *count, int *abort, unsign
       atomicExch(abort, 1);
       ok = 0;
     } else {
-      red_release_add_u32(count, 1u);
+      if (!skip_arrival) red_release_add_u32(count, 1u);
       uint64_t t0 = 0;
       for (unsigned spins = 0;; ++spins) {
         if (static_cast<int>(ld_acquire_u32(count) - target) >= 0) break;

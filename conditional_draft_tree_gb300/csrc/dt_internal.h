@@ -21,6 +21,7 @@ struct Plan {
   int umma;            // search GEMM on tcgen05 (bf16 weights)
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
   int cluster;         // 0, or the cluster size (= ks) of the search launch
+  int test_timeout;    // DT_OPT_TEST_BARRIER_TIMEOUT
   int num_sms;
   int chain_grid;      // co-resident blocks of the search kernel
   int wave;            // requests per search launch (<= chain_grid)

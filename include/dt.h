@@ -118,6 +118,13 @@ typedef struct {
  * up to the rounding of a different K split. */
 #define DT_OPT_CLUSTER_SUM 1
 
+/* dt_options.flags, test hook for failure detection: in the search launch the
+ * last block skips its first grid-barrier arrival and every barrier wait is
+ * limited to 2 ms, so the other blocks' bounded waits run out. Every request
+ * then reports DT_ERR_TIMEOUT with empty rows; no fault, and the context stays
+ * usable. */
+#define DT_OPT_TEST_BARRIER_TIMEOUT 2
+
 #define DT_NUM_PHASE_EVENTS 4 /* start, after top-M, after the projection, after the search */
 
 /* Bytes of the prepared-weights buffer for `dims`: the GRU input projection of
@@ -134,6 +141,13 @@ int dt_prepare_weights(const dt_dims *dims, const dt_weights *w, void *prepared,
 
 /* Scratch bytes dt_build_trees needs for `dims` and `opt` (may be NULL). */
 size_t dt_workspace_bytes(const dt_dims *dims, const dt_options *opt);
+
+/* Kernel launches one dt_build_trees call makes for `dims`, weight type
+ * `wdtype` (DT_F32 / DT_BF16) and `opt` (may be NULL): top-M, projection (plus
+ * its split-K sum when K is split), one search launch per wave of requests.
+ * Memsets and event records are not counted. Returns 0 for invalid dims.
+ * Host only; needs the device for its SM count. */
+int dt_kernel_launches(const dt_dims *dims, int wdtype, const dt_options *opt);
 
 /* Build one round of draft trees for dims->batch requests.
  *   base_logits [batch][D][V] fp32  base logits L_base^j of depths j = 1..D

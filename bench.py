@@ -268,7 +268,7 @@ def main():
     clocks = clk.stop()
     ctrl = tb.workspace[:32].view(torch.int32).cpu().tolist()   # search counters of the last round
     search_steps, search_expansions = ctrl[4], ctrl[5]
-    t_ns = tb.workspace[32:32 + 8 * 24].view(torch.int64).cpu().tolist()
+    t_ns = tb.workspace[32:32 + 8 * 32].view(torch.int64).cpu().tolist()
     search_split_us = dict(zip(["gemm", "barrier1", "score_reduce", "barrier2", "tail",
                                 "barrier3", "tail_children", "tail_pop_select", "gru",
                                 "gemm_mma", "gemm_epilogue", "gemm_wait_copies", "gemm_wait_mma",
@@ -276,6 +276,8 @@ def main():
                                 "barrier4", "csum_sync1", "csum_send", "csum_sync2",
                                 "csum_add"],
                                [x / 1000.0 for x in t_ns]))
+    gemm_cycles = dict(zip(["wait_free_buffer", "wait_landed_copy", "copy_issue", "mma_issue"],
+                           t_ns[24:28]))
     per = [ph[i][0].elapsed_time(ph[i][3]) for i in range(K)]
     topm_ms = [ph[i][0].elapsed_time(ph[i][1]) for i in range(K)]
     proj_ms = [ph[i][1].elapsed_time(ph[i][2]) for i in range(K)]
@@ -326,6 +328,7 @@ def main():
                        "phases_ms": phases, "expansions_per_round": cnt["expansions"],
                        "search_steps": search_steps, "search_expansions": search_expansions,
                        "search_block0_us": search_split_us,
+                       "search_block0_gemm_issuer_cycles": gemm_cycles,
                        "roofline_topm": roof_topm,
                        "round_algorithmic_bytes": round_bytes,
                        "round_hbm_frac": round_bytes / (total_ms / K * 1e-3) / 1e9 / pk["hbm_gbs"],

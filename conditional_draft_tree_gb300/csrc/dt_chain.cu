@@ -83,6 +83,7 @@ struct ChainParams {
   // shared memory; the input columns arrive as three bf16 terms per state
   int umma, n_mt, ks, kc, cols_cap;
   int cluster;         // 0, or the cluster size (= ks): K chunks summed in distributed shared memory
+  int mcast;           // 1: CTA pairs (two M tiles, one K chunk) share each B slice by multicast
   float *partial;      // [ks][cols_cap][R] per-K-chunk partial products, by slot
   uint16_t *gin16;     // B operand in tile layout (bcol_index)
   Ctrl *ctrl;
@@ -305,11 +306,24 @@ __device__ void gemm_phase(const ChainParams &p, unsigned char *smem) {
 
 constexpr uint32_t kTmemCols = 256;   // fp32 accumulator columns per block
 
+// (M tile, K chunk) of GEMM block g: consecutive blocks share the M tile, or,
+// with multicast pairs, a cluster of two blocks shares the K chunk.
+__device__ __forceinline__ void gemm_tile(const ChainParams &p, int g, int &mt, int &kz) {
+  if (p.mcast) {
+    const int q = g >> 1;
+    kz = q % p.ks;
+    mt = 2 * (q / p.ks) + (g & 1);
+  } else {
+    mt = g / p.ks;
+    kz = g % p.ks;
+  }
+}
+
 // Rows [mt*128, mt*128+128) of [W_hh; W1_S] and K columns [kz*kc, kz*kc+kc) as
 // bf16 into the A tile (zero beyond R rows or d_s columns). Once per launch.
 __device__ void load_a_tile(const ChainParams &p, unsigned char *sA) {
-  const int g = blockIdx.x;
-  const int mt = g / p.ks, kz = g % p.ks;
+  int mt, kz;
+  gemm_tile(p, blockIdx.x, mt, kz);
   const int R = 3 * p.d_s + p.r, k0 = kz * p.kc;
   const int kg = p.kc / 8;
   for (int i = threadIdx.x; i < 128 * kg; i += kThreads) {
@@ -467,11 +481,14 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
                                 UmmaState &u) {
   __shared__ int s_hi[16];           // per pass: last active column + 1
   __shared__ uint32_t s_mask[16][8]; // per pass: active columns
+  __shared__ int s_fail;              // a bounded wait of an issuing thread ran out
   int *slots = reinterpret_cast<int *>(scratch);
-  const int total = compact_slots(p, slots);
+  if (threadIdx.x == 0) s_fail = 0;
+  const int total = compact_slots(p, slots);   // (synchronises the block)
   if (total == 0 || blockIdx.x >= p.n_mt * p.ks) return true;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int mt = blockIdx.x / p.ks, kz = blockIdx.x % p.ks;
+  int mt, kz;
+  gemm_tile(p, blockIdx.x, mt, kz);
   const int R = 3 * p.d_s + p.r;
   const int n_pass = (p.cols_cap + 255) >> 8;
   if (threadIdx.x < 16 * 9) {
@@ -496,52 +513,80 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
     const int hi = s_hi[pass];
     if (hi == 0) continue;
     const uint64_t t0 = clock_me ? global_ns() : 0;
+    const int npad = (hi + 15) & ~15;
+    const uint32_t g0 = u.next;
     if (threadIdx.x == 0) {
-      const int npad = (hi + 15) & ~15;
-      const uint32_t bytes = static_cast<uint32_t>(npad) * 32;
-      const uint32_t idesc = umma_idesc_bf16(128, npad);
+      // producer: one bulk copy per K slice (the three term tiles are adjacent
+      // in global memory; the last is needed up to npad columns only); with
+      // multicast pairs each CTA copies half of it into both CTAs
+      const uint32_t bytes = 2 * kTermBytes + static_cast<uint32_t>(npad) * 32;
+      const uint32_t part = p.mcast ? bytes / 2 : bytes;
+      const uint32_t my_off = p.mcast ? (blockIdx.x & 1) * part : 0;
       const unsigned char *src = reinterpret_cast<const unsigned char *>(p.gin16) +
                                  static_cast<size_t>(pass * p.ks + kz) * nkb * kSliceBytes;
-      const uint32_t g0 = u.next;
       fence_async_global();   // columns written before the grid barrier -> bulk reads
-      fence_async_smem();     // earlier generic use of the stage buffers -> bulk writes
-      auto issue = [&](int s) {
-        const uint32_t g = g0 + s, buf = g % kBufs;
-        // the buffer's previous slice must be consumed by its MMAs
-        if (g >= kBufs) ok &= mbar_wait(&empty[buf], ((g / kBufs) - 1) & 1u, p.limit_ns);
-        mbar_expect_tx(&full[buf], 3 * bytes);
-#pragma unroll
-        for (int sp = 0; sp < 3; ++sp)
-          bulk_g2s(sB + buf * kSliceBytes + sp * kTermBytes,
-                   src + static_cast<size_t>(s) * kSliceBytes + sp * kTermBytes, bytes,
-                   &full[buf]);
-      };
-      for (int s = 0; s < kBufs && s < nkb; ++s) issue(s);
-      uint64_t t_wait = 0;
+      fence_async_smem();     // earlier generic use of the buffers -> bulk writes
+      long long c_empty = 0, c_copy = 0;
       for (int s = 0; s < nkb; ++s) {
         const uint32_t g = g0 + s, buf = g % kBufs;
-        const uint64_t tw = clock_me ? global_ns() : 0;
-        ok &= mbar_wait(&full[buf], (g / kBufs) & 1u, p.limit_ns);
-        if (clock_me) t_wait += global_ns() - tw;
+        // the buffer's previous slice must be consumed by its MMAs (both CTAs'
+        // with multicast: each commit arrives on both empty barriers)
+        const long long c0 = clock64();
+        if (g >= kBufs && !mbar_wait(&empty[buf], ((g / kBufs) - 1) & 1u, p.limit_ns)) {
+          s_fail = 1;
+          break;
+        }
+        const long long c1 = clock64();
+        mbar_expect_tx(&full[buf], bytes);
+        unsigned char *dst = sB + buf * kSliceBytes + my_off;
+        const unsigned char *from = src + static_cast<size_t>(s) * kSliceBytes + my_off;
+        if (p.mcast) bulk_g2s_multicast(dst, from, part, &full[buf], 0x3);
+        else bulk_g2s(dst, from, part, &full[buf]);
+        c_empty += c1 - c0;
+        c_copy += clock64() - c1;
+      }
+      if (clock_me) {
+        p.ctrl->t_ns[24] += c_empty;
+        p.ctrl->t_ns[26] += c_copy;
+      }
+    } else if (threadIdx.x == 32) {
+      // MMA issuer: three MMAs (hi, mid, lo terms) per K slice into one TMEM
+      // accumulator, each slice's buffer released by a commit
+      const uint32_t idesc = umma_idesc_bf16(128, npad);
+      const uint32_t a0 = smem_u32(sA), b_base = smem_u32(sB);
+      long long c_full = 0, c_mma = 0;
+      int s = 0;
+      for (; s < nkb; ++s) {
+        const uint32_t g = g0 + s, buf = g % kBufs;
+        const long long cf = clock64();
+        if (!mbar_wait(&full[buf], (g / kBufs) & 1u, p.limit_ns)) {
+          s_fail = 1;
+          break;
+        }
+        const long long cm = clock64();
         tmem_fence_after();
-        const uint64_t ad = umma_desc(smem_u32(sA) + s * 256, 128, 16u * p.kc);
-        const uint32_t b0 = smem_u32(sB + buf * kSliceBytes);
+        const uint64_t ad = umma_desc(a0 + s * 256, 128, 16u * p.kc);
+        const uint32_t b0 = b_base + buf * kSliceBytes;
 #pragma unroll
         for (int sp = 0; sp < 3; ++sp)
           umma_bf16(u.tmem, ad, umma_desc(b0 + sp * kTermBytes, 128, 256), idesc, s > 0 || sp > 0);
-        umma_commit(&empty[buf]);
-        // refill the buffer of the previous slice (its MMAs were issued one slice ago)
-        if (s >= 1 && s + kBufs - 1 < nkb) issue(s + kBufs - 1);
+        if (p.mcast) umma_commit_multicast(&empty[buf], 0x3);
+        else umma_commit(&empty[buf]);
+        c_full += cm - cf;
+        c_mma += clock64() - cm;
       }
-      u.next = g0 + nkb;
-      const uint32_t last = u.next - 1;
-      const uint64_t tm = clock_me ? global_ns() : 0;
-      ok &= mbar_wait(&empty[last % kBufs], (last / kBufs) & 1u, p.limit_ns);
-      if (clock_me) {
-        p.ctrl->t_ns[11] += t_wait;
+      const uint64_t tm = global_ns();
+      if (s > 0) {   // commits complete in order: the last one covers every MMA
+        const uint32_t last = g0 + s - 1;
+        if (!mbar_wait(&empty[last % kBufs], (last / kBufs) & 1u, p.limit_ns)) s_fail = 1;
+      }
+      if (blockIdx.x == 0) {
         p.ctrl->t_ns[12] += global_ns() - tm;
+        p.ctrl->t_ns[25] += c_full;
+        p.ctrl->t_ns[27] += c_mma;
       }
     }
+    u.next = g0 + nkb;
     tmem_fence_before();
     __syncthreads();
     tmem_fence_after();
@@ -580,7 +625,8 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
     __syncthreads();
     if (clock_me) p.ctrl->t_ns[10] += global_ns() - t1;
   }
-  return ok;
+  __syncthreads();
+  return ok && s_fail == 0;
 }
 
 // Sum of the K-chunk partials (fixed order) + b_hh into gh_store, for the
@@ -1302,7 +1348,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + p.sm_tmem);
     if (threadIdx.x == 0) {
-      for (int i = 0; i < 2 * kBufs; ++i) mbar_init(&mbar[i], 1);
+      for (int i = 0; i < kBufs; ++i) mbar_init(&mbar[i], 1);                  // full
+      for (int i = kBufs; i < 2 * kBufs; ++i) mbar_init(&mbar[i], p.mcast ? 2u : 1u);  // empty
       if (p.cluster) mbar_init(&mbar[2 * kBufs], static_cast<uint32_t>(p.cluster));
     }
     load_a_tile(p, smem + p.sm_A);
@@ -1325,7 +1372,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     fence_async_global();
   }
   // every CTA's cluster barrier is initialised before any CTA arrives on it
-  if (p.cluster) cluster_sync_all();
+  if (p.cluster || p.mcast) cluster_sync_all();
   if (tail) tail_init(p, t, ts, b);
   unsigned bar_target = 0, red_base = 0;
   bool ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
@@ -1401,7 +1448,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     if ((threadIdx.x >> 5) == 0) tmem_dealloc(u.tmem, kTmemCols);
   }
   // no CTA leaves while another CTA of its cluster may still address its memory
-  if (p.cluster) cluster_sync_all();
+  if (p.cluster || p.mcast) cluster_sync_all();
 }
 
 }  // namespace
@@ -1490,6 +1537,7 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.pbuf = reinterpret_cast<float *>(w + pl.off_p);
   cp.colexp = reinterpret_cast<int *>(w + pl.off_colexp);
   cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc; cp.cluster = pl.cluster;
+  cp.mcast = pl.mcast;
   cp.cols_cap = pl.wave * pl.spec;
   cp.partial = pl.umma ? reinterpret_cast<float *>(w + pl.off_partial) : nullptr;
   cp.gin16 = pl.umma ? reinterpret_cast<uint16_t *>(w + pl.off_gin16) : nullptr;
@@ -1515,7 +1563,8 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   // the barrier counters of the control block are re-zeroed for every wave
   e = cudaMemsetAsync(cp.ctrl, 0, sizeof(Ctrl), st);
   if (e != cudaSuccess) return e;
-  if (!pl.cluster) {
+  const int cdim = pl.cluster ? pl.cluster : (pl.mcast ? 2 : 0);
+  if (!cdim) {
     void *args[] = {&cp};
     return cudaLaunchCooperativeKernel(fn, dim3(pl.chain_grid), dim3(kThreads), args,
                                        pl.chain_smem, st);
@@ -1524,7 +1573,7 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = static_cast<unsigned>(pl.cluster);
+  at[0].val.clusterDim.x = static_cast<unsigned>(cdim);
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   at[1].id = cudaLaunchAttributeCooperative;

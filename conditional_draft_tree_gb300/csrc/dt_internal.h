@@ -22,6 +22,7 @@ struct Plan {
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
   int cluster;         // 0, or the cluster size (= ks) of the search launch
   int test_timeout;    // DT_OPT_TEST_BARRIER_TIMEOUT
+  int mcast;           // search GEMM in CTA pairs sharing B by multicast (n_mt even)
   int num_sms;
   int chain_grid;      // co-resident blocks of the search kernel
   int wave;            // requests per search launch (<= chain_grid)
@@ -48,8 +49,10 @@ struct Ctrl {
   // [12] waits for MMA completion; scoring of block 0's first node: [13] h,
   // [14] candidate loop (incl. block sync), [15] softmax + sort + write;
   // [16] barrier after the GRU phase; cluster sum of the GEMM: [17] barrier
-  // before the stores, [18] stores, [19] barrier after them, [20] sums
-  unsigned long long t_ns[24];
+  // before the stores, [18] stores, [19] barrier after them, [20] sums;
+  // GEMM issuing thread, in SM cycles: [24] waits for free buffers, [25] waits
+  // for landed copies, [26] copy issue, [27] MMA issue
+  unsigned long long t_ns[32];
   // followed by: unsigned row_ticket[batch * D]; int req_flags[batch]; gemm tickets
 };
 

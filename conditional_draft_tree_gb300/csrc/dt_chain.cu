@@ -71,12 +71,10 @@ struct ChainParams {
   const float *cand_val;
   const float *U;
   float *S_store, *gh_store, *gin, *pbuf;
-  int *colexp, *col_count;
-  // per GEMM column (slot): depth of the children and score of the expanded
-  // node (written with the selection); its k children once scored
-  int *col_dep;
-  float *col_score;
-  int *col_tok, *col_par;   // GRU input token and parent expansion (-1: state0) per slot
+  int *col_count;
+  // per GEMM column (slot): its record (written with the selection, see
+  // col_record) and its k children once scored
+  int4 *col_rec;
   float *kid_score;
   int32_t *kid_tok;
   // tensor-core GEMM path (bf16 weights): A tiles of 128 rows x kc K stay in
@@ -169,15 +167,36 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t v[SLOTS], int lane) {
 
 // ---------------------------------------------------------------- GEMM phase
 
-// Active GEMM columns in (request, rank) order: slot ids written to `slots`,
-// count returned. nb <= 256 requests per wave: one thread per request, then a
-// block-wide exclusive scan.
-__device__ int compact_slots(const ChainParams &p, int *slots) {
+// Record of one GEMM column: the expansion e it computes (kState0: the state0
+// column of the first step), its parent expansion (-1: the root, whose input
+// state is state0), the depth of its children, its token (the GRU input) and
+// its path score. One 16-byte word so that a column's facts arrive together.
+__device__ __forceinline__ int4 col_record(int e, int parent, int child_depth, int tok,
+                                           float score) {
+  return make_int4(e, (parent + 1) | (child_depth << 16), tok, __float_as_int(score));
+}
+__device__ __forceinline__ int rec_parent(const int4 &r) { return (r.y & 0xffff) - 1; }
+__device__ __forceinline__ int rec_child_depth(const int4 &r) {
+  return static_cast<int>(static_cast<unsigned>(r.y) >> 16);
+}
+
+// Active GEMM columns in (request, rank) order: slot ids written to `slots` and
+// (when `recs` is given) their records, count returned. nb <= 256 requests per
+// wave: one thread per request reads its count and, in the same round trip,
+// the records of all its P slots; then a block-wide exclusive scan.
+__device__ int compact_slots(const ChainParams &p, int *slots, int4 *recs = nullptr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ int s_warp_sum[kWarps];
   __shared__ int s_total;
   const int b_me = threadIdx.x;
-  const int c_me = (b_me < p.nb) ? __ldcg(p.col_count + b_me) : 0;
+  const bool mine = b_me < p.nb;
+  const int c_me = mine ? __ldcg(p.col_count + b_me) : 0;
+  int4 r8[8];
+  if (recs) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      r8[i] = (mine && i < p.P) ? __ldcg(p.col_rec + b_me * p.P + i) : make_int4(0, 0, 0, 0);
+  }
   int incl = c_me;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -189,7 +208,14 @@ __device__ int compact_slots(const ChainParams &p, int *slots) {
   int base = 0;
   for (int w = 0; w < warp; ++w) base += s_warp_sum[w];
   if (threadIdx.x == kThreads - 1) s_total = base + incl;
-  for (int i = 0; i < c_me; ++i) slots[base + incl - c_me + i] = b_me * p.P + i;
+  const int first = base + incl - c_me;
+  for (int i = 0; i < c_me; ++i) slots[first + i] = b_me * p.P + i;
+  if (recs) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < c_me) recs[first + i] = r8[i];
+    for (int i = 8; i < c_me; ++i) recs[first + i] = __ldcg(p.col_rec + b_me * p.P + i);
+  }
   __syncthreads();
   return s_total;
 }
@@ -285,7 +311,7 @@ __device__ void gemm_phase(const ChainParams &p, unsigned char *smem) {
         if (row < R && c < ncol) {
           const int slot = slots[c0 + c];
           const int b = slot / p.P;
-          const int e = __ldcg(p.colexp + slot);
+          const int e = __ldcg(p.col_rec + slot).x;
           if (row < 3 * ds) {
             const int e_slot = (e == kState0) ? p.e_cap : e;
             float *dst = p.gh_store + (static_cast<size_t>(b) * (p.e_cap + 1) + e_slot) * 3 * ds + row;
@@ -401,7 +427,7 @@ __device__ bool cluster_reduce(const ChainParams &p, unsigned char *sB, uint64_t
     long long off = -1;
     if (c < hi && ((mask[c >> 5] >> (c & 31)) & 1u)) {
       const int slot = pass * 256 + c;
-      const int e = __ldcg(p.colexp + slot);
+      const int e = __ldcg(p.col_rec + slot).x;
       const int e_slot = (e == kState0) ? p.e_cap : e;
       off = (static_cast<long long>(slot / p.P) * (p.e_cap + 1) + e_slot) * 3 * ds;
     }
@@ -630,13 +656,13 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
 }
 
 // Sum of the K-chunk partials (fixed order) + b_hh into gh_store, for the
-// columns of the last GEMM (`slots`, and `esl` their expansion slots, both
-// taken before the tails reassign the columns). It runs beside the tails: one
+// columns of the last GEMM (`slots` and `recs`, taken before the tails
+// reassign the columns). It runs beside the tails: one
 // column per chunk, chunks handed out by a global counter, so that the blocks
 // without a request start at once and the tails join when they are done. Every
 // block calls this once per step and makes exactly one failing grab, so the
 // counter of the next step starts at base + columns + gridDim.
-__device__ void gh_reduce(const ChainParams &p, const int *slots, const int *esl, int total,
+__device__ void gh_reduce(const ChainParams &p, const int *slots, const int4 *recs, int total,
                           unsigned &base) {
   __shared__ int s_idx;
   const int ds = p.d_s, R = 3 * ds + p.r, n4 = 3 * ds / 4;
@@ -651,7 +677,8 @@ __device__ void gh_reduce(const ChainParams &p, const int *slots, const int *esl
     if (col >= total) break;
     const int slot = slots[col];
     float *dst = p.gh_store +
-                 (static_cast<size_t>(slot / p.P) * (p.e_cap + 1) + esl[col]) * 3 * ds;
+                 (static_cast<size_t>(slot / p.P) * (p.e_cap + 1) +
+                  (recs[col].x == kState0 ? p.e_cap : recs[col].x)) * 3 * ds;
     const float *src = p.partial + static_cast<size_t>(slot) * R;
     for (int i0 = threadIdx.x; i0 < n4; i0 += IT * kThreads) {
       float4 acc[IT];
@@ -823,7 +850,7 @@ __device__ __forceinline__ float gru_unit(float gir, float giz, float gin, float
   return (1.f - z) * n + z * sp;
 }
 
-__device__ void gru_phase(const ChainParams &p, const int *slots, int total) {
+__device__ void gru_phase(const ChainParams &p, const int *slots, const int4 *recs, int total) {
   const int ds = p.d_s, q4 = ds / 4;
   const int items = total * q4;
   const int stride = gridDim.x * kThreads;
@@ -841,9 +868,8 @@ __device__ void gru_phase(const ChainParams &p, const int *slots, int total) {
         u[k] = (i - c * q4) * 4;
         slot[k] = slots[c];
         const int b = slot[k] / p.P;
-        const int e = __ldcg(p.colexp + slot[k]);
-        const int pe = __ldcg(p.col_par + slot[k]);
-        const int tok = __ldcg(p.col_tok + slot[k]);
+        const int4 rec = recs[c];
+        const int e = rec.x, pe = rec_parent(rec), tok = rec.z;
         const size_t ebase = static_cast<size_t>(b) * (p.e_cap + 1);
         const float *g = p.G + static_cast<size_t>(tok) * 3 * ds + u[k];
         const float *ghp = p.gh_store + (ebase + (pe < 0 ? p.e_cap : pe)) * 3 * ds + u[k];
@@ -879,13 +905,14 @@ __device__ void gru_phase(const ChainParams &p, const int *slots, int total) {
 // in fixed order) and the corrected logits L_c = (L_base^j[c] + W2[c,:] h) / T
 // of its share of the M candidates; then one of them takes the log-sum-exp
 // over the M values and the k best (L desc, id asc) as the children, with
-// scores col_score + L_c - lse, and warms L2 with the prepared rows of the two
+// scores score(node) + L_c - lse, and warms L2 with the prepared rows of the two
 // best (the likeliest next expansions).
 constexpr int kWPN = 4;                // warps per node
 constexpr int kNPB = kWarps / kWPN;    // nodes per block and round
 
 template <int WDT, int SLOTS, bool SMALL_R>
-__device__ void score_phase(const ChainParams &p, const int *slots, int total, float *sm) {
+__device__ void score_phase(const ChainParams &p, const int *slots, const int4 *recs, int total,
+                            float *sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int node_in_block = warp / kWPN, wq = warp % kWPN;
   float *Lsm = sm + node_in_block * p.M;
@@ -895,79 +922,71 @@ __device__ void score_phase(const ChainParams &p, const int *slots, int total, f
   const size_t plane = static_cast<size_t>(p.cols_cap) * R;
   const float ninf = -__int_as_float(0x7f800000);
   const int mq = (p.M + kWPN - 1) / kWPN;
+  constexpr int G = WDT == 1 ? 16 : 8;   // candidate rows in flight
   const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
+  const bool psum = p.umma && !p.cluster;   // p still split over K chunks
   for (int n0 = blockIdx.x * kNPB; n0 < total; n0 += gridDim.x * kNPB) {
     const int n = n0 + node_in_block;
-    const int slot = n < total ? slots[n] : 0;
-    const bool live = n < total && __ldcg(p.colexp + slot) >= 0;
+    const bool any = n < total;
+    const int slot = any ? slots[n] : 0;
+    uint64_t t_in = clock_me ? global_ns() : 0;
+    // 1. everything indexed by the column alone, issued together: the
+    //    expansion, the children's depth and this lane's share of p
+    int e = -1, j = 1;
+    float pa[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pa[i] = 0.f;
+    if (any) {
+      e = recs[n].x;
+      j = rec_child_depth(recs[n]);
+      if (SMALL_R && lane < nq) {
+        if (psum) {
+          const float *src = p.partial + static_cast<size_t>(slot) * R + 3 * p.d_s + 8 * lane;
+          for (int z0 = 0; z0 < p.ks; z0 += 4) {
+            float4 v[4][2];
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+              const bool ok = z0 + z < p.ks;
+              const float4 *q = reinterpret_cast<const float4 *>(src + (z0 + z) * plane);
+              v[z][0] = ok ? __ldcg(q) : make_float4(0.f, 0.f, 0.f, 0.f);
+              v[z][1] = ok ? __ldcg(q + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+              pa[0] += v[z][0].x; pa[1] += v[z][0].y; pa[2] += v[z][0].z; pa[3] += v[z][0].w;
+              pa[4] += v[z][1].x; pa[5] += v[z][1].y; pa[6] += v[z][1].z; pa[7] += v[z][1].w;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            pa[i] = ldcg(p.pbuf + static_cast<size_t>(slot) * p.r + 8 * lane + i);
+        }
+      }
+    }
+    const bool live = any && e >= 0;
     const int b = slot / p.P;
-    const int j = live ? __ldcg(p.col_dep + slot) : 1;
     const size_t row = static_cast<size_t>(p.b0 + b) * p.D + (j - 1);
     const int32_t *cid = p.cand_id + row * p.M;
     const float *cval = p.cand_val + row * p.M;
     float T = p.temperature ? p.temperature[p.b0 + b] : 1.0f;
     T = (T == 0.0f) ? 1.0f : T;
-    uint64_t t_in = clock_me ? global_ns() : 0;
+    // the finishing warp's candidate ids, loaded early
+    int fid[SLOTS];
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+      const int c = s * 32 + lane;
+      fid[s] = (live && wq == 0 && c < p.M) ? __ldg(cid + c) : -1;
+    }
     if (live) {
       const float *U = p.U + row * p.r;
-      // h = SiLU(U_j + p): p from the partials (tensor-core path) or pbuf
-      float h[8];
-      if (SMALL_R) {
-        if (lane < nq) {
-          float a[8];
-          if (p.umma && !p.cluster) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] = 0.f;
-            const float *src = p.partial + static_cast<size_t>(slot) * R + 3 * p.d_s + 8 * lane;
-            for (int z0 = 0; z0 < p.ks; z0 += 4) {
-              float4 v[4][2];
-#pragma unroll
-              for (int z = 0; z < 4; ++z) {
-                const bool ok = z0 + z < p.ks;
-                const float4 *q = reinterpret_cast<const float4 *>(src + (z0 + z) * plane);
-                v[z][0] = ok ? __ldcg(q) : make_float4(0.f, 0.f, 0.f, 0.f);
-                v[z][1] = ok ? __ldcg(q + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-              }
-#pragma unroll
-              for (int z = 0; z < 4; ++z) {
-                a[0] += v[z][0].x; a[1] += v[z][0].y; a[2] += v[z][0].z; a[3] += v[z][0].w;
-                a[4] += v[z][1].x; a[5] += v[z][1].y; a[6] += v[z][1].z; a[7] += v[z][1].w;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              a[i] = ldcg(p.pbuf + static_cast<size_t>(slot) * p.r + 8 * lane + i);
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) h[i] = siluf_(__ldg(U + 8 * lane + i) + a[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) h[i] = 0.f;
-        }
-      } else {
-        for (int q = lane; q < p.r; q += 32) {
-          float a = 0.f;
-          if (p.umma && !p.cluster) {
-            for (int z = 0; z < p.ks; ++z)
-              a += ldcg(p.partial + z * plane + static_cast<size_t>(slot) * R + 3 * p.d_s + q);
-          } else {
-            a = ldcg(p.pbuf + static_cast<size_t>(slot) * p.r + q);
-          }
-          hbuf[q] = siluf_(__ldg(U + q) + a);
-        }
-        __syncwarp();
-      }
-      if (clock_me) {
-        volatile float sink = h[0];
-        (void)sink;
-        const uint64_t now = global_ns();
-        p.ctrl->t_ns[13] += now - t_in;
-        t_in = now;
-      }
-      // this warp's candidates [c_beg, c_end), G rows in flight
-      constexpr int G = WDT == 1 ? 16 : 8;
+      // 2. U_j and the first candidate group (ids, base values, W2 rows) before
+      //    h is formed, so that the row gathers overlap the U loads
       const int c_beg = wq * mq, c_end = min(p.M, c_beg + mq);
+      float h[8];
+      float uu[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) uu[i] = (SMALL_R && lane < nq) ? __ldg(U + 8 * lane + i) : 0.f;
       for (int c0 = c_beg; c0 < c_end; c0 += G) {
         const int my_c = c0 + lane;
         const bool mine = lane < G && my_c < c_end;
@@ -989,6 +1008,10 @@ __device__ void score_phase(const ChainParams &p, const int *slots, int total, f
                                static_cast<const uint16_t *>(p.W2) +
                                static_cast<size_t>(ids[g]) * p.r + 8 * lane))
                          : make_uint4(0u, 0u, 0u, 0u);
+          if (c0 == c_beg) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[i] = (lane < nq) ? siluf_(uu[i] + pa[i]) : 0.f;
+          }
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             const uint32_t w4[4] = {raw[g].x, raw[g].y, raw[g].z, raw[g].w};
@@ -1009,11 +1032,29 @@ __device__ void score_phase(const ChainParams &p, const int *slots, int total, f
               for (int i = 0; i < 8; ++i) wf[g][i] = 0.f;
             }
           }
+          if (c0 == c_beg) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[i] = (lane < nq) ? siluf_(uu[i] + pa[i]) : 0.f;
+          }
 #pragma unroll
           for (int g = 0; g < G; ++g)
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[g] = fmaf(wf[g][i], h[i], acc[g]);
         } else {
+          if (c0 == c_beg) {
+            // h in shared memory (r > 256): p summed over the chunks here
+            for (int q = lane; q < p.r; q += 32) {
+              float a = 0.f;
+              if (psum) {
+                for (int z = 0; z < p.ks; ++z)
+                  a += ldcg(p.partial + z * plane + static_cast<size_t>(slot) * R + 3 * p.d_s + q);
+              } else {
+                a = ldcg(p.pbuf + static_cast<size_t>(slot) * p.r + q);
+              }
+              hbuf[q] = siluf_(__ldg(U + q) + a);
+            }
+            __syncwarp();
+          }
 #pragma unroll 1
           for (int q = lane; q - lane < nq; q += 32) {
             if (q < nq) {
@@ -1031,6 +1072,11 @@ __device__ void score_phase(const ChainParams &p, const int *slots, int total, f
               }
             }
           }
+        }
+        if (clock_me && c0 == c_beg) {
+          const uint64_t now = global_ns();
+          p.ctrl->t_ns[13] += now - t_in;
+          t_in = now;
         }
         float my_dl = 0.f;
 #pragma unroll
@@ -1056,12 +1102,9 @@ __device__ void score_phase(const ChainParams &p, const int *slots, int total, f
         const int c = s * 32 + lane;
         key[s] = 0ull;
         Lv[s] = ninf;
-        if (c < p.M) {
-          const int id = __ldg(cid + c);
-          if (id >= 0) {
-            Lv[s] = Lsm[c];
-            key[s] = make_key(Lv[s], static_cast<uint32_t>(id));
-          }
+        if (c < p.M && fid[s] >= 0) {
+          Lv[s] = Lsm[c];
+          key[s] = make_key(Lv[s], static_cast<uint32_t>(fid[s]));
         }
         mx = fmaxf(mx, Lv[s]);
       }
@@ -1073,7 +1116,7 @@ __device__ void score_phase(const ChainParams &p, const int *slots, int total, f
       sum = warp_sum(sum);
       const float lse = (mx == ninf) ? ninf : mx + logf(sum);
       warp_sort_desc<SLOTS>(key, lane);
-      const float base_score = __ldcg(p.col_score + slot);
+      const float base_score = __int_as_float(recs[n].w);
 #pragma unroll
       for (int s = 0; s < SLOTS; ++s) {
         const int i = s * 32 + lane;
@@ -1206,9 +1249,8 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
       t.exp_score[e] = t.child_score[slot_c];
       t.exp_tok[e] = t.child_tok[slot_c];
       ts.sel_e[nsel] = e;
-      p.colexp[b * p.P + nsel] = e;
-      p.col_dep[b * p.P + nsel] = dep + 1;   // the children's depth
-      p.col_score[b * p.P + nsel] = t.child_score[slot_c];
+      p.col_rec[b * p.P + nsel] =
+          col_record(e, er, dep + 1, t.child_tok[slot_c], t.child_score[slot_c]);
     }
     if (lane == (r & 31)) {
       t.vhead[r] = static_cast<uint8_t>(h + 1);
@@ -1255,7 +1297,7 @@ __device__ void tail_init(const ChainParams &p, const Tables &t, TailState &ts, 
   for (int u = threadIdx.x; u < p.d_s; u += kThreads) write_column(p, b * p.P, u, s0[u]);
   if (p.umma) fence_async_global();
   if (threadIdx.x == 0) {
-    p.colexp[b * p.P] = kState0;
+    p.col_rec[b * p.P] = col_record(kState0, -1, 0, 0, 0.0f);
     p.col_count[b] = 1;
     atomicAdd(&p.ctrl->active, 1);
   }
@@ -1282,16 +1324,12 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
     // the root: S_0 = GRU(state0, E[anchor]); its recurrent half came from the state0 column
     const int anchor = p.anchor[p.b0 + b];
     if (threadIdx.x == 0) {
-      p.col_tok[b * p.P] = anchor;
-      p.col_par[b * p.P] = -1;
       t.exp_depth[0] = 0; t.exp_parent[0] = -1; t.exp_score[0] = 0.0f; t.exp_tok[0] = anchor;
       ts.e_count = 1;
       ts.n_sel = 1;
       atomicAdd(&p.ctrl->expansions, 1u);
       ts.sel_e[0] = 0;
-      p.colexp[b * p.P] = 0;
-      p.col_dep[b * p.P] = 1;
-      p.col_score[b * p.P] = 0.0f;
+      p.col_rec[b * p.P] = col_record(0, -1, 1, anchor, 0.0f);
       p.col_count[b] = 1;
     }
     __syncthreads();
@@ -1321,13 +1359,6 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
   __syncthreads();
   if (clock_me) { const uint64_t n = global_ns(); p.ctrl->t_ns[7] += n - t0; t0 = n; }
   if (ts.done == 2) { finalize(p, t, ts, b, true); return; }
-  // 3. the GRU jobs of the chosen nodes (run grid-wide next)
-  if (threadIdx.x < ts.n_sel) {
-    const int i = threadIdx.x, e = ts.sel_e[i];
-    p.col_tok[b * p.P + i] = t.exp_tok[e];
-    p.col_par[b * p.P + i] = t.exp_parent[e];
-  }
-  __syncthreads();
 }
 
 template <int WDT, int SLOTS>
@@ -1401,16 +1432,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     // columns and their expansion slots are kept for the gh sums of the tail
     // phase, since the tails reassign the columns
     int *slots = reinterpret_cast<int *>(smem + p.sm_scratch);
-    int *esl = slots + p.cols_cap;
-    const int total = compact_slots(p, slots);
-    for (int c = threadIdx.x; c < total; c += kThreads) {
-      const int e = __ldcg(p.colexp + slots[c]);
-      esl[c] = (e == kState0) ? p.e_cap : e;
-    }
+    int4 *recs = reinterpret_cast<int4 *>(smem + p.sm_scratch + ((p.cols_cap * 4 + 15) & ~15));
+    const int total = compact_slots(p, slots, recs);
     {
-      float *sc = reinterpret_cast<float *>(smem + p.sm_scratch + ((2 * p.cols_cap * 4 + 15) & ~15));
-      if (p.r <= 256) score_phase<WDT, SLOTS, true>(p, slots, total, sc);
-      else score_phase<WDT, SLOTS, false>(p, slots, total, sc);
+      float *sc = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(recs) +
+                                            static_cast<size_t>(p.cols_cap) * 16);
+      if (p.r <= 256) score_phase<WDT, SLOTS, true>(p, slots, recs, total, sc);
+      else score_phase<WDT, SLOTS, false>(p, slots, recs, total, sc);
     }
     lap(2);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
@@ -1418,7 +1446,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     lap(3);
     if (!ok) break;
     if (tail && !ts.done) tail_step<WDT, SLOTS>(p, t, ts, b);
-    if (p.umma && !p.cluster) gh_reduce(p, slots, esl, total, red_base);
+    if (p.umma && !p.cluster) gh_reduce(p, slots, recs, total, red_base);
     lap(4);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
                       false);
@@ -1428,8 +1456,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     __syncthreads();
     if (s_active == 0) break;
     {
-      int *slots = reinterpret_cast<int *>(smem + p.sm_scratch);
-      gru_phase(p, slots, compact_slots(p, slots));
+      int *gslots = reinterpret_cast<int *>(smem + p.sm_scratch);
+      int4 *grecs = reinterpret_cast<int4 *>(smem + p.sm_scratch + ((p.cols_cap * 4 + 15) & ~15));
+      const int gtotal = compact_slots(p, gslots, grecs);
+      gru_phase(p, gslots, grecs, gtotal);
     }
     lap(8);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
@@ -1480,10 +1510,10 @@ static int chain_smem_layout(const Plan &pl, int e_cap, int wave, ChainParams *c
     cp->sm_mbar = off = al(off, 16);  off += 16 * kBufs + 8;
     cp->sm_tmem = off;                off += 16;
   }
-  cp->sm_scratch = off;
+  cp->sm_scratch = off = al(off, 16);   // holds int4 column records
   const int gemm_scratch = al(wave * pl.spec * 4, 16) + (pl.umma ? 0 : kGemmCols * kGemmKC * 4);
-  const int score_scratch =
-      al(2 * wave * pl.spec * 4, 16) + kNPB * d.M * 4 + (d.r > 256 ? kWarps * d.r * 4 : 0);
+  const int score_scratch = al(wave * pl.spec * 4, 16) + wave * pl.spec * 16 + kNPB * d.M * 4 +
+                            (d.r > 256 ? kWarps * d.r * 4 : 0);
   off += gemm_scratch > score_scratch ? gemm_scratch : score_scratch;
   cp->sm_total = off;
   return off;
@@ -1535,17 +1565,13 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.gh_store = reinterpret_cast<float *>(w + pl.off_gh);
   cp.gin = reinterpret_cast<float *>(w + pl.off_gin);
   cp.pbuf = reinterpret_cast<float *>(w + pl.off_p);
-  cp.colexp = reinterpret_cast<int *>(w + pl.off_colexp);
+  cp.col_rec = reinterpret_cast<int4 *>(w + pl.off_colinfo);
   cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc; cp.cluster = pl.cluster;
   cp.mcast = pl.mcast;
   cp.cols_cap = pl.wave * pl.spec;
   cp.partial = pl.umma ? reinterpret_cast<float *>(w + pl.off_partial) : nullptr;
   cp.gin16 = pl.umma ? reinterpret_cast<uint16_t *>(w + pl.off_gin16) : nullptr;
-  cp.col_count = cp.colexp + static_cast<size_t>(pl.wave) * pl.spec;
-  cp.col_dep = reinterpret_cast<int *>(w + pl.off_colinfo);
-  cp.col_score = reinterpret_cast<float *>(cp.col_dep + static_cast<size_t>(pl.wave) * pl.spec);
-  cp.col_tok = reinterpret_cast<int *>(cp.col_score + static_cast<size_t>(pl.wave) * pl.spec);
-  cp.col_par = cp.col_tok + static_cast<size_t>(pl.wave) * pl.spec;
+  cp.col_count = reinterpret_cast<int *>(w + pl.off_colexp);
   cp.kid_score = reinterpret_cast<float *>(w + pl.off_kids);
   cp.kid_tok = reinterpret_cast<int32_t *>(cp.kid_score +
                                            static_cast<size_t>(pl.wave) * pl.spec * d.k);

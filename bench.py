@@ -276,8 +276,9 @@ def main():
                                 "barrier4", "csum_sync1", "csum_send", "csum_sync2",
                                 "csum_add"],
                                [x / 1000.0 for x in t_ns]))
-    gemm_cycles = dict(zip(["wait_free_buffer", "wait_landed_copy", "copy_issue", "mma_issue"],
-                           t_ns[24:28]))
+    gemm_cycles = dict(zip(["wait_free_buffer", "wait_landed_copy", "copy_issue", "mma_issue",
+                            "pop_iterations", "pop_cycles", "select_iterations",
+                            "select_cycles"], t_ns[24:32]))
     per = [ph[i][0].elapsed_time(ph[i][3]) for i in range(K)]
     topm_ms = [ph[i][0].elapsed_time(ph[i][1]) for i in range(K)]
     proj_ms = [ph[i][1].elapsed_time(ph[i][2]) for i in range(K)]

@@ -1179,9 +1179,13 @@ __device__ void finalize(const ChainParams &p, const Tables &t, TailState &ts, i
 __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailState &ts, int b,
                                   int lane) {
   int count = ts.count, n_runs = ts.n_runs;
+  const bool clock_me = blockIdx.x == 0 && lane == 0;
+  long long c_start = clock64();
+  int it_pop = 0;
   LaneBest lb = lane_scan(t.run_hs, n_runs, lane);
   bool done = false;
   while (true) {
+    ++it_pop;
     if (count >= p.N) { done = true; break; }
     const int r = warp_best(lb);
     if (r < 0) { done = true; break; }
@@ -1213,6 +1217,12 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
     count = pos;
     __syncwarp();
   }
+  if (clock_me) {
+    const long long c = clock64();
+    p.ctrl->t_ns[28] += it_pop;
+    p.ctrl->t_ns[29] += c - c_start;
+    c_start = c;
+  }
   if (done) {
     if (lane == 0) {
       ts.count = count; ts.n_runs = n_runs; ts.n_sel = 0; ts.done = 2;
@@ -1231,7 +1241,9 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
   __syncwarp();
   int nsel = 0, nspec = 0, i = 0;
   const int e_count = ts.e_count;
+  int it_sel = 0;
   while (nsel < p.P) {
+    ++it_sel;
     const int r = warp_best(lb);
     if (r < 0) break;
     ++i;
@@ -1263,6 +1275,10 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
     }
     __syncwarp();
   }
+  if (clock_me) {
+    p.ctrl->t_ns[30] += it_sel;
+    p.ctrl->t_ns[31] += clock64() - c_start;
+  }
   if (lane == 0) {
     ts.count = count;
     ts.n_runs = n_runs;
@@ -1275,6 +1291,219 @@ __device__ void replay_and_select(const ChainParams &p, const Tables &t, TailSta
   __syncwarp();
 }
 
+
+// The same replay and selection with the run state in registers: run r lives
+// in slot r / 32 of lane r % 32 as two packed words and its head score:
+//   w1 = head h (6 bits) | expansion er (12 bits) << 6 | output row of its parent (11 bits) << 18
+//   w2 = depth of its entries (8 bits) | (expansion of the head + 1) << 8
+// so a pop needs two shuffles from the owning lane and no shared-memory lookup,
+// and only the owner of the popped run (and of a new run) reads the next head's
+// score and expansion. The output rows and the chosen expansions are logged in
+// registers (pop i and choice i by lane i % 32) and written after the loops.
+// Used while the runs fit (N + 1 <= 32 RS); the run state is loaded from and
+// stored back to the shared tables.
+template <int RS>
+__device__ __forceinline__ uint32_t pick_slot(const uint32_t (&v)[RS], int s) {
+  uint32_t x = v[0];
+#pragma unroll
+  for (int i = 1; i < RS; ++i) x = (s == i) ? v[i] : x;
+  return x;
+}
+
+template <int RS>
+__device__ __forceinline__ LaneBest lane_best_reg(const float (&hs)[RS], int n_runs, int lane) {
+  LaneBest lb{0u, -1};
+#pragma unroll
+  for (int s = 0; s < RS; ++s) {
+    const int r = s * 32 + lane;
+    if (r < n_runs) {
+      const uint32_t k = hs_key(hs[s]);
+      if (k > lb.key) { lb.key = k; lb.run = r; }
+    }
+  }
+  return lb;
+}
+
+__device__ __forceinline__ uint32_t run_w1(int h, int er, int pos) {
+  return static_cast<uint32_t>(h) | (static_cast<uint32_t>(er) << 6) |
+         (static_cast<uint32_t>(pos) << 18);
+}
+__device__ __forceinline__ uint32_t run_w2(int dep, int ce) {
+  return static_cast<uint32_t>(dep) | (static_cast<uint32_t>(ce + 1) << 8);
+}
+// expansion of entry h of expansion er's children (-1: not expanded; -2: past the end)
+__device__ __forceinline__ int head_exp(const ChainParams &p, const Tables &t, int er, int h) {
+  return h < p.k ? t.child_exp[er * p.k + h] : -2;
+}
+
+template <int RS>
+__device__ void replay_and_select_reg(const ChainParams &p, const Tables &t, TailState &ts, int b,
+                                      int lane) {
+  int count = ts.count, n_runs = ts.n_runs;
+  const int count0 = count;
+  const bool clock_me = blockIdx.x == 0 && lane == 0;
+  long long c_start = clock64();
+  int it_pop = 0;
+  uint32_t w1[RS], w2[RS], plog[RS];
+  float rh[RS];
+#pragma unroll
+  for (int s = 0; s < RS; ++s) {
+    const int r = s * 32 + lane;
+    plog[s] = 0u;
+    if (r < n_runs) {
+      const int h = t.run_head[r], er = t.run_e[r];
+      w1[s] = run_w1(h, er, t.run_pos[r]);
+      w2[s] = run_w2(t.exp_depth[er] + 1, head_exp(p, t, er, h));
+      rh[s] = t.run_hs[r];
+    } else {
+      w1[s] = 0u;
+      w2[s] = 0u;
+      rh[s] = __int_as_float(0x7fc00000);
+    }
+  }
+  LaneBest lb = lane_best_reg<RS>(rh, n_runs, lane);
+  bool done = false;
+  while (true) {
+    ++it_pop;
+    if (count >= p.N) { done = true; break; }
+    const int r = warp_best(lb);
+    if (r < 0) { done = true; break; }
+    const int sl = r >> 5, own = r & 31;
+    const uint32_t a = __shfl_sync(kFull, pick_slot<RS>(w1, sl), own);
+    const uint32_t c = __shfl_sync(kFull, pick_slot<RS>(w2, sl), own);
+    const int h = a & 63, er = (a >> 6) & 4095;
+    const int dep = c & 255, ce = static_cast<int>(c >> 8) - 1, pos = count + 1;
+    const bool need = dep < p.D && pos < p.N;
+    if (need && ce < 0) break;  // stall: this node's children are not known yet
+    const int i = pos - count0 - 1;   // pop index within this step
+    if (lane == (i & 31)) {
+#pragma unroll
+      for (int s = 0; s < RS; ++s)
+        if (s == (i >> 5)) plog[s] = a;
+    }
+    if (lane == own) {
+      const float nh = head_score(p, t, er, h + 1);
+      const int nce = head_exp(p, t, er, h + 1);
+#pragma unroll
+      for (int s = 0; s < RS; ++s)
+        if (s == sl) { w1[s] = a + 1u; w2[s] = run_w2(dep, nce); rh[s] = nh; }
+      lb = lane_best_reg<RS>(rh, n_runs, lane);
+    }
+    if (need && lane == (n_runs & 31)) {
+      const float hs0 = head_score(p, t, ce, 0);
+      const int ce0 = head_exp(p, t, ce, 0);
+      const int s2 = n_runs >> 5;
+#pragma unroll
+      for (int s = 0; s < RS; ++s)
+        if (s == s2) { w1[s] = run_w1(0, ce, pos); w2[s] = run_w2(dep + 1, ce0); rh[s] = hs0; }
+      const uint32_t k0 = hs_key(hs0);
+      if (k0 > lb.key) { lb.key = k0; lb.run = n_runs; }
+    }
+    n_runs += need ? 1 : 0;
+    count = pos;
+  }
+  // the popped rows (pop i logged by lane i % 32), then the run state back to
+  // the shared tables (it persists across steps)
+  const int n_pop = count - count0;
+#pragma unroll
+  for (int s = 0; s < RS; ++s) {
+    const int i = s * 32 + lane;
+    if (i < n_pop) {
+      const uint32_t a = plog[s];
+      const int h = a & 63, er = (a >> 6) & 4095, rpos = static_cast<int>(a >> 18);
+      const int pos = count0 + 1 + i;
+      write_row(p, b, pos, t.child_tok[er * p.k + h], rpos, t.exp_depth[er] + 1,
+                t.child_score[er * p.k + h]);
+      t.par[pos] = static_cast<int16_t>(rpos);
+    }
+    const int r = s * 32 + lane;
+    if (r < n_runs) {
+      t.run_head[r] = static_cast<uint8_t>(w1[s] & 63);
+      t.run_e[r] = static_cast<int16_t>((w1[s] >> 6) & 4095);
+      t.run_pos[r] = static_cast<int16_t>(w1[s] >> 18);
+      t.run_hs[r] = rh[s];
+    }
+  }
+  __syncwarp();
+  if (clock_me) {
+    const long long cc = clock64();
+    p.ctrl->t_ns[28] += it_pop;
+    p.ctrl->t_ns[29] += cc - c_start;
+    c_start = cc;
+  }
+  if (done) {
+    if (lane == 0) {
+      ts.count = count; ts.n_runs = n_runs; ts.n_sel = 0; ts.done = 2;
+      p.col_count[b] = 0;
+    }
+    __syncwarp();
+    return;
+  }
+  // choose the stalled node plus up to P-1 of the next frontier nodes in order,
+  // walking the register copy of the run heads (the real state is stored)
+  const int spec_left = p.e_cap - p.N - ts.spec_used;
+  int nsel = 0, nspec = 0, vi = 0;
+  const int e_count = ts.e_count;
+  int it_sel = 0;
+  uint32_t my_pick = 0xffffffffu;   // choice `lane`: entry (er, h), depth
+  while (nsel < p.P) {
+    ++it_sel;
+    const int r = warp_best(lb);
+    if (r < 0) break;
+    ++vi;
+    if (count + vi >= p.N) break;
+    const int sl = r >> 5, own = r & 31;
+    const uint32_t a = __shfl_sync(kFull, pick_slot<RS>(w1, sl), own);
+    const uint32_t c = __shfl_sync(kFull, pick_slot<RS>(w2, sl), own);
+    const int h = a & 63, er = (a >> 6) & 4095;
+    const int dep = c & 255, ce = static_cast<int>(c >> 8) - 1;
+    const bool fresh = dep < p.D && ce == -1;
+    const bool take = fresh && (nsel == 0 || nspec < spec_left);
+    if (take && lane == nsel) my_pick = (a & 0x3ffffu) | (static_cast<uint32_t>(dep) << 18);
+    if (lane == own) {
+      const float nh = head_score(p, t, er, h + 1);
+      const int nce = head_exp(p, t, er, h + 1);
+#pragma unroll
+      for (int s = 0; s < RS; ++s)
+        if (s == sl) { w1[s] = a + 1u; w2[s] = run_w2(dep, nce); rh[s] = nh; }
+      lb = lane_best_reg<RS>(rh, n_runs, lane);
+    }
+    if (take) {
+      nspec += (nsel > 0) ? 1 : 0;
+      ++nsel;
+    }
+  }
+  // the chosen expansions (choice i by lane i)
+  if (lane < nsel) {
+    const int h = my_pick & 63, er = (my_pick >> 6) & 4095, dep = my_pick >> 18;
+    const int slot_c = er * p.k + h;
+    const int e = e_count + lane;
+    const float sc = t.child_score[slot_c];
+    const int tok = t.child_tok[slot_c];
+    t.child_exp[slot_c] = static_cast<int16_t>(e);
+    t.exp_depth[e] = static_cast<int8_t>(dep);
+    t.exp_parent[e] = static_cast<int16_t>(er);
+    t.exp_score[e] = sc;
+    t.exp_tok[e] = tok;
+    ts.sel_e[lane] = e;
+    p.col_rec[b * p.P + lane] = col_record(e, er, dep + 1, tok, sc);
+  }
+  __syncwarp();
+  if (clock_me) {
+    p.ctrl->t_ns[30] += it_sel;
+    p.ctrl->t_ns[31] += clock64() - c_start;
+  }
+  if (lane == 0) {
+    ts.count = count;
+    ts.n_runs = n_runs;
+    ts.e_count = e_count + nsel;
+    ts.n_sel = nsel;
+    ts.spec_used += nspec;
+    p.col_count[b] = nsel;
+    atomicAdd(&p.ctrl->expansions, static_cast<unsigned>(nsel));
+  }
+  __syncwarp();
+}
 
 __device__ void tail_init(const ChainParams &p, const Tables &t, TailState &ts, int b) {
   if (threadIdx.x == 0) {
@@ -1355,7 +1584,10 @@ __device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, 
   __syncthreads();
   if (clock_me) { const uint64_t n = global_ns(); p.ctrl->t_ns[6] += n - t0; t0 = n; }
   // 2. canonical pops, then the next expansions
-  if (warp == 0) replay_and_select(p, t, ts, b, lane);
+  if (warp == 0) {
+    if (p.N + 1 <= 128) replay_and_select_reg<4>(p, t, ts, b, lane);
+    else replay_and_select(p, t, ts, b, lane);
+  }
   __syncthreads();
   if (clock_me) { const uint64_t n = global_ns(); p.ctrl->t_ns[7] += n - t0; t0 = n; }
   if (ts.done == 2) { finalize(p, t, ts, b, true); return; }

@@ -51,7 +51,9 @@ struct Ctrl {
   // [16] barrier after the GRU phase; cluster sum of the GEMM: [17] barrier
   // before the stores, [18] stores, [19] barrier after them, [20] sums;
   // GEMM issuing thread, in SM cycles: [24] waits for free buffers, [25] waits
-  // for landed copies, [26] copy issue, [27] MMA issue
+  // for landed copies, [26] copy issue, [27] MMA issue; request 0's replay:
+  // [28] pop iterations, [29] their cycles, [30] selection iterations, [31]
+  // their cycles
   unsigned long long t_ns[32];
   // followed by: unsigned row_ticket[batch * D]; int req_flags[batch]; gemm tickets
 };

@@ -78,6 +78,18 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   long long ns = by_size;
   if (by_util > ns) ns = by_util < by_min ? by_util : (by_min > ns ? by_min : ns);
   p->nsplit = static_cast<int>(ns < 1 ? 1 : ns);
+  // rows of a multiple of 4 floats: one wave of blocks (3 per SM) over the
+  // concatenated rows, each streaming a contiguous range (at least 2048 float4)
+  p->topm_blocks = 0;
+  if (d.V % 4 == 0) {
+    const long long units = rows * (d.V / 4);
+    long long nb = 3LL * p->num_sms;
+    if (nb > units / 2048) nb = units / 2048;
+    if (nb >= 1) {
+      p->topm_blocks = static_cast<int>(nb);
+      p->nsplit = static_cast<int>((nb + rows - 1) / rows) + 2;   // pieces of one row, at most
+    }
+  }
 
   // search kernel: expansion slots, shared memory and co-resident grid
   const void *fn = chain_kernel_ptr(wdtype, d.M);

@@ -16,7 +16,8 @@ struct Plan {
   int wdtype;          // DT_F32 / DT_BF16
   int spec;            // speculative expansions per request and step (P)
   int e_cap;           // expansion slots per request
-  int nsplit;          // top-M row segments
+  int nsplit;          // top-M row segments (pieces per row at most, with topm_blocks)
+  int topm_blocks;     // > 0: top-M over contiguous unit ranges, this many blocks
   int proj_ksplit;     // K split of the projection GEMM
   int umma;            // search GEMM on tcgen05 (bf16 weights)
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
@@ -67,6 +68,9 @@ int validate_dims(const dt_dims *dims);
 // top-M over base logits -> candidate ids/values (+ optional user copy)
 cudaError_t launch_topm(const Plan &p, const float *base_logits, void *ws, int32_t *topm_out,
                         cudaStream_t st);
+cudaError_t launch_topm_raw(const float *base_logits, int batch, int D, int V, int M, int nsplit,
+                            int nblk, uint64_t *partial, unsigned *ticket, int *req_flags,
+                            int32_t *cand_id, float *cand_val, int32_t *topm_out, cudaStream_t st);
 
 // C[m][n] = sum_k A[m][k] * B[n][k] (+ bias[n]); fp32 accumulation.
 // a_dtype/b_dtype: DT_F32 or DT_BF16.

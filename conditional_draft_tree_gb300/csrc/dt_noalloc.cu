@@ -27,8 +27,8 @@
 
 namespace dt {
 cudaError_t launch_topm_raw(const float *base_logits, int batch, int D, int V, int M, int nsplit,
-                            uint64_t *partial, unsigned *ticket, int *req_flags, int32_t *cand_id,
-                            float *cand_val, int32_t *topm_out, cudaStream_t st);
+                            int nblk, uint64_t *partial, unsigned *ticket, int *req_flags,
+                            int32_t *cand_id, float *cand_val, int32_t *topm_out, cudaStream_t st);
 }
 
 namespace {
@@ -89,7 +89,18 @@ extern "C" int dt_select_topm_noalloc(const float *base_logits, int batch, int D
     return al(sizeof(unsigned) * rows) + al(sizeof(int) * batch) + al(sizeof(float) * rows * M) +
            al(part);
   };
-  while (ns > 1 && need(ns) > DT_NOALLOC_SCRATCH_BYTES) --ns;
+  // rows of a multiple of 4 floats: the contiguous-range launch of
+  // dt_build_trees (one wave of blocks; at most ns pieces of a row)
+  long long nblk = 0;
+  if (V % 4 == 0) {
+    const long long units = rows * (V / 4);
+    nblk = 3LL * sms;
+    if (nblk > units / 2048) nblk = units / 2048;
+    if (nblk >= 1) ns = (nblk + rows - 1) / rows + 2;
+    if (nblk >= 1 && need(ns) > DT_NOALLOC_SCRATCH_BYTES) nblk = 0;
+    if (nblk < 1) nblk = 0;
+  }
+  while (nblk == 0 && ns > 1 && need(ns) > DT_NOALLOC_SCRATCH_BYTES) --ns;
   if (need(ns) > DT_NOALLOC_SCRATCH_BYTES) return DT_ERR_INVALID_ARG;  // beyond the static scratch
   unsigned char *base = nullptr;
   int rc = scratch_address(&base);
@@ -105,7 +116,8 @@ extern "C" int dt_select_topm_noalloc(const float *base_logits, int batch, int D
   if (cudaMemsetAsync(base, 0, al(sizeof(unsigned) * rows) + al(sizeof(int) * batch), st) !=
       cudaSuccess)
     return DT_ERR_CUDA;
-  if (dt::launch_topm_raw(base_logits, batch, D, V, M, static_cast<int>(ns), partial, ticket,
+  if (dt::launch_topm_raw(base_logits, batch, D, V, M, static_cast<int>(ns),
+                          static_cast<int>(nblk), partial, ticket,
                           flags, topm, cand_val, nullptr, st) != cudaSuccess)
     return DT_ERR_CUDA;
   flags_to_status<<<(batch + 255) / 256, 256, 0, st>>>(flags, status, batch);

@@ -245,31 +245,21 @@ __device__ void block_merge_lists(uint64_t *lists /* [8][MP] */, int warp, int l
   __syncthreads();
 }
 
+// Top-M keys of float4 units [u0, u1) of a row's aligned part (element
+// a0 + 4u + c), plus the scalar head [0, a0) when `head` and the tail
+// [a0 + 4 nv, V) when `tail`, by all warps of the block. The block's M best
+// keys end in lists[0, M) (sorted, 0 past the end); a NaN or +inf sets
+// kReqFlagNonfinite in *flag.
 template <int SLOTS>
-__global__ void __launch_bounds__(kTopmThreads, 3)
-topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
-            uint64_t *__restrict__ partial, unsigned *__restrict__ ticket,
-            int *__restrict__ req_flags, int32_t *__restrict__ cand_id,
-            float *__restrict__ cand_val, int32_t *__restrict__ topm_out) {
+__device__ void block_topm(const float *rowp, int V, int M, int a0, int nv, int u0, int u1,
+                           bool head, bool tail, uint64_t *lists, uint64_t *bufs,
+                           unsigned long long *s_tau_p, unsigned long long *s_wq, int *flag) {
   constexpr int MP = SLOTS * 32;
-  __shared__ uint64_t lists[kTopmWarps * MP];
-  __shared__ uint64_t bufs[kTopmWarps * kBuf];
-  __shared__ unsigned long long s_tau;
-  __shared__ unsigned long long s_wq[kTopmWarps];
-  __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int row = blockIdx.y, split = blockIdx.x;
-  const size_t row_base = static_cast<size_t>(row) * V;
-  const float *rowp = logits + row_base;
+  unsigned long long &s_tau = *s_tau_p;
   if (threadIdx.x == 0) s_tau = 0ull;
   if (threadIdx.x < kTopmWarps) s_wq[threadIdx.x] = 0ull;
   __syncthreads();
-
-  // vector part [a0, a0 + 4 nv) is 16-byte aligned; scalar head [0, a0), tail
-  const int a0 = min(V, static_cast<int>((4 - (row_base & 3)) & 3));
-  const int nv = (V - a0) >> 2;
-  const int u0 = static_cast<int>(static_cast<long long>(split) * nv / nsplit);
-  const int u1 = static_cast<int>(static_cast<long long>(split + 1) * nv / nsplit);
   const int cnt = u1 - u0;
   const int w0 = u0 + static_cast<int>(static_cast<long long>(warp) * cnt / kTopmWarps);
   const int w1 = u0 + static_cast<int>(static_cast<long long>(warp + 1) * cnt / kTopmWarps);
@@ -373,40 +363,52 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
     if (b2 + kQ * 32 < w1) load_tile(ta, b2 + kQ * 32);
     filter_tile(tb, b2);
   }
-  // scalar head (split 0) and tail (last split), warp 0
+  // scalar head and tail, warp 0
   if (warp == 0) {
-    if (split == 0 && a0 > 0) {
+    if (head && a0 > 0) {
       bool ok = lane < a0;
       st.push(ok ? __ldg(rowp + lane) : 0.f, static_cast<uint32_t>(lane), ok);
     }
     const int t0 = a0 + 4 * nv;
-    if (split == nsplit - 1 && t0 < V) {
+    if (tail && t0 < V) {
       bool ok = t0 + lane < V;
       st.push(ok ? __ldg(rowp + t0 + lane) : 0.f, static_cast<uint32_t>(t0 + lane), ok);
     }
     st.drain();
   }
   st.flush();
-  if (__any_sync(kFull, st.bad) && lane == 0) atomicOr(req_flags + row / D, kReqFlagNonfinite);
+  if (__any_sync(kFull, st.bad) && lane == 0) atomicOr(flag, kReqFlagNonfinite);
 
   st.L.store(lists + warp * MP, lane);
   block_merge_lists<SLOTS>(lists, warp, lane);
+}
 
-  if (nsplit > 1) {
-    // publish this segment's list; the last block of the row merges them all
+// The result of one piece of a row: written directly when the piece is the
+// whole row; otherwise published as list `slot` of the row, and the last of
+// the row's `npieces` pieces to arrive (atomic ticket, no waiting) merges them
+// and writes the row.
+template <int SLOTS>
+__device__ void finish_piece(int row, int slot, int npieces, int M, const float *rowp,
+                             uint64_t *lists, uint64_t *partial, int maxpieces, unsigned *ticket,
+                             int32_t *cand_id, float *cand_val, int32_t *topm_out) {
+  constexpr int MP = SLOTS * 32;
+  __shared__ int s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (npieces > 1) {
     for (int i = threadIdx.x; i < M; i += kTopmThreads)
-      partial[(static_cast<size_t>(row) * nsplit + split) * M + i] = lists[i];
+      partial[(static_cast<size_t>(row) * maxpieces + slot) * M + i] = lists[i];
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(ticket + row, 1u) == static_cast<unsigned>(nsplit - 1));
+    if (threadIdx.x == 0)
+      s_last = (atomicAdd(ticket + row, 1u) == static_cast<unsigned>(npieces - 1));
     __syncthreads();
     if (!s_last) return;
     __threadfence();
     WarpList<SLOTS> acc;
     acc.clear();
-    for (int s = warp; s < nsplit; s += kTopmWarps) {
+    for (int s = warp; s < npieces; s += kTopmWarps) {
       WarpList<SLOTS> b;
-      b.load(partial + (static_cast<size_t>(row) * nsplit + s) * M, M, lane, true);
+      b.load(partial + (static_cast<size_t>(row) * maxpieces + s) * M, M, lane, true);
       acc.merge(b, lane);
     }
     __syncwarp();
@@ -415,14 +417,72 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
     if (threadIdx.x == 0) ticket[row] = 0u;
   }
   for (int i = threadIdx.x; i < M; i += kTopmThreads) {
-    uint64_t k = lists[i];
-    size_t o = static_cast<size_t>(row) * M + i;
+    const uint64_t k = lists[i];
+    const size_t o = static_cast<size_t>(row) * M + i;
     // key 0 only survives when the row holds fewer than M non-NaN values; the
     // request is then flagged non-finite and never searched
-    int32_t id = (k != 0ull) ? static_cast<int32_t>(key_id(k)) : -1;
+    const int32_t id = (k != 0ull) ? static_cast<int32_t>(key_id(k)) : -1;
     cand_id[o] = id;
     cand_val[o] = (id >= 0) ? __ldg(rowp + id) : -__int_as_float(0x7f800000);
     if (topm_out) topm_out[o] = id;
+  }
+  __syncthreads();   // lists are reused by the block's next piece
+}
+
+// Two launch shapes.
+//  * nblk == 0: row blockIdx.y in `maxpieces` equal segments, one per block.
+//  * nblk > 0 (rows of a multiple of 4 floats, 16-byte aligned): the rows'
+//    float4 units, concatenated, in nblk equal contiguous ranges, one per
+//    block; a range covers pieces of one or two rows (rarely more). A block
+//    thus streams about rows / nblk of a row with one threshold, instead of
+//    one segment, and the grid is one wave of resident blocks.
+template <int SLOTS>
+__global__ void __launch_bounds__(kTopmThreads, 3)
+topm_kernel(const float *__restrict__ logits, int V, int D, int M, int maxpieces, int nblk,
+            int rows, uint64_t *__restrict__ partial, unsigned *__restrict__ ticket,
+            int *__restrict__ req_flags, int32_t *__restrict__ cand_id,
+            float *__restrict__ cand_val, int32_t *__restrict__ topm_out) {
+  constexpr int MP = SLOTS * 32;
+  __shared__ uint64_t lists[kTopmWarps * MP];
+  __shared__ uint64_t bufs[kTopmWarps * kBuf];
+  __shared__ unsigned long long s_tau;
+  __shared__ unsigned long long s_wq[kTopmWarps];
+  if (nblk == 0) {
+    const int row = blockIdx.y, split = blockIdx.x;
+    const size_t row_base = static_cast<size_t>(row) * V;
+    const float *rowp = logits + row_base;
+    // vector part [a0, a0 + 4 nv) is 16-byte aligned; scalar head [0, a0), tail
+    const int a0 = min(V, static_cast<int>((4 - (row_base & 3)) & 3));
+    const int nv = (V - a0) >> 2;
+    const int u0 = static_cast<int>(static_cast<long long>(split) * nv / maxpieces);
+    const int u1 = static_cast<int>(static_cast<long long>(split + 1) * nv / maxpieces);
+    block_topm<SLOTS>(rowp, V, M, a0, nv, u0, u1, split == 0, split == maxpieces - 1, lists,
+                      bufs, &s_tau, s_wq, req_flags + row / D);
+    finish_piece<SLOTS>(row, split, maxpieces, M, rowp, lists, partial, maxpieces, ticket,
+                        cand_id, cand_val, topm_out);
+    return;
+  }
+  const int nv = V >> 2;
+  const long long TU = static_cast<long long>(rows) * nv;
+  auto bound = [&](long long b) { return b * TU / nblk; };   // first unit of block b
+  auto block_of = [&](long long x) {                         // block holding unit x
+    long long b = x * nblk / TU;
+    while (b + 1 < nblk && bound(b + 1) <= x) ++b;
+    while (b > 0 && bound(b) > x) --b;
+    return b;
+  };
+  const long long g0 = bound(blockIdx.x), g1 = bound(blockIdx.x + 1);
+  for (long long r = g0 / nv; r * nv < g1; ++r) {
+    const int row = static_cast<int>(r);
+    const long long rb = r * nv;
+    const int u0 = static_cast<int>((g0 > rb ? g0 : rb) - rb);
+    const int u1 = static_cast<int>((g1 < rb + nv ? g1 : rb + nv) - rb);
+    const float *rowp = logits + static_cast<size_t>(row) * V;
+    block_topm<SLOTS>(rowp, V, M, 0, nv, u0, u1, false, false, lists, bufs, &s_tau, s_wq,
+                      req_flags + row / D);
+    const long long fb = block_of(rb), lb = block_of(rb + nv - 1);
+    finish_piece<SLOTS>(row, static_cast<int>(blockIdx.x - fb), static_cast<int>(lb - fb + 1), M,
+                        rowp, lists, partial, maxpieces, ticket, cand_id, cand_val, topm_out);
   }
 }
 
@@ -431,26 +491,31 @@ topm_kernel(const float *__restrict__ logits, int V, int D, int M, int nsplit,
 // The same kernel on explicit scratch pointers (used by the allocation-free
 // entry point, whose scratch is a static device array).
 cudaError_t launch_topm_raw(const float *base_logits, int batch, int D, int V, int M, int nsplit,
-                            uint64_t *partial, unsigned *ticket, int *req_flags, int32_t *cand_id,
-                            float *cand_val, int32_t *topm_out, cudaStream_t st) {
-  dim3 grid(nsplit, batch * D);
+                            int nblk, uint64_t *partial, unsigned *ticket, int *req_flags,
+                            int32_t *cand_id, float *cand_val, int32_t *topm_out, cudaStream_t st) {
+  const int rows = batch * D;
+  dim3 grid = nblk > 0 ? dim3(nblk, 1) : dim3(nsplit, rows);
   const int mp = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   switch (mp) {
     case 32:
-      topm_kernel<1><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, partial, ticket,
-                                                   req_flags, cand_id, cand_val, topm_out);
+      topm_kernel<1><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, nblk, rows,
+                                                   partial, ticket, req_flags, cand_id, cand_val,
+                                                   topm_out);
       break;
     case 64:
-      topm_kernel<2><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, partial, ticket,
-                                                   req_flags, cand_id, cand_val, topm_out);
+      topm_kernel<2><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, nblk, rows,
+                                                   partial, ticket, req_flags, cand_id, cand_val,
+                                                   topm_out);
       break;
     case 128:
-      topm_kernel<4><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, partial, ticket,
-                                                   req_flags, cand_id, cand_val, topm_out);
+      topm_kernel<4><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, nblk, rows,
+                                                   partial, ticket, req_flags, cand_id, cand_val,
+                                                   topm_out);
       break;
     default:
-      topm_kernel<8><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, partial, ticket,
-                                                   req_flags, cand_id, cand_val, topm_out);
+      topm_kernel<8><<<grid, kTopmThreads, 0, st>>>(base_logits, V, D, M, nsplit, nblk, rows,
+                                                   partial, ticket, req_flags, cand_id, cand_val,
+                                                   topm_out);
       break;
   }
   return cudaGetLastError();
@@ -465,24 +530,29 @@ cudaError_t launch_topm(const Plan &p, const float *base_logits, void *ws, int32
   uint64_t *partial = reinterpret_cast<uint64_t *>(w + p.off_part);
   int32_t *cid = reinterpret_cast<int32_t *>(w + p.off_cand_id);
   float *cval = reinterpret_cast<float *>(w + p.off_cand_val);
-  dim3 grid(p.nsplit, d.batch * d.D);
+  const int rows = d.batch * d.D, nblk = p.topm_blocks;
+  dim3 grid = nblk > 0 ? dim3(nblk, 1) : dim3(p.nsplit, rows);
   const int mp = d.M <= 32 ? 32 : d.M <= 64 ? 64 : d.M <= 128 ? 128 : 256;
   switch (mp) {
     case 32:
-      topm_kernel<1><<<grid, kTopmThreads, 0, st>>>(base_logits, d.V, d.D, d.M, p.nsplit, partial,
-                                                   ticket, req_flags, cid, cval, topm_out);
+      topm_kernel<1><<<grid, kTopmThreads, 0, st>>>(base_logits, d.V, d.D, d.M, p.nsplit, nblk,
+                                                   rows, partial, ticket, req_flags, cid, cval,
+                                                   topm_out);
       break;
     case 64:
-      topm_kernel<2><<<grid, kTopmThreads, 0, st>>>(base_logits, d.V, d.D, d.M, p.nsplit, partial,
-                                                   ticket, req_flags, cid, cval, topm_out);
+      topm_kernel<2><<<grid, kTopmThreads, 0, st>>>(base_logits, d.V, d.D, d.M, p.nsplit, nblk,
+                                                   rows, partial, ticket, req_flags, cid, cval,
+                                                   topm_out);
       break;
     case 128:
-      topm_kernel<4><<<grid, kTopmThreads, 0, st>>>(base_logits, d.V, d.D, d.M, p.nsplit, partial,
-                                                   ticket, req_flags, cid, cval, topm_out);
+      topm_kernel<4><<<grid, kTopmThreads, 0, st>>>(base_logits, d.V, d.D, d.M, p.nsplit, nblk,
+                                                   rows, partial, ticket, req_flags, cid, cval,
+                                                   topm_out);
       break;
     default:
-      topm_kernel<8><<<grid, kTopmThreads, 0, st>>>(base_logits, d.V, d.D, d.M, p.nsplit, partial,
-                                                   ticket, req_flags, cid, cval, topm_out);
+      topm_kernel<8><<<grid, kTopmThreads, 0, st>>>(base_logits, d.V, d.D, d.M, p.nsplit, nblk,
+                                                   rows, partial, ticket, req_flags, cid, cval,
+                                                   topm_out);
       break;
   }
   return cudaGetLastError();

@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--spec", type=int, default=0, help="speculative expansions per step (0=default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
+    ap.add_argument("--flags", type=int, default=0,
+                    help="dt_options flags (profiling runs; e.g. 4 = no multicast pairs, whose "
+                         "non-cluster launch is the one profiled under ncu)")
     return ap.parse_args()
 
 
@@ -227,7 +230,7 @@ def main():
     dev = torch.device("cuda", local)
 
     t0 = time.perf_counter()
-    tb = dt.TreeBuilder.from_numpy(wl, spec_width=args.spec, device=dev)
+    tb = dt.TreeBuilder.from_numpy(wl, spec_width=args.spec, device=dev, flags=args.flags)
     torch.cuda.synchronize()
     prep = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     prep[0].record()
@@ -259,7 +262,7 @@ def main():
     wall0 = time.perf_counter()
     for i in range(K):
         flush.fill_(i & 0xff)                       # L2 flush outside the timed interval
-        tb.run(**inp, out=out, opt=dt.options(args.spec, ph[i]))
+        tb.run(**inp, out=out, opt=dt.options(args.spec, ph[i], args.flags))
         ends[i].record(st)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0

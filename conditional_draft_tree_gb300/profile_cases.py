@@ -5,9 +5,11 @@
         480 rows x 151936 fp32, 292 MB) through dt_select_topm_noalloc, whose
         top-M kernel and launch shape are those of dt_build_trees. Only the
         logits and the outputs live on the device.
-    python -m conditional_draft_tree_gb300.profile_cases round [--reps R] [--cfg C]
+    python -m conditional_draft_tree_gb300.profile_cases round [--reps R] [--cfg C] [--flags F]
         R whole dt_build_trees rounds of the workload (weights, prepared table
-        and workspace on the device: about 3.5 GB for the default workload).
+        and workspace on the device: about 3.5 GB for the default workload);
+        F = dt_options flags (4: search GEMM without multicast cluster pairs, the
+        launch to use under ncu).
 
 Each case does one untimed launch first, then R timed ones (CUDA events on the
 current stream, L2 flushed by a 256 MB write before each), and prints one line
@@ -58,9 +60,9 @@ def case_topm(cfg, reps, dev):
           f"mean_us={1000 * ms:.1f} GB/s={gbs:.0f}")
 
 
-def case_round(cfg, reps, dev):
+def case_round(cfg, reps, dev, flags=0):
     wl = W.make_workload(cfg)
-    tb = dt.TreeBuilder.from_numpy(wl, device=dev)
+    tb = dt.TreeBuilder.from_numpy(wl, device=dev, flags=flags)
     inp = tb.inputs_to_device(wl)
     out = dt.alloc_outputs(tb.dims, dev)
     ms = _timed(lambda: tb.run(**inp, out=out), reps, dev)
@@ -73,11 +75,15 @@ def main():
     ap.add_argument("case", choices=["topm", "round"])
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--cfg", type=int, default=3)
+    ap.add_argument("--flags", type=int, default=0)
     args = ap.parse_args()
     dev = torch.device("cuda", 0)
     from conditional_draft_tree_gb300 import build
     build.build()
-    {"topm": case_topm, "round": case_round}[args.case](args.cfg, args.reps, dev)
+    if args.case == "round":
+        case_round(args.cfg, args.reps, dev, args.flags)
+    else:
+        case_topm(args.cfg, args.reps, dev)
 
 
 if __name__ == "__main__":

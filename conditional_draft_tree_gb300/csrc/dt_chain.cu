@@ -504,13 +504,20 @@ __device__ bool cluster_reduce(const ChainParams &p, unsigned char *sB, uint64_t
 // 256. Thread 0 runs the pipeline (bulk copies into kBufs slice buffers, MMAs,
 // commits); all warps read the accumulators back.
 __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsigned char *scratch,
-                                UmmaState &u) {
+                                UmmaState &u, int &total_out) {
   __shared__ int s_hi[16];           // per pass: last active column + 1
   __shared__ uint32_t s_mask[16][8]; // per pass: active columns
   __shared__ int s_fail;              // a bounded wait of an issuing thread ran out
   int *slots = reinterpret_cast<int *>(scratch);
   if (threadIdx.x == 0) s_fail = 0;
   const int total = compact_slots(p, slots);   // (synchronises the block)
+  total_out = total;
+  // the columns' records, for the scoring phase that follows: loaded by warps
+  // 2..7 while the issuing threads run the pipeline
+  int4 *recs = reinterpret_cast<int4 *>(scratch + ((p.cols_cap * 4 + 15) & ~15));
+  if (threadIdx.x >= 64)
+    for (int c = static_cast<int>(threadIdx.x) - 64; c < total; c += kThreads - 64)
+      recs[c] = __ldcg(p.col_rec + slots[c]);
   if (total == 0 || blockIdx.x >= p.n_mt * p.ks) return true;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int mt, kz;
@@ -1653,19 +1660,19 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
   for (int step = 0; ok && step < p.N + 3; ++step) {
     if (clock_me) p.ctrl->steps = static_cast<unsigned>(step + 1);
     bool gemm_ok = true;
-    if (p.umma) gemm_ok = gemm_phase_umma(p, smem, smem + p.sm_scratch, u);
+    int total = 0;
+    if (p.umma) gemm_ok = gemm_phase_umma(p, smem, smem + p.sm_scratch, u, total);
     else gemm_phase<WDT>(p, smem + p.sm_scratch);
     lap(0);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
                       !gemm_ok);
     lap(1);
     if (!ok) break;
-    // children of the new expansions (their p summed by the scorers); the
-    // columns and their expansion slots are kept for the gh sums of the tail
-    // phase, since the tails reassign the columns
+    // children of the new expansions (their p summed by the scorers), for the
+    // columns listed by the GEMM phase (the fp32 GEMM's staging overwrote them)
     int *slots = reinterpret_cast<int *>(smem + p.sm_scratch);
     int4 *recs = reinterpret_cast<int4 *>(smem + p.sm_scratch + ((p.cols_cap * 4 + 15) & ~15));
-    const int total = compact_slots(p, slots, recs);
+    if (!p.umma) total = compact_slots(p, slots, recs);
     {
       float *sc = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(recs) +
                                             static_cast<size_t>(p.cols_cap) * 16);

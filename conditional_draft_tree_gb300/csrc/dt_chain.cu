@@ -504,20 +504,25 @@ __device__ bool cluster_reduce(const ChainParams &p, unsigned char *sB, uint64_t
 // 256. Thread 0 runs the pipeline (bulk copies into kBufs slice buffers, MMAs,
 // commits); all warps read the accumulators back.
 __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsigned char *scratch,
-                                UmmaState &u, int &total_out) {
+                                UmmaState &u, int known_total, int &total_out) {
   __shared__ int s_hi[16];           // per pass: last active column + 1
   __shared__ uint32_t s_mask[16][8]; // per pass: active columns
   __shared__ int s_fail;              // a bounded wait of an issuing thread ran out
   int *slots = reinterpret_cast<int *>(scratch);
   if (threadIdx.x == 0) s_fail = 0;
-  const int total = compact_slots(p, slots);   // (synchronises the block)
+  int total = known_total;
+  if (total < 0) {
+    total = compact_slots(p, slots);   // (synchronises the block)
+    // the columns' records, for the scoring phase that follows: loaded by
+    // warps 2..7 while the issuing threads run the pipeline
+    int4 *recs = reinterpret_cast<int4 *>(scratch + ((p.cols_cap * 4 + 15) & ~15));
+    if (threadIdx.x >= 64)
+      for (int c = static_cast<int>(threadIdx.x) - 64; c < total; c += kThreads - 64)
+        recs[c] = __ldcg(p.col_rec + slots[c]);
+  } else {
+    __syncthreads();   // the GRU phase listed the columns and records already
+  }
   total_out = total;
-  // the columns' records, for the scoring phase that follows: loaded by warps
-  // 2..7 while the issuing threads run the pipeline
-  int4 *recs = reinterpret_cast<int4 *>(scratch + ((p.cols_cap * 4 + 15) & ~15));
-  if (threadIdx.x >= 64)
-    for (int c = static_cast<int>(threadIdx.x) - 64; c < total; c += kThreads - 64)
-      recs[c] = __ldcg(p.col_rec + slots[c]);
   if (total == 0 || blockIdx.x >= p.n_mt * p.ks) return true;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int mt, kz;
@@ -1645,6 +1650,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
   if (p.cluster || p.mcast) cluster_sync_all();
   if (tail) tail_init(p, t, ts, b);
   unsigned bar_target = 0, red_base = 0;
+  int next_total = -1;   // columns of the next GEMM when already listed in shared memory
   bool ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
                          false, p.test_skip && blockIdx.x == gridDim.x - 1);
   // block 0 accounts its time per phase (for profiling; a few timer reads a step)
@@ -1661,7 +1667,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     if (clock_me) p.ctrl->steps = static_cast<unsigned>(step + 1);
     bool gemm_ok = true;
     int total = 0;
-    if (p.umma) gemm_ok = gemm_phase_umma(p, smem, smem + p.sm_scratch, u, total);
+    if (p.umma) gemm_ok = gemm_phase_umma(p, smem, smem + p.sm_scratch, u, next_total, total);
     else gemm_phase<WDT>(p, smem + p.sm_scratch);
     lap(0);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
@@ -1699,6 +1705,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
       int4 *grecs = reinterpret_cast<int4 *>(smem + p.sm_scratch + ((p.cols_cap * 4 + 15) & ~15));
       const int gtotal = compact_slots(p, gslots, grecs);
       gru_phase(p, gslots, grecs, gtotal);
+      next_total = gtotal;   // the next GEMM's columns (col_count does not change before it)
     }
     lap(8);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,

@@ -54,7 +54,7 @@ int validate_dims(const dt_dims *d) {
   return DT_OK;
 }
 
-int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
+int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   int rc = validate_dims(dims);
   if (rc) return rc;
   if (wdtype != DT_F32 && wdtype != DT_BF16) return DT_ERR_INVALID_ARG;
@@ -274,6 +274,49 @@ int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
   const size_t cols256 = (cols + 255) / 256 * 256;
   off = al(off + (p->umma ? sizeof(uint16_t) * cols256 * 3 * p->ks * p->kc : 0));
   p->off_end = off;
+  return DT_OK;
+}
+
+// Plans are pure functions of (device, dims, weight type, options) and cost
+// several occupancy and attribute queries; the last few are kept so that a
+// serving loop calling with the same shape pays for them once.
+int make_plan(const dt_dims *dims, int wdtype, const dt_options *opt, Plan *p) {
+  struct Entry {
+    bool used;
+    int device, wdtype, spec, flags;
+    dt_dims dims;
+    Plan plan;
+  };
+  static std::mutex mu;
+  static Entry cache[8];
+  static int next = 0;
+  const int vrc = validate_dims(dims);   // before any device query
+  if (vrc) return vrc;
+  if (wdtype != DT_F32 && wdtype != DT_BF16) return DT_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DT_ERR_CUDA;
+  const int spec = opt ? opt->spec_width : 0, flags = opt ? opt->flags : 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry &e : cache)
+      if (e.used && e.device == dev && e.wdtype == wdtype && e.spec == spec && e.flags == flags &&
+          std::memcmp(&e.dims, dims, sizeof(dt_dims)) == 0) {
+        *p = e.plan;
+        return DT_OK;
+      }
+  }
+  const int rc = make_plan_uncached(dims, wdtype, opt, p);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry &e = cache[next];
+  next = (next + 1) % 8;
+  e.used = true;
+  e.device = dev;
+  e.wdtype = wdtype;
+  e.spec = spec;
+  e.flags = flags;
+  e.dims = *dims;
+  e.plan = *p;
   return DT_OK;
 }
 

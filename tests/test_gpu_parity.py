@@ -266,3 +266,19 @@ def test_config3_multicast_matches_no_multicast():
     b = run_gpu(wl, builder=dt.TreeBuilder.from_numpy(wl, flags=dt.OPT_NO_MULTICAST))
     for key in ("tokens", "parents", "depths", "scores", "mask", "topm", "status"):
         np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+
+
+# --------------------------------------------- more requests than one wave
+
+def test_batch_beyond_one_wave():
+    """300 requests: the search runs as two waves of launches (at most one block
+    per SM and request per wave); requests of both waves against the oracle."""
+    wl = W.custom_workload(V=3000, d=64, d_s=32, r=24, D=7, M=20, k=4, N=48, batch=300,
+                           wdtype="bf16", seed=31, logits="zipf", zipf=(0.8, 1.6))
+    tb = dt.TreeBuilder.from_numpy(wl)
+    assert dt.kernel_launches(tb.dims, tb.w.wdtype, tb.opt) >= 5   # >= 2 search waves
+    g = run_gpu(wl, builder=tb)
+    for b in range(wl.batch):
+        assert g["status"][b] == 0
+        check_structure(wl, b, g)
+    check_against_oracle(wl, g, [0, 1, 151, 152, 153, 299], max_near_ties=1)

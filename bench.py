@@ -46,8 +46,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--flags", type=int, default=0,
-                    help="dt_options flags (profiling runs; e.g. 4 = no multicast pairs, whose "
-                         "non-cluster launch is the one profiled under ncu)")
+                    help="dt_options flags (e.g. 1 = K-chunk sums in thread-block clusters)")
     return ap.parse_args()
 
 

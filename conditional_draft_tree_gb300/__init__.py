@@ -23,7 +23,6 @@ F32, BF16 = 0, 1
 NUM_PHASE_EVENTS = 4
 OPT_CLUSTER_SUM = 1          # dt_options.flags: K-chunk sums in distributed shared memory
 OPT_TEST_BARRIER_TIMEOUT = 2  # dt_options.flags: failure-detection test hook
-OPT_NO_MULTICAST = 4          # dt_options.flags: search GEMM without multicast pairs
 MAX_SPEC = 16
 
 # every symbol include/dt.h declares

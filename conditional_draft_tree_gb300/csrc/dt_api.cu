@@ -159,51 +159,6 @@ int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, P
       *p = q;
       placed = true;
     }
-    // default: K-chunk partials summed through global memory; the blocks of two
-    // M tiles with the same K chunk form a cluster pair that fetches each B
-    // slice once, by multicast (the tile count is padded to even)
-    const bool allow_mcast = !(opt && (opt->flags & DT_OPT_NO_MULTICAST));
-    if (!placed && allow_mcast) {
-      const int n_mt_e = n_mt + (n_mt & 1);
-      int ks = p->num_sms / n_mt_e;
-      if (ks >= 1) {
-        const int kc = ((d.d_s + ks - 1) / ks + 15) / 16 * 16;
-        ks = (d.d_s + kc - 1) / kc;
-        Plan q = *p;
-        q.umma = 1; q.mcast = 1; q.n_mt = n_mt_e; q.ks = ks; q.kc = kc;
-        int wave = wave0;
-        if (kc <= 512 && fit_smem(&q, wave)) {
-          if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(q.chain_smem)) != cudaSuccess)
-            return DT_ERR_CUDA;
-          cudaLaunchConfig_t cfg = {};
-          cudaLaunchAttribute at[1];
-          at[0].id = cudaLaunchAttributeClusterDimension;
-          at[0].val.clusterDim.x = 2;
-          at[0].val.clusterDim.y = 1;
-          at[0].val.clusterDim.z = 1;
-          cfg.gridDim = dim3(2 * ks * (n_mt_e / 2));
-          cfg.blockDim = dim3(256);
-          cfg.dynamicSmemBytes = q.chain_smem;
-          cfg.attrs = at;
-          cfg.numAttrs = 1;
-          int nclusters = 0;
-          if (cudaOccupancyMaxActiveClusters(&nclusters, fn, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            nclusters = 0;
-          }
-          if (2 * nclusters >= n_mt_e * ks) {
-            q.chain_grid = 2 * nclusters;
-            if (wave > q.chain_grid) wave = q.chain_grid;
-            q.wave = wave;
-            if (fit_smem(&q, wave)) {
-              *p = q;
-              placed = true;
-            }
-          }
-        }
-      }
-    }
     if (!placed) {
       // without clusters: K-chunk partials are summed through global memory
       int ks = p->num_sms / n_mt;

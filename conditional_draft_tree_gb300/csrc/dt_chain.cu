@@ -81,7 +81,6 @@ struct ChainParams {
   // shared memory; the input columns arrive as three bf16 terms per state
   int umma, n_mt, ks, kc, cols_cap;
   int cluster;         // 0, or the cluster size (= ks): K chunks summed in distributed shared memory
-  int mcast;           // 1: CTA pairs (two M tiles, one K chunk) share each B slice by multicast
   float *partial;      // [ks][cols_cap][R] per-K-chunk partial products, by slot
   uint16_t *gin16;     // B operand in tile layout (bcol_index)
   Ctrl *ctrl;
@@ -332,17 +331,10 @@ __device__ void gemm_phase(const ChainParams &p, unsigned char *smem) {
 
 constexpr uint32_t kTmemCols = 256;   // fp32 accumulator columns per block
 
-// (M tile, K chunk) of GEMM block g: consecutive blocks share the M tile, or,
-// with multicast pairs, a cluster of two blocks shares the K chunk.
+// (M tile, K chunk) of GEMM block g: consecutive blocks share the M tile.
 __device__ __forceinline__ void gemm_tile(const ChainParams &p, int g, int &mt, int &kz) {
-  if (p.mcast) {
-    const int q = g >> 1;
-    kz = q % p.ks;
-    mt = 2 * (q / p.ks) + (g & 1);
-  } else {
-    mt = g / p.ks;
-    kz = g % p.ks;
-  }
+  mt = g / p.ks;
+  kz = g % p.ks;
 }
 
 // Rows [mt*128, mt*128+128) of [W_hh; W1_S] and K columns [kz*kc, kz*kc+kc) as
@@ -555,11 +547,8 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
     const uint32_t g0 = u.next;
     if (threadIdx.x == 0) {
       // producer: one bulk copy per K slice (the three term tiles are adjacent
-      // in global memory; the last is needed up to npad columns only); with
-      // multicast pairs each CTA copies half of it into both CTAs
+      // in global memory; the last is needed up to npad columns only)
       const uint32_t bytes = 2 * kTermBytes + static_cast<uint32_t>(npad) * 32;
-      const uint32_t part = p.mcast ? bytes / 2 : bytes;
-      const uint32_t my_off = p.mcast ? (blockIdx.x & 1) * part : 0;
       const unsigned char *src = reinterpret_cast<const unsigned char *>(p.gin16) +
                                  static_cast<size_t>(pass * p.ks + kz) * nkb * kSliceBytes;
       fence_async_global();   // columns written before the grid barrier -> bulk reads
@@ -567,8 +556,7 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
       long long c_empty = 0, c_copy = 0;
       for (int s = 0; s < nkb; ++s) {
         const uint32_t g = g0 + s, buf = g % kBufs;
-        // the buffer's previous slice must be consumed by its MMAs (both CTAs'
-        // with multicast: each commit arrives on both empty barriers)
+        // the buffer's previous slice must be consumed by its MMAs
         const long long c0 = clock64();
         if (g >= kBufs && !mbar_wait(&empty[buf], ((g / kBufs) - 1) & 1u, p.limit_ns)) {
           s_fail = 1;
@@ -576,10 +564,8 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
         }
         const long long c1 = clock64();
         mbar_expect_tx(&full[buf], bytes);
-        unsigned char *dst = sB + buf * kSliceBytes + my_off;
-        const unsigned char *from = src + static_cast<size_t>(s) * kSliceBytes + my_off;
-        if (p.mcast) bulk_g2s_multicast(dst, from, part, &full[buf], 0x3);
-        else bulk_g2s(dst, from, part, &full[buf]);
+        bulk_g2s(sB + buf * kSliceBytes, src + static_cast<size_t>(s) * kSliceBytes, bytes,
+                 &full[buf]);
         c_empty += c1 - c0;
         c_copy += clock64() - c1;
       }
@@ -608,8 +594,7 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
 #pragma unroll
         for (int sp = 0; sp < 3; ++sp)
           umma_bf16(u.tmem, ad, umma_desc(b0 + sp * kTermBytes, 128, 256), idesc, s > 0 || sp > 0);
-        if (p.mcast) umma_commit_multicast(&empty[buf], 0x3);
-        else umma_commit(&empty[buf]);
+        umma_commit(&empty[buf]);
         c_full += cm - cf;
         c_mma += clock64() - cm;
       }
@@ -1623,8 +1608,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + p.sm_tmem);
     if (threadIdx.x == 0) {
-      for (int i = 0; i < kBufs; ++i) mbar_init(&mbar[i], 1);                  // full
-      for (int i = kBufs; i < 2 * kBufs; ++i) mbar_init(&mbar[i], p.mcast ? 2u : 1u);  // empty
+      for (int i = 0; i < 2 * kBufs; ++i) mbar_init(&mbar[i], 1);   // full, empty
       if (p.cluster) mbar_init(&mbar[2 * kBufs], static_cast<uint32_t>(p.cluster));
     }
     load_a_tile(p, smem + p.sm_A);
@@ -1647,7 +1631,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     fence_async_global();
   }
   // every CTA's cluster barrier is initialised before any CTA arrives on it
-  if (p.cluster || p.mcast) cluster_sync_all();
+  if (p.cluster) cluster_sync_all();
   if (tail) tail_init(p, t, ts, b);
   unsigned bar_target = 0, red_base = 0;
   int next_total = -1;   // columns of the next GEMM when already listed in shared memory
@@ -1724,7 +1708,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     if ((threadIdx.x >> 5) == 0) tmem_dealloc(u.tmem, kTmemCols);
   }
   // no CTA leaves while another CTA of its cluster may still address its memory
-  if (p.cluster || p.mcast) cluster_sync_all();
+  if (p.cluster) cluster_sync_all();
 }
 
 }  // namespace
@@ -1813,7 +1797,6 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.pbuf = reinterpret_cast<float *>(w + pl.off_p);
   cp.col_rec = reinterpret_cast<int4 *>(w + pl.off_colinfo);
   cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc; cp.cluster = pl.cluster;
-  cp.mcast = pl.mcast;
   cp.cols_cap = pl.wave * pl.spec;
   cp.partial = pl.umma ? reinterpret_cast<float *>(w + pl.off_partial) : nullptr;
   cp.gin16 = pl.umma ? reinterpret_cast<uint16_t *>(w + pl.off_gin16) : nullptr;
@@ -1835,7 +1818,7 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   // the barrier counters of the control block are re-zeroed for every wave
   e = cudaMemsetAsync(cp.ctrl, 0, sizeof(Ctrl), st);
   if (e != cudaSuccess) return e;
-  const int cdim = pl.cluster ? pl.cluster : (pl.mcast ? 2 : 0);
+  const int cdim = pl.cluster;
   if (!cdim) {
     void *args[] = {&cp};
     return cudaLaunchCooperativeKernel(fn, dim3(pl.chain_grid), dim3(kThreads), args,

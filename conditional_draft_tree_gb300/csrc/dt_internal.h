@@ -23,7 +23,6 @@ struct Plan {
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
   int cluster;         // 0, or the cluster size (= ks) of the search launch
   int test_timeout;    // DT_OPT_TEST_BARRIER_TIMEOUT
-  int mcast;           // search GEMM in CTA pairs sharing B by multicast (n_mt even)
   int num_sms;
   int chain_grid;      // co-resident blocks of the search kernel
   int wave;            // requests per search launch (<= chain_grid)

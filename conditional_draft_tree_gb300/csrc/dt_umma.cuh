@@ -169,26 +169,6 @@ __device__ __forceinline__ void st_cluster_f4(uint32_t caddr, float a, float b, 
                "f"(c), "f"(d)
                : "memory");
 }
-// Bulk copy global -> the same shared-memory offset in every CTA of `mask`
-// (this cluster), completion counted on each destination's mbarrier at the same
-// offset.
-__device__ __forceinline__ void bulk_g2s_multicast(void *smem_dst, const void *gsrc,
-                                                   uint32_t bytes, uint64_t *mbar,
-                                                   uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
-      "l"(gsrc), "r"(bytes), "r"(smem_u32(mbar)), "h"(mask)
-      : "memory");
-}
-// one arrival on the mbarrier at this offset in every CTA of `mask` once every
-// MMA issued so far by this thread is done
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *mbar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(mbar)), "h"(mask)
-      : "memory");
-}
 // one arrival (release, cluster scope) on an mbarrier of another CTA
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)

@@ -8,8 +8,7 @@
     python -m conditional_draft_tree_gb300.profile_cases round [--reps R] [--cfg C] [--flags F]
         R whole dt_build_trees rounds of the workload (weights, prepared table
         and workspace on the device: about 3.5 GB for the default workload);
-        F = dt_options flags (4: search GEMM without multicast cluster pairs, the
-        launch to use under ncu).
+        F = dt_options flags (default 0).
 
 Each case does one untimed launch first, then R timed ones (CUDA events on the
 current stream, L2 flushed by a 256 MB write before each), and prints one line

@@ -125,11 +125,6 @@ typedef struct {
  * usable. */
 #define DT_OPT_TEST_BARRIER_TIMEOUT 2
 
-/* dt_options.flags: by default the search GEMM runs in cluster pairs of blocks
- * (two 128-row weight tiles, one K chunk) that fetch each slice of the node
- * states once and multicast it to both; this flag turns the pairs off (every
- * block fetches its own copy). Same results. */
-#define DT_OPT_NO_MULTICAST 4
 
 #define DT_NUM_PHASE_EVENTS 4 /* start, after top-M, after the projection, after the search */
 

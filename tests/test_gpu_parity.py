@@ -247,27 +247,6 @@ def test_config3_cluster_sum_sampled():
     check_against_oracle(wl, g, [3, 17], max_near_ties=1)
 
 
-# ----------------------------------------- search GEMM without multicast pairs
-
-@pytest.mark.parametrize("name", ["bf16-bias-state0-T", "big-ds", "M256-k32"])
-def test_no_multicast_path(name):
-    """Every GEMM block fetching its own B slices (DT_OPT_NO_MULTICAST) against
-    the oracle; the default pairs share them by multicast."""
-    wl = W.custom_workload(name=name, **SHAPES[name])
-    tb = dt.TreeBuilder.from_numpy(wl, flags=dt.OPT_NO_MULTICAST)
-    g = run_gpu(wl, builder=tb)
-    check_against_oracle(wl, g, list(range(wl.batch)), max_near_ties=1)
-
-
-def test_config3_multicast_matches_no_multicast():
-    """Same K split, same sums: the trees of the two fetch modes are identical."""
-    wl = workload(3)
-    a = run_gpu(wl, builder=dt.TreeBuilder.from_numpy(wl))
-    b = run_gpu(wl, builder=dt.TreeBuilder.from_numpy(wl, flags=dt.OPT_NO_MULTICAST))
-    for key in ("tokens", "parents", "depths", "scores", "mask", "topm", "status"):
-        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
-
-
 # --------------------------------------------- more requests than one wave
 
 def test_batch_beyond_one_wave():

@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--spec", type=int, default=0, help="speculative expansions per step (0=default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
+    ap.add_argument("--no-marginal", action="store_true",
+                    help="skip the marginal-score (W2 = 0 ablation) leg")
     ap.add_argument("--flags", type=int, default=0,
                     help="dt_options flags (e.g. 1 = K-chunk sums in thread-block clusters)")
     return ap.parse_args()
@@ -202,6 +204,39 @@ def e2e_leg(args, tb, wl, dt, np, torch, dist, world, dev, flush, st, K, Wm):
     return e2e_value, h2d, d2h, ok_e2e
 
 
+def marginal_leg(wl, dt, torch, dev, flush, st, K, Wm, inp):
+    """The marginal-score builder (the conditionality ablation) on the same
+    workload and inputs: top-M, then one tree kernel; no weights. Device-timed
+    like the main leg (phase events, L2 flushed before every round)."""
+    mb = dt.MarginalTreeBuilder(dt.dims_of(wl.V, wl.d, wl.d_s, wl.r, wl.D, wl.M, wl.k, wl.N,
+                                           wl.batch), device=dev)
+    out = dt.alloc_outputs(mb.dims, dev)
+    ph = [[torch.cuda.Event(enable_timing=True) for _ in range(dt.NUM_PHASE_EVENTS)]
+          for _ in range(K)]
+    for evs in ph:
+        for e in evs:
+            e.record(st)
+    run = lambda opt=None: mb.run(inp["base_logits"], inp["anchor_tok"], inp["temperature"],
+                                  out=out, opt=opt)
+    for _ in range(Wm):
+        flush.fill_(1)
+        run()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0xff)
+        run(dt.options(0, ph[i], dt.OPT_MARGINAL))
+    torch.cuda.synchronize()
+    per = [ph[i][0].elapsed_time(ph[i][3]) for i in range(K)]
+    topm = [ph[i][0].elapsed_time(ph[i][1]) for i in range(K)]
+    tree = [ph[i][2].elapsed_time(ph[i][3]) for i in range(K)]
+    ms = statistics.mean(per)
+    return {"us_per_round": 1000.0 * ms, "trees_per_s": wl.batch / (ms * 1e-3),
+            "topm_us": 1000.0 * statistics.mean(topm),
+            "tree_kernel_us": 1000.0 * statistics.mean(tree),
+            "kernel_launches_per_round": dt.kernel_launches(mb.dims, dt.F32, mb.opt),
+            "ok": bool((out["status"] == 0).all().item())}
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -298,6 +333,9 @@ def main():
     if not args.no_e2e:
         e2e_value, h2d, d2h, ok_e2e = e2e_leg(args, tb, wl, dt, np, torch, dist, world, dev, flush,
                                                st, K, Wm)
+    marginal = None
+    if not args.no_marginal:
+        marginal = marginal_leg(wl, dt, torch, dev, flush, st, K, Wm, inp)
     if rank == 0:
         o = {k: v.cpu().numpy() for k, v in out.items() if v is not None}
         cnt = algorithmic_counts(wl, o["tokens"], o["depths"])
@@ -333,6 +371,7 @@ def main():
                        "search_block0_us": search_split_us,
                        "search_block0_gemm_issuer_cycles": gemm_cycles,
                        "roofline_topm": roof_topm,
+                       "marginal_mode": marginal,
                        "round_algorithmic_bytes": round_bytes,
                        "round_hbm_frac": round_bytes / (total_ms / K * 1e-3) / 1e9 / pk["hbm_gbs"],
                        "peaks": pk["source"], "wall_s": wall},

@@ -23,6 +23,7 @@ F32, BF16 = 0, 1
 NUM_PHASE_EVENTS = 4
 OPT_CLUSTER_SUM = 1          # dt_options.flags: K-chunk sums in distributed shared memory
 OPT_TEST_BARRIER_TIMEOUT = 2  # dt_options.flags: failure-detection test hook
+OPT_MARGINAL = 8             # dt_options.flags: marginal (path-independent) scores
 MAX_SPEC = 16
 
 # every symbol include/dt.h declares
@@ -193,10 +194,12 @@ def _out_struct(out) -> DtTreeOut:
 
 def build_trees(dims: DtDims, w: DeviceWeights, prepared, base_logits, H, state0, anchor_tok,
                 temperature, workspace, out, opt: DtOptions | None = None, stream=None):
-    """Enqueue one round on device tensors (dt_build_trees)."""
-    ws = w.struct()
+    """Enqueue one round on device tensors (dt_build_trees). With OPT_MARGINAL in
+    ``opt.flags``, ``w``, ``prepared``, ``H`` and ``state0`` may be None."""
+    ws = w.struct() if w is not None else None
     o = _out_struct(out)
-    _check(lib().dt_build_trees(C.byref(dims), C.byref(ws), _ptr(prepared), _ptr(base_logits),
+    _check(lib().dt_build_trees(C.byref(dims), C.byref(ws) if ws else None, _ptr(prepared),
+                                _ptr(base_logits),
                                 _ptr(H), _ptr(state0), _ptr(anchor_tok), _ptr(temperature),
                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 C.byref(o), C.byref(opt) if opt else None, _stream(stream)),
@@ -208,9 +211,9 @@ def build_trees_host(dims: DtDims, w: DeviceWeights, prepared, base_logits, H, s
                      stream=None):
     """Enqueue one round on HOST input/output tensors (dt_build_trees_host). Synchronise
     the stream before reading ``host_out``."""
-    ws = w.struct()
+    ws = w.struct() if w is not None else None
     o = _out_struct(host_out)
-    _check(lib().dt_build_trees_host(C.byref(dims), C.byref(ws), _ptr(prepared),
+    _check(lib().dt_build_trees_host(C.byref(dims), C.byref(ws) if ws else None, _ptr(prepared),
                                      _ptr(base_logits), _ptr(H), _ptr(state0), _ptr(anchor_tok),
                                      _ptr(temperature), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), C.byref(o),
@@ -283,4 +286,38 @@ class TreeBuilder:
         f = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(self.device)
         return dict(base_logits=f(wl.base_logits, np.float32), H=f(wl.H, np.float32),
                     state0=f(wl.state0, np.float32), anchor_tok=f(wl.anchor, np.int32),
+                    temperature=f(wl.temperature, np.float32))
+
+
+class MarginalTreeBuilder:
+    """Workspace for marginal-score trees (OPT_MARGINAL) of one shape: no
+    weights, no GRU state; ``run(base_logits, anchor_tok, temperature)`` builds
+    one round on device tensors. ``dims`` keeps d, d_s and r only for the
+    shape checks of the C ABI (any valid values)."""
+
+    def __init__(self, dims: DtDims, device="cuda", spec_width: int = 0):
+        self.dims = dims
+        self.device = torch.device(device)
+        self.opt = options(spec_width, flags=OPT_MARGINAL)
+        wsb = workspace_bytes(dims, self.opt)
+        if wsb == 0:
+            raise DtError("dt_workspace_bytes failed (invalid dims or unsupported device)")
+        self.workspace = torch.empty(wsb, dtype=torch.uint8, device=self.device)
+
+    @classmethod
+    def from_workload(cls, wl, device="cuda", batch=None):
+        return cls(dims_of(wl.V, wl.d, wl.d_s, wl.r, wl.D, wl.M, wl.k, wl.N,
+                           wl.batch if batch is None else batch), device)
+
+    def run(self, base_logits, anchor_tok, temperature=None, out=None, stream=None, opt=None):
+        if out is None:
+            out = alloc_outputs(self.dims, self.device)
+        build_trees(self.dims, None, None, base_logits, None, None, anchor_tok, temperature,
+                    self.workspace, out, opt or self.opt, stream)
+        return out
+
+    def inputs_to_device(self, wl):
+        import numpy as np
+        f = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(self.device)
+        return dict(base_logits=f(wl.base_logits, np.float32), anchor_tok=f(wl.anchor, np.int32),
                     temperature=f(wl.temperature, np.float32))

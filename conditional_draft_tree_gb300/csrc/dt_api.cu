@@ -68,6 +68,7 @@ int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, P
   const dt_dims &d = *dims;
   p->spec = (opt && opt->spec_width > 0) ? opt->spec_width : 8;
   p->test_timeout = (opt && (opt->flags & DT_OPT_TEST_BARRIER_TIMEOUT)) ? 1 : 0;
+  p->marginal = (opt && (opt->flags & DT_OPT_MARGINAL)) ? 1 : 0;
 
   // top-M segments: at most 64K elements per block, enough blocks to fill the GPU
   const long long rows = static_cast<long long>(d.batch) * d.D;
@@ -91,110 +92,114 @@ int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, P
     }
   }
 
-  // search kernel: expansion slots, shared memory and co-resident grid
-  const void *fn = chain_kernel_ptr(wdtype, d.M);
-  cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return DT_ERR_CUDA;
-  // the opt-in limit covers static + dynamic shared memory of a block
-  const int smem_max = smem_optin - static_cast<int>(fa.sharedSizeBytes);
-  const int wave0 = d.batch < 256 ? (d.batch < p->num_sms ? d.batch : p->num_sms) : 256;
-  // e_cap (expansion slots) and shared memory for the GEMM choice in *p; false
-  // when even the smallest e_cap does not fit
-  auto fit_smem = [&](Plan *q, int wave) {
-    int e_cap = d.N + 1 + (q->spec > 1 ? d.N + 1 : 0);
-    int smem = chain_smem_bytes(*q, e_cap, wave);
-    while (smem > smem_max && e_cap > d.N + 1) {
-      e_cap = d.N + 1 + (e_cap - d.N - 1) / 2;
-      smem = chain_smem_bytes(*q, e_cap, wave);
-    }
-    if (smem > smem_max) return false;
-    q->e_cap = e_cap;
-    q->chain_smem = static_cast<size_t>(smem);
-    return true;
-  };
-  bool placed = false;
-  p->umma = 0;
-  p->cluster = 0;
-  if (wdtype == DT_BF16) {
-    // search GEMM on the tensor cores: 128-row tiles of [W_hh; W1_S] times K
-    // chunks, one (tile, chunk) per block, at most 512 K columns per chunk.
-    // On request (DT_OPT_CLUSTER_SUM) the K chunks of a tile form one
-    // thread-block cluster and sum their partial products in distributed
-    // shared memory; the cluster size is the largest whose clusters all fit on
-    // the GPU at once. By default the partials are summed through global memory.
-    const int R = 3 * d.d_s + d.r;
-    const int n_mt = (R + 127) / 128;
-    const bool allow_cluster = opt && (opt->flags & DT_OPT_CLUSTER_SUM);
-    for (int cs = 8; allow_cluster && cs >= 2 && !placed; --cs) {
-      const int kc = ((d.d_s + cs - 1) / cs + 15) / 16 * 16;
-      if (kc > 512 || (d.d_s + kc - 1) / kc != cs) continue;
-      Plan q = *p;
-      q.umma = 1; q.cluster = cs; q.n_mt = n_mt; q.ks = cs; q.kc = kc;
-      int wave = wave0;
-      if (!fit_smem(&q, wave)) continue;
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(q.chain_smem)) != cudaSuccess)
-        return DT_ERR_CUDA;
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = cs;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3(cs * n_mt);
-      cfg.blockDim = dim3(256);
-      cfg.dynamicSmemBytes = q.chain_smem;
-      cfg.attrs = at;
-      cfg.numAttrs = 1;
-      int nclusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&nclusters, fn, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        continue;
+  // search kernel: expansion slots, shared memory and co-resident grid (the
+  // marginal mode has no search: its workspace ends after the candidates)
+  if (!p->marginal) {
+    const void *fn = chain_kernel_ptr(wdtype, d.M);
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return DT_ERR_CUDA;
+    // the opt-in limit covers static + dynamic shared memory of a block
+    const int smem_max = smem_optin - static_cast<int>(fa.sharedSizeBytes);
+    const int wave0 = d.batch < 256 ? (d.batch < p->num_sms ? d.batch : p->num_sms) : 256;
+    // e_cap (expansion slots) and shared memory for the GEMM choice in *p; false
+    // when even the smallest e_cap does not fit
+    auto fit_smem = [&](Plan *q, int wave) {
+      int e_cap = d.N + 1 + (q->spec > 1 ? d.N + 1 : 0);
+      int smem = chain_smem_bytes(*q, e_cap, wave);
+      while (smem > smem_max && e_cap > d.N + 1) {
+        e_cap = d.N + 1 + (e_cap - d.N - 1) / 2;
+        smem = chain_smem_bytes(*q, e_cap, wave);
       }
-      if (nclusters < n_mt) continue;
-      q.chain_grid = cs * nclusters;
-      if (wave > q.chain_grid) wave = q.chain_grid;
-      q.wave = wave;
-      if (!fit_smem(&q, wave)) continue;
-      *p = q;
-      placed = true;
-    }
-    if (!placed) {
-      // without clusters: K-chunk partials are summed through global memory
-      int ks = p->num_sms / n_mt;
-      if (ks >= 1) {
-        int kc = ((d.d_s + ks - 1) / ks + 15) / 16 * 16;
-        ks = (d.d_s + kc - 1) / kc;
-        if (kc <= 512 && n_mt * ks <= p->num_sms) {
-          p->umma = 1;
-          p->n_mt = n_mt;
-          p->ks = ks;
-          p->kc = kc;
+      if (smem > smem_max) return false;
+      q->e_cap = e_cap;
+      q->chain_smem = static_cast<size_t>(smem);
+      return true;
+    };
+    bool placed = false;
+    p->umma = 0;
+    p->cluster = 0;
+    if (wdtype == DT_BF16) {
+      // search GEMM on the tensor cores: 128-row tiles of [W_hh; W1_S] times K
+      // chunks, one (tile, chunk) per block, at most 512 K columns per chunk.
+      // On request (DT_OPT_CLUSTER_SUM) the K chunks of a tile form one
+      // thread-block cluster and sum their partial products in distributed
+      // shared memory; the cluster size is the largest whose clusters all fit on
+      // the GPU at once. By default the partials are summed through global memory.
+      const int R = 3 * d.d_s + d.r;
+      const int n_mt = (R + 127) / 128;
+      const bool allow_cluster = opt && (opt->flags & DT_OPT_CLUSTER_SUM);
+      for (int cs = 8; allow_cluster && cs >= 2 && !placed; --cs) {
+        const int kc = ((d.d_s + cs - 1) / cs + 15) / 16 * 16;
+        if (kc > 512 || (d.d_s + kc - 1) / kc != cs) continue;
+        Plan q = *p;
+        q.umma = 1; q.cluster = cs; q.n_mt = n_mt; q.ks = cs; q.kc = kc;
+        int wave = wave0;
+        if (!fit_smem(&q, wave)) continue;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(q.chain_smem)) != cudaSuccess)
+          return DT_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = cs;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(cs * n_mt);
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = q.chain_smem;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, fn, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          continue;
+        }
+        if (nclusters < n_mt) continue;
+        q.chain_grid = cs * nclusters;
+        if (wave > q.chain_grid) wave = q.chain_grid;
+        q.wave = wave;
+        if (!fit_smem(&q, wave)) continue;
+        *p = q;
+        placed = true;
+      }
+      if (!placed) {
+        // without clusters: K-chunk partials are summed through global memory
+        int ks = p->num_sms / n_mt;
+        if (ks >= 1) {
+          int kc = ((d.d_s + ks - 1) / ks + 15) / 16 * 16;
+          ks = (d.d_s + kc - 1) / kc;
+          if (kc <= 512 && n_mt * ks <= p->num_sms) {
+            p->umma = 1;
+            p->n_mt = n_mt;
+            p->ks = ks;
+            p->kc = kc;
+          }
         }
       }
     }
-  }
-  if (!placed) {
-    int wave = wave0;
-    if (!fit_smem(p, wave)) return DT_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(p->chain_smem)) != cudaSuccess)
-      return DT_ERR_CUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256,
-                                                      static_cast<int>(p->chain_smem)) !=
-        cudaSuccess)
-      return DT_ERR_CUDA;
-    if (per_sm < 1) return DT_ERR_UNSUPPORTED;
-    p->chain_grid = per_sm * p->num_sms;
-    if (wave > p->chain_grid) wave = p->chain_grid;
-    p->wave = wave;
+    if (!placed) {
+      int wave = wave0;
+      if (!fit_smem(p, wave)) return DT_ERR_UNSUPPORTED;
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(p->chain_smem)) != cudaSuccess)
+        return DT_ERR_CUDA;
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256,
+                                                        static_cast<int>(p->chain_smem)) !=
+          cudaSuccess)
+        return DT_ERR_CUDA;
+      if (per_sm < 1) return DT_ERR_UNSUPPORTED;
+      p->chain_grid = per_sm * p->num_sms;
+      if (wave > p->chain_grid) wave = p->chain_grid;
+      p->wave = wave;
+    }
   }
   const int wave = p->wave;
   const int e_cap = p->e_cap;
 
   // projection GEMM: split K so that the tiles x chunks fill every SM once
-  {
+  p->proj_ksplit = 1;
+  if (!p->marginal) {
     const int tiles = gemm_tiles(static_cast<int>(rows), d.r);
     int ks = p->num_sms / tiles;
     const int kmax = (d.d + 15) / 16;
@@ -210,6 +215,11 @@ int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, P
   off = al(off + (p->nsplit > 1 ? sizeof(uint64_t) * rows * p->nsplit * d.M : 0));
   p->off_cand_id = off;   off = al(off + sizeof(int32_t) * rows * d.M);
   p->off_cand_val = off;  off = al(off + sizeof(float) * rows * d.M);
+  if (p->marginal) {
+    p->off_U = p->off_S = p->off_gh = p->off_gin = p->off_p = p->off_colexp = p->off_colinfo =
+        p->off_kids = p->off_upart = p->off_partial = p->off_gin16 = p->off_end = off;
+    return DT_OK;
+  }
   p->off_U = off;         off = al(off + sizeof(float) * rows * d.r);
   const size_t slots_e = static_cast<size_t>(wave) * (e_cap + 1);
   p->off_S = off;         off = al(off + sizeof(float) * slots_e * d.d_s);
@@ -281,6 +291,8 @@ using dt::Plan;
 
 namespace {
 
+bool is_marginal(const dt_options *opt) { return opt && (opt->flags & DT_OPT_MARGINAL); }
+
 int check_weights(const dt_weights *w) {
   if (!w || !w->E || !w->W_ih || !w->W_hh || !w->W1 || !w->W2) return DT_ERR_INVALID_ARG;
   if (!dt::aligned16(w->E) || !dt::aligned16(w->W_ih) || !dt::aligned16(w->W_hh) ||
@@ -347,6 +359,19 @@ int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const f
   char *wsb = static_cast<char *>(ws);
   if (cudaMemsetAsync(wsb + pl.off_ctrl, 0, pl.off_part - pl.off_ctrl, st) != cudaSuccess)
     return DT_ERR_CUDA;
+  if (pl.marginal) {
+    if (dt::launch_topm(pl, base_logits, ws, out->topm, st) != cudaSuccess) return DT_ERR_CUDA;
+    rc = record(opt, 1, st);
+    if (!rc) rc = record(opt, 2, st);
+    if (rc) return rc;
+    const unsigned *ticket = reinterpret_cast<const unsigned *>(wsb + pl.off_ctrl + dt::kCtrlHeader);
+    const int *req_flags = reinterpret_cast<const int *>(ticket + static_cast<size_t>(d.batch) * d.D);
+    if (dt::launch_marginal(d, reinterpret_cast<const int32_t *>(wsb + pl.off_cand_id),
+                            reinterpret_cast<const float *>(wsb + pl.off_cand_val), req_flags,
+                            anchor_tok, temperature, out, st) != cudaSuccess)
+      return DT_ERR_CUDA;
+    return record(opt, 3, st);
+  }
   // the projection (compute bound) runs on a side stream beside the top-M
   // selection (HBM bound); the two touch disjoint workspace regions
   cudaStream_t side = side_stream();
@@ -463,6 +488,7 @@ int dt_kernel_launches(const dt_dims *dims, int wdtype, const dt_options *opt) {
   Plan pl;
   if (!dims || (wdtype != DT_F32 && wdtype != DT_BF16)) return 0;
   if (dt::make_plan(dims, wdtype, opt, &pl)) return 0;
+  if (pl.marginal) return 2;
   const int waves = (dims->batch + pl.wave - 1) / pl.wave;
   return 2 + (pl.proj_ksplit > 1 ? 1 : 0) + waves;
 }
@@ -474,19 +500,23 @@ int dt_build_trees(const dt_dims *dims, const dt_weights *w, const void *prepare
                    void *stream) {
   int rc = dt::validate_dims(dims);
   if (rc) return rc;
-  rc = check_weights(w);
-  if (rc) return rc;
+  const bool marginal = is_marginal(opt);
+  if (!marginal) {
+    rc = check_weights(w);
+    if (rc) return rc;
+    if (!prepared || !H || !state0 || !dt::aligned16(prepared) || !dt::aligned16(H) ||
+        !dt::aligned16(state0))
+      return DT_ERR_INVALID_ARG;
+  }
   rc = check_out(out);
   if (rc) return rc;
-  if (!prepared || !base_logits || !H || !state0 || !anchor_tok || !workspace)
-    return DT_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || !dt::aligned16(prepared) ||
-      !dt::aligned16(H) || !dt::aligned16(state0) || !dt::aligned4(base_logits) ||
+  if (!base_logits || !anchor_tok || !workspace) return DT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || !dt::aligned4(base_logits) ||
       !dt::aligned4(anchor_tok) || (temperature && !dt::aligned4(temperature)))
     return DT_ERR_INVALID_ARG;
   if (dims->V % 4 == 0 && !dt::aligned16(base_logits)) return DT_ERR_INVALID_ARG;
   Plan pl;
-  rc = dt::make_plan(dims, w->wdtype, opt, &pl);
+  rc = dt::make_plan(dims, marginal ? DT_F32 : w->wdtype, opt, &pl);
   if (rc) return rc;
   if (workspace_bytes < pl.off_end) return DT_ERR_INVALID_ARG;
   return run_round(pl, w, prepared, base_logits, H, state0, anchor_tok, temperature, workspace,
@@ -506,14 +536,18 @@ int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *pr
                         const dt_options *opt, void *stream) {
   int rc = dt::validate_dims(dims);
   if (rc) return rc;
-  rc = check_weights(w);
-  if (rc) return rc;
+  const bool marginal = is_marginal(opt);
+  if (!marginal) {
+    rc = check_weights(w);
+    if (rc) return rc;
+    if (!prepared || !H || !state0) return DT_ERR_INVALID_ARG;
+  }
   if (!host_out || !host_out->tokens || !host_out->parents || !host_out->depths ||
-      !host_out->scores || !host_out->status || !prepared || !base_logits || !H || !state0 ||
-      !anchor_tok || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      !host_out->scores || !host_out->status || !base_logits || !anchor_tok || !workspace ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return DT_ERR_INVALID_ARG;
   Plan pl;
-  rc = dt::make_plan(dims, w->wdtype, opt, &pl);
+  rc = dt::make_plan(dims, marginal ? DT_F32 : w->wdtype, opt, &pl);
   if (rc) return rc;
   const size_t ws_dev = dt_workspace_bytes(dims, opt);
   const HostStaging s = host_staging(*dims, dt::al(ws_dev));
@@ -530,8 +564,8 @@ int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *pr
   };
   const size_t nb = static_cast<size_t>(d.batch);
   if (!h2d(s.base, base_logits, sizeof(float) * nb * d.D * d.V) ||
-      !h2d(s.H, H, sizeof(float) * nb * d.D * d.d) ||
-      !h2d(s.state0, state0, sizeof(float) * nb * d.d_s) ||
+      (!marginal && !h2d(s.H, H, sizeof(float) * nb * d.D * d.d)) ||
+      (!marginal && !h2d(s.state0, state0, sizeof(float) * nb * d.d_s)) ||
       !h2d(s.anchor, anchor_tok, sizeof(int32_t) * nb) ||
       (temperature && !h2d(s.temp, temperature, sizeof(float) * nb)))
     return DT_ERR_CUDA;

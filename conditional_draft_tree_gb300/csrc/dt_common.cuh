@@ -152,6 +152,44 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Full descending bitonic sort of 32*SLOTS keys held slot-major in a warp.
+template <int SLOTS>
+__device__ __forceinline__ void warp_sort_desc(uint64_t v[SLOTS], int lane) {
+  constexpr int n = 32 * SLOTS;
+#pragma unroll
+  for (int size = 2; size <= n; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride >= 1; stride >>= 1) {
+      if (stride >= 32) {
+        const int ds = stride >> 5;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+          if ((s & ds) == 0) {
+            const int i = s * 32 + lane;
+            const bool desc = (i & size) == 0;
+            uint64_t a = v[s], b = v[s + ds];
+            bool sw = desc ? (a < b) : (a > b);
+            v[s] = sw ? b : a;
+            v[s + ds] = sw ? a : b;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+          const int i = s * 32 + lane;
+          const bool desc = (i & size) == 0;
+          uint64_t o = shfl64_xor(v[s], stride);
+          const bool low = (lane & stride) == 0;
+          // lower index keeps the larger key in a descending run
+          const bool keep_max = (low == desc);
+          uint64_t mx = v[s] > o ? v[s] : o, mn = v[s] > o ? o : v[s];
+          v[s] = keep_max ? mx : mn;
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ math
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }

@@ -23,6 +23,7 @@ struct Plan {
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
   int cluster;         // 0, or the cluster size (= ks) of the search launch
   int test_timeout;    // DT_OPT_TEST_BARRIER_TIMEOUT
+  int marginal;        // DT_OPT_MARGINAL: top-M, then the marginal tree kernel
   int num_sms;
   int chain_grid;      // co-resident blocks of the search kernel
   int wave;            // requests per search launch (<= chain_grid)
@@ -91,5 +92,12 @@ struct ChainArgs {
   int b0, nb;
 };
 cudaError_t launch_chain(const Plan &p, const ChainArgs &a, void *ws, cudaStream_t st);
+
+// Marginal-score trees (DT_OPT_MARGINAL): one block per request over the top-M
+// kernel's candidates (cand_id / cand_val [batch][D][M], req_flags [batch]).
+size_t marginal_smem_bytes(const dt_dims &d);
+cudaError_t launch_marginal(const dt_dims &d, const int32_t *cand_id, const float *cand_val,
+                            const int *req_flags, const int32_t *anchor, const float *temperature,
+                            const dt_tree_out *out, cudaStream_t st);
 
 }  // namespace dt

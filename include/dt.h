@@ -125,6 +125,17 @@ typedef struct {
  * usable. */
 #define DT_OPT_TEST_BARRIER_TIMEOUT 2
 
+/* dt_options.flags: marginal scoring, the conditionality ablation of
+ * "Riassunto Tecnico: DominoTree" (Risultati Sperimentali), a DDTree-style
+ * builder. The children of a node at depth j - 1 are the k best of C_j (the
+ * depth's top-M candidates) by L_c = L_base^j[c] / T alone, with
+ * lp_c = L_c - logsumexp over C_j; no GRU state and no correction, so a node's
+ * score is the sum of its path's per-depth lp and the result equals the
+ * conditional build with W2 = 0. Best-first order, budget and outputs are those
+ * of the conditional build. In this mode w, prepared, H and state0 are not read
+ * and may be NULL; one small kernel replaces the projection and the search. */
+#define DT_OPT_MARGINAL 8
+
 
 #define DT_NUM_PHASE_EVENTS 4 /* start, after top-M, after the projection, after the search */
 
@@ -145,7 +156,8 @@ size_t dt_workspace_bytes(const dt_dims *dims, const dt_options *opt);
 
 /* Kernel launches one dt_build_trees call makes for `dims`, weight type
  * `wdtype` (DT_F32 / DT_BF16) and `opt` (may be NULL): top-M, projection (plus
- * its split-K sum when K is split), one search launch per wave of requests.
+ * its split-K sum when K is split), one search launch per wave of requests;
+ * with DT_OPT_MARGINAL, top-M and the marginal tree kernel.
  * Memsets and event records are not counted. Returns 0 for invalid dims.
  * Host only; needs the device for its SM count. */
 int dt_kernel_launches(const dt_dims *dims, int wdtype, const dt_options *opt);

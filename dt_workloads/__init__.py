@@ -26,12 +26,12 @@ import dataclasses
 import numpy as np
 
 __all__ = ["Workload", "CONFIGS", "make_workload", "custom_workload", "f32_to_bf16_bits",
-           "bf16_bits_to_f32"]
+           "bf16_bits_to_f32", "chain_uniforms"]
 
 # Index of each tensor's child seed. Fixed forever: changing it changes every input.
 _SEED_SLOTS = {
     "base": 0, "spikes": 1, "H": 2, "E": 3, "W_ih": 4, "W_hh": 5, "W1": 6, "W2": 7,
-    "anchor": 8, "zipf_s": 9, "state0": 10, "b_ih": 11, "b_hh": 12,
+    "anchor": 8, "zipf_s": 9, "state0": 10, "b_ih": 11, "b_hh": 12, "chain_u": 13,
 }
 _N_SLOTS = 16
 
@@ -205,3 +205,12 @@ def make_workload(cfg: int, batch: int | None = None) -> Workload:
     return custom_workload(logits=c["logits"], zipf=c.get("zipf", (1.1, 1.1)),
                            temperature=c.get("temperature"),
                            e_std=0.02 if cfg == 0 else None, **kw)
+
+
+def chain_uniforms(batch: int, D: int, seed: int = 0) -> np.ndarray:
+    """Uniform draws in [0, 1), float32 [batch][D]: the random numbers of the
+    sampled (T > 0) chain decoder, one per draft position, passed to both the
+    CUDA path and the oracle as an input. Drawn from the ``seed``'s own child
+    stream, so they never change another tensor of the same seed."""
+    kid = np.random.SeedSequence(seed).spawn(_N_SLOTS)[_SEED_SLOTS["chain_u"]]
+    return np.random.default_rng(kid).random((batch, D), dtype=np.float32)

@@ -72,6 +72,8 @@ def lib():
                                    C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
         L.orc_score_path.argtypes = [C.POINTER(_Model), C.POINTER(_Request), C.c_void_p, C.c_int,
                                      C.c_void_p, C.c_void_p]
+        L.orc_chain.argtypes = [C.POINTER(_Model), C.POINTER(_Request), C.c_void_p, C.c_void_p,
+                                C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
         _lib = L
     return _lib
 
@@ -194,3 +196,35 @@ def score_path(w, path, b: int = 0):
     if rc:
         raise ValueError(f"orc_score_path failed: {rc}")
     return float(sc[0]), int(it[0])
+
+
+def chain(w, b: int = 0, uniforms=None, forced=None) -> dict:
+    """Domino chain decoding of request ``b`` (``orc_chain``): D draft tokens,
+    greedy at T = 0, else drawn by inverse CDF at ``uniforms[b]`` ([batch][D]
+    array, or None for zeros). ``forced`` ([D] tokens) replays the chain along
+    given tokens. Returns decided, tokens, lp, margin and the status."""
+    m, keep = _model(w)
+    q = _request(w, b, keep)
+    u = None
+    if uniforms is not None:
+        u = np.ascontiguousarray(np.asarray(uniforms)[b], dtype=np.float32)
+    f = None if forced is None else np.ascontiguousarray(np.asarray(forced), dtype=np.int32)
+    out = dict(decided=np.full(w.D, -1, np.int32), tokens=np.full(w.D, -1, np.int32),
+               lp=np.full(w.D, np.nan, np.float32), margin=np.full(w.D, np.nan, np.float32))
+    rc = lib().orc_chain(C.byref(m), C.byref(q), _ptr(u), _ptr(f), out["decided"].ctypes.data,
+                         out["tokens"].ctypes.data, out["lp"].ctypes.data,
+                         out["margin"].ctypes.data)
+    out["status"] = rc
+    return out
+
+
+def chains(w, requests=None, uniforms=None, forced=None, *, threads: int | None = None):
+    """``chain`` for several requests (all by default), ``threads`` at a time;
+    ``forced`` is then [batch][D]."""
+    reqs = list(range(w.batch)) if requests is None else list(requests)
+    lib()
+    run = lambda b: chain(w, b, uniforms, None if forced is None else np.asarray(forced)[b])
+    if (threads or 1) == 1 or len(reqs) == 1:
+        return [run(b) for b in reqs]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(run, reqs))

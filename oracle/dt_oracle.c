@@ -1,6 +1,6 @@
 /*
  * dt_oracle.c -- plain CPU oracle of the DominoTree per-round conditional
- * draft-tree builder.
+ * draft-tree builder and of Domino's chain decoder (orc_chain, at the end).
  *
  * TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the
  * benchmark's CPU-baseline leg may load, call or link this file. The CUDA
@@ -458,4 +458,128 @@ int orc_score_path(const orc_model *m, const orc_request *q, const int32_t *path
   *in_tree = ok;
   free(s); free(s2); ctx_free(&c);
   return ORC_OK;
+}
+
+/* ------------------------------------------------- Domino chain decoding */
+
+/* One request of Domino's chain decoder ([DOM] method steps, inference: the
+ * parallel backbone gives the base logits, the head updates the causal state
+ * from the previously drawn draft token, corrects the logits and each draft
+ * token is drawn from the corrected logits; [DOM] core method for the state
+ * and the correction; [TREE] Definizione del Problema: the released decoder
+ * follows this single chain). With the same readings as the tree builder
+ * (root state, GRU gates, temperature divides the corrected logits):
+ *
+ *   S_0 = GRU(state0, E[anchor])
+ *   for i = 1..D:
+ *     h   = SiLU(W1[:, :d] . H_i + W1[:, d:] . S_{i-1})
+ *     x_v = (L_base^i[v] + W2[v, :] . h) / Teff          every v in [0, V)
+ *     m   = max_v x_v,  Z = sum_v exp(x_v - m)            (fp64, id order)
+ *     T = 0 (greedy):  d_i = argmax_v x_v, lowest id among equal values
+ *     T > 0 (sampled): d_i = min { v : sum_{w <= v} exp(x_w - m) > u_i Z },
+ *                      the inverse CDF of softmax(x) in token-id order at the
+ *                      caller's uniform draw u_i (clamped into [0, 1); NaN
+ *                      reads as 0); the last v with exp(x_v - m) > 0 if the
+ *                      sum never exceeds u_i Z
+ *     t_i = forced[i-1] when `forced` is given, else d_i
+ *     lp_i = x_{t_i} - (m + log Z)
+ *     S_i = GRU(S_{i-1}, E[t_i])
+ * Teff = T, or 1 when T = 0. A depth whose x values are all -inf gives
+ * d_i = 0 and lp_i = -inf.
+ *
+ * Per step i (arrays of D): decided = d_i, tokens = t_i, lp = lp_i, and margin
+ * = how close the decision was: greedy, x_(1) - x_(2) (best minus second-best
+ * value, 0 on a tie); sampled, the distance of u_i Z from the nearer end of
+ * d_i's CDF interval divided by Z. `forced` lets a caller replay the oracle
+ * along another decoder's tokens and judge every step on its own.
+ * Returns ORC_ENONFINITE when a base logit is NaN or +inf, ORC_EINVAL for a
+ * temperature < 0 or not finite, or a token out of range. */
+int orc_chain(const orc_model *m, const orc_request *q, const float *u, const int32_t *forced,
+              int32_t *decided, int32_t *tokens, float *lp, float *margin) {
+  int rc = check_model(m);
+  if (rc) return rc;
+  if (!q || !q->base || !q->H || !q->state0 || !decided || !tokens || !lp || !margin)
+    return ORC_EINVAL;
+  if (q->anchor < 0 || q->anchor >= m->V) return ORC_EINVAL;
+  if (!(q->temperature >= 0.0f) || isinf(q->temperature)) return ORC_EINVAL;
+  for (size_t i = 0; i < (size_t)m->D * m->V; ++i)
+    if (isnan(q->base[i]) || (isinf(q->base[i]) && q->base[i] > 0)) return ORC_ENONFINITE;
+  const int greedy = q->temperature == 0.0f;
+  const double Teff = greedy ? 1.0 : (double)q->temperature;
+  const int V = m->V, ds = m->d_s, r = m->r;
+  float *s = (float *)malloc(sizeof(float) * ds);
+  float *s2 = (float *)malloc(sizeof(float) * ds);
+  float *x = (float *)malloc(sizeof(float) * m->d);
+  float *h = (float *)malloc(sizeof(float) * r);
+  float *xv = (float *)malloc(sizeof(float) * V);
+  if (!s || !s2 || !x || !h || !xv) {
+    free(s); free(s2); free(x); free(h); free(xv);
+    return ORC_ENOMEM;
+  }
+  embed(m, q->anchor, x);
+  orc_gru_step(m->d, ds, m->wdtype, m->W_ih, m->W_hh, m->b_ih, m->b_hh, x, q->state0, s);
+  rc = ORC_OK;
+  for (int i = 0; i < m->D && rc == ORC_OK; ++i) {
+    const float *base = q->base + (size_t)i * V;
+    for (int t = 0; t < r; ++t) {
+      const size_t row = (size_t)t * (m->d + ds);
+      float U = dot_w(m->W1, m->wdtype, row, q->H + (size_t)i * m->d, m->d);
+      float P = dot_w(m->W1, m->wdtype, row + m->d, s, ds);
+      double a = (double)U + (double)P;
+      h[t] = (float)(a * sigmoid64(a));
+    }
+    double mx = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+      float dl = dot_w(m->W2, m->wdtype, (size_t)v * r, h, r);
+      xv[v] = (float)(((double)base[v] + (double)dl) / Teff);
+      if ((double)xv[v] > mx) mx = (double)xv[v];
+    }
+    int d = 0;
+    double Z = 0.0, mg = 0.0;
+    if (mx == -INFINITY) {
+      d = 0;
+      mg = 0.0;
+    } else {
+      for (int v = 0; v < V; ++v) Z += exp((double)xv[v] - mx);
+      if (greedy) {
+        float best = xv[0], second = -INFINITY;
+        int arg = 0;
+        for (int v = 1; v < V; ++v) {
+          if (xv[v] > best) { second = best; best = xv[v]; arg = v; }
+          else if (xv[v] > second) second = xv[v];   /* a tie with best makes the gap 0 */
+        }
+        d = arg;
+        mg = (double)best - (double)second;
+      } else {
+        float uu = u ? u[i] : 0.0f;
+        double uc = (uu >= 0.0f) ? (uu < 1.0f ? (double)uu : (double)nextafterf(1.0f, 0.0f)) : 0.0;
+        const double target = uc * Z;
+        double cum = 0.0, lo_end = 0.0, hi_end = 0.0;
+        int last_pos = 0;
+        d = -1;
+        for (int v = 0; v < V; ++v) {
+          const double e = exp((double)xv[v] - mx);
+          if (e > 0.0) last_pos = v;
+          if (cum + e > target) { d = v; lo_end = cum; hi_end = cum + e; break; }
+          cum += e;
+        }
+        if (d < 0) { d = last_pos; lo_end = hi_end = cum; }
+        const double a = target - lo_end, b = hi_end - target;
+        mg = (a < b ? a : b) / Z;
+      }
+    }
+    const int32_t t = forced ? forced[i] : d;
+    if (t < 0 || t >= V) { rc = ORC_EINVAL; break; }
+    decided[i] = d;
+    tokens[i] = t;
+    margin[i] = (float)mg;
+    lp[i] = (mx == -INFINITY) ? -INFINITY : (float)((double)xv[t] - (mx + log(Z)));
+    if (i + 1 < m->D) {
+      embed(m, t, x);
+      orc_gru_step(m->d, ds, m->wdtype, m->W_ih, m->W_hh, m->b_ih, m->b_hh, x, s, s2);
+      memcpy(s, s2, sizeof(float) * ds);
+    }
+  }
+  free(s); free(s2); free(x); free(h); free(xv);
+  return rc;
 }

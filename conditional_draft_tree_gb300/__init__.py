@@ -29,7 +29,9 @@ MAX_SPEC = 16
 # every symbol include/dt.h declares
 EXPORTS = ("dt_abi_version", "dt_status_string", "dt_prepared_bytes", "dt_prepare_weights",
            "dt_workspace_bytes", "dt_build_trees", "dt_host_workspace_bytes",
-           "dt_build_trees_host", "dt_select_topm_noalloc", "dt_kernel_launches")
+           "dt_build_trees_host", "dt_select_topm_noalloc", "dt_kernel_launches",
+           "dt_chain_prepared_bytes", "dt_prepare_chain", "dt_chain_workspace_bytes",
+           "dt_chain_kernel_launches", "dt_decode_chains")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -87,6 +89,16 @@ def lib():
         L.dt_build_trees_host.argtypes = sig
         L.dt_select_topm_noalloc.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
                                              C.c_void_p, C.c_void_p, C.c_void_p]
+        L.dt_chain_prepared_bytes.restype = C.c_size_t
+        L.dt_chain_prepared_bytes.argtypes = [C.POINTER(DtDims)]
+        L.dt_prepare_chain.argtypes = [C.POINTER(DtDims), C.POINTER(DtWeights), C.c_void_p,
+                                       C.c_size_t, C.c_void_p]
+        L.dt_chain_workspace_bytes.restype = C.c_size_t
+        L.dt_chain_workspace_bytes.argtypes = [C.POINTER(DtDims)]
+        L.dt_chain_kernel_launches.restype = C.c_int
+        L.dt_chain_kernel_launches.argtypes = [C.POINTER(DtDims)]
+        L.dt_decode_chains.argtypes = [C.POINTER(DtDims), C.POINTER(DtWeights)] + \
+            [C.c_void_p] * 9 + [C.c_size_t] + [C.c_void_p] * 4
         _lib = L
     return _lib
 
@@ -321,3 +333,93 @@ class MarginalTreeBuilder:
         f = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(self.device)
         return dict(base_logits=f(wl.base_logits, np.float32), anchor_tok=f(wl.anchor, np.int32),
                     temperature=f(wl.temperature, np.float32))
+
+
+
+# ------------------------------------------------------------ chain decoding
+
+def chain_prepared_bytes(dims: DtDims) -> int:
+    return lib().dt_chain_prepared_bytes(C.byref(dims))
+
+
+def prepare_chain(dims: DtDims, w: DeviceWeights, chain_prepared: torch.Tensor, stream=None):
+    """dt_prepare_chain: the weight tiles of the chain decoder's tensor-core products."""
+    ws = w.struct()
+    _check(lib().dt_prepare_chain(C.byref(dims), C.byref(ws), chain_prepared.data_ptr(),
+                                  chain_prepared.numel() * chain_prepared.element_size(),
+                                  _stream(stream)), "dt_prepare_chain")
+
+
+def chain_workspace_bytes(dims: DtDims) -> int:
+    return lib().dt_chain_workspace_bytes(C.byref(dims))
+
+
+def chain_kernel_launches(dims: DtDims) -> int:
+    return lib().dt_chain_kernel_launches(C.byref(dims))
+
+
+def decode_chains(dims: DtDims, w: DeviceWeights, prepared, chain_prepared, base_logits, H,
+                  state0, anchor_tok, temperature, uniforms, workspace, tokens, logprobs, status,
+                  stream=None):
+    """Enqueue one chain-decoding round on device tensors (dt_decode_chains)."""
+    ws = w.struct()
+    _check(lib().dt_decode_chains(C.byref(dims), C.byref(ws), _ptr(prepared), _ptr(chain_prepared),
+                                  _ptr(base_logits), _ptr(H), _ptr(state0), _ptr(anchor_tok),
+                                  _ptr(temperature), _ptr(uniforms), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _ptr(tokens),
+                                  _ptr(logprobs), _ptr(status), _stream(stream)),
+           "dt_decode_chains")
+
+
+class ChainDecoder:
+    """Device weights, both prepared tables and a workspace for Domino chain
+    decoding of one shape (bf16 weights). ``run(...)`` decodes one round:
+    D draft tokens and their log-probabilities per request."""
+
+    def __init__(self, dims: DtDims, weights: DeviceWeights, device="cuda"):
+        self.dims = dims
+        self.w = weights
+        self.device = torch.device(device)
+        nbytes = prepared_bytes(dims)
+        cbytes = chain_prepared_bytes(dims)
+        if nbytes == 0 or cbytes == 0:
+            raise DtError("invalid dims")
+        self.prepared = torch.empty(nbytes // 4, dtype=torch.float32, device=self.device)
+        prepare_weights(dims, weights, self.prepared)
+        self.chain_prepared = torch.empty(cbytes, dtype=torch.uint8, device=self.device)
+        prepare_chain(dims, weights, self.chain_prepared)
+        wsb = chain_workspace_bytes(dims)
+        if wsb == 0:
+            raise DtError("dt_chain_workspace_bytes failed (invalid dims or unsupported device)")
+        self.workspace = torch.empty(wsb, dtype=torch.uint8, device=self.device)
+
+    @classmethod
+    def from_numpy(cls, wl, device="cuda", batch=None):
+        dims = dims_of(wl.V, wl.d, wl.d_s, wl.r, wl.D, wl.M, wl.k, wl.N,
+                       wl.batch if batch is None else batch)
+        return cls(dims, TreeBuilder.weights_from_numpy(wl, device), device)
+
+    def alloc_outputs(self):
+        B, D = self.dims.batch, self.dims.D
+        return dict(tokens=torch.empty((B, D), dtype=torch.int32, device=self.device),
+                    logprobs=torch.empty((B, D), dtype=torch.float32, device=self.device),
+                    status=torch.empty((B,), dtype=torch.int32, device=self.device))
+
+    def run(self, base_logits, H, state0, anchor_tok, temperature=None, uniforms=None, out=None,
+            stream=None):
+        if out is None:
+            out = self.alloc_outputs()
+        decode_chains(self.dims, self.w, self.prepared, self.chain_prepared, base_logits, H,
+                      state0, anchor_tok, temperature, uniforms, self.workspace, out["tokens"],
+                      out["logprobs"], out["status"], stream)
+        return out
+
+    def inputs_to_device(self, wl, uniforms=None):
+        import numpy as np
+        f = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(self.device)
+        d = dict(base_logits=f(wl.base_logits, np.float32), H=f(wl.H, np.float32),
+                 state0=f(wl.state0, np.float32), anchor_tok=f(wl.anchor, np.int32),
+                 temperature=f(wl.temperature, np.float32))
+        if uniforms is not None:
+            d["uniforms"] = f(uniforms, np.float32)
+        return d

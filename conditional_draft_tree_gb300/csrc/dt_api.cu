@@ -407,6 +407,40 @@ int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const f
   return record(opt, 3, st);
 }
 
+// Chain-decoding plan: kernel shapes plus the workspace carve-up.
+int decode_plan_for(const dt_dims *dims, dt::DecodePlan *pl) {
+  int rc = dt::validate_dims(dims);
+  if (rc) return rc;
+  int sms = 0, smem = 0;
+  rc = dt::device_sm_count(&sms, &smem);
+  if (rc) return rc;
+  rc = dt::decode_plan(*dims, sms, smem, pl);
+  if (rc) return rc;
+  const dt_dims &d = *dims;
+  const size_t wave = static_cast<size_t>(pl->wave);
+  const long long rows = static_cast<long long>(d.batch) * d.D;
+  {
+    const int tiles = dt::gemm_tiles(static_cast<int>(rows), d.r);
+    const int ks = sms / tiles, kmax = (d.d + 15) / 16;
+    pl->proj_ksplit = ks < 1 ? 1 : (ks > 32 ? 32 : (ks > kmax ? kmax : ks));
+  }
+  const size_t vpad = static_cast<size_t>(pl->n_tV) * 128, gn = static_cast<size_t>(pl->n_tV) * 4;
+  size_t off = 0;
+  pl->off_ctrl = off;  off = dt::al(off + sizeof(dt::Ctrl));
+  pl->off_U = off;     off = dt::al(off + sizeof(float) * rows * d.r);
+  pl->off_upart = off;
+  off = dt::al(off + (pl->proj_ksplit > 1 ? sizeof(float) * pl->proj_ksplit * rows * d.r : 0));
+  pl->off_ypart = off; off = dt::al(off + sizeof(float) * pl->n_kz * wave * pl->R);
+  pl->off_S = off;     off = dt::al(off + sizeof(float) * wave * d.d_s);
+  pl->off_X = off;     off = dt::al(off + sizeof(float) * wave * vpad);
+  pl->off_stm = off;   off = dt::al(off + sizeof(float) * wave * gn);
+  pl->off_sts = off;   off = dt::al(off + sizeof(float) * wave * gn);
+  pl->off_sta = off;   off = dt::al(off + sizeof(int32_t) * wave * gn);
+  pl->off_flags = off; off = dt::al(off + sizeof(int) * wave);
+  pl->off_end = off;
+  return DT_OK;
+}
+
 struct HostStaging {
   size_t base, H, state0, anchor, temp, tokens, parents, depths, scores, mask, topm, status, end;
 };
@@ -592,6 +626,107 @@ int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *pr
       (host_out->mask && !d2h(host_out->mask, s.mask, nb * n1 * n1)) ||
       (host_out->topm && !d2h(host_out->topm, s.topm, sizeof(int32_t) * nb * d.D * d.M)))
     return DT_ERR_CUDA;
+  return DT_OK;
+}
+
+/* ------------------------------------------------- Domino chain decoding */
+
+size_t dt_chain_prepared_bytes(const dt_dims *dims) {
+  if (dt::validate_dims(dims)) return 0;
+  return dt::decode_prepared_bytes(*dims);
+}
+
+int dt_prepare_chain(const dt_dims *dims, const dt_weights *w, void *chain_prepared,
+                     size_t chain_prepared_bytes, void *stream) {
+  int rc = dt::validate_dims(dims);
+  if (rc) return rc;
+  rc = check_weights(w);
+  if (rc) return rc;
+  if (w->wdtype != DT_BF16) return DT_ERR_UNSUPPORTED;
+  if (!chain_prepared || (reinterpret_cast<uintptr_t>(chain_prepared) & 255u) ||
+      chain_prepared_bytes < dt_chain_prepared_bytes(dims))
+    return DT_ERR_INVALID_ARG;
+  int sms = 0, smem = 0;
+  rc = dt::device_sm_count(&sms, &smem);
+  if (rc) return rc;
+  if (dt::launch_decode_prepare(*dims, w, chain_prepared, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return DT_ERR_CUDA;
+  return DT_OK;
+}
+
+size_t dt_chain_workspace_bytes(const dt_dims *dims) {
+  dt::DecodePlan pl;
+  if (decode_plan_for(dims, &pl)) return 0;
+  return pl.off_end;
+}
+
+int dt_chain_kernel_launches(const dt_dims *dims) {
+  dt::DecodePlan pl;
+  if (decode_plan_for(dims, &pl)) return 0;
+  return 1 + (pl.proj_ksplit > 1 ? 1 : 0) + (dims->batch + pl.wave - 1) / pl.wave;
+}
+
+int dt_decode_chains(const dt_dims *dims, const dt_weights *w, const void *prepared,
+                     const void *chain_prepared, const float *base_logits, const float *H,
+                     const float *state0, const int32_t *anchor_tok, const float *temperature,
+                     const float *uniforms, void *workspace, size_t workspace_bytes,
+                     int32_t *tokens, float *logprobs, int32_t *status, void *stream) {
+  int rc = dt::validate_dims(dims);
+  if (rc) return rc;
+  rc = check_weights(w);
+  if (rc) return rc;
+  if (w->wdtype != DT_BF16) return DT_ERR_UNSUPPORTED;
+  if (!prepared || !chain_prepared || !base_logits || !H || !state0 || !anchor_tok ||
+      !workspace || !tokens || !logprobs || !status)
+    return DT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || !dt::aligned16(prepared) ||
+      !dt::aligned16(chain_prepared) || !dt::aligned16(H) || !dt::aligned16(state0) ||
+      !dt::aligned4(base_logits) || !dt::aligned4(anchor_tok) ||
+      (temperature && !dt::aligned4(temperature)) || (uniforms && !dt::aligned4(uniforms)) ||
+      !dt::aligned4(tokens) || !dt::aligned4(logprobs) || !dt::aligned4(status))
+    return DT_ERR_INVALID_ARG;
+  dt::DecodePlan pl;
+  rc = decode_plan_for(dims, &pl);
+  if (rc) return rc;
+  if (workspace_bytes < pl.off_end) return DT_ERR_INVALID_ARG;
+  const dt_dims &d = *dims;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char *wsb = static_cast<char *>(workspace);
+  float *U = reinterpret_cast<float *>(wsb + pl.off_U);
+  // U_i = W1[:, :d] H_i for every request and position (path independent)
+  if (dt::launch_gemm_nt(d.batch * d.D, d.r, d.d, H, DT_F32, d.d, w->W1, w->wdtype,
+                         static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r, pl.proj_ksplit,
+                         reinterpret_cast<float *>(wsb + pl.off_upart), st) != cudaSuccess)
+    return DT_ERR_CUDA;
+  dt::DecodeArgs a;
+  a.chain_prepared = chain_prepared;
+  a.G = static_cast<const float *>(prepared);
+  a.b_hh = w->b_hh;
+  a.U = U;
+  a.base = base_logits;
+  a.state0 = state0;
+  a.temperature = temperature;
+  a.uniforms = uniforms;
+  a.anchor = anchor_tok;
+  a.ypart = reinterpret_cast<float *>(wsb + pl.off_ypart);
+  a.S = reinterpret_cast<float *>(wsb + pl.off_S);
+  a.X = reinterpret_cast<float *>(wsb + pl.off_X);
+  a.st_m = reinterpret_cast<float *>(wsb + pl.off_stm);
+  a.st_s = reinterpret_cast<float *>(wsb + pl.off_sts);
+  a.st_a = reinterpret_cast<int32_t *>(wsb + pl.off_sta);
+  a.flags = reinterpret_cast<int *>(wsb + pl.off_flags);
+  a.ctrl = reinterpret_cast<dt::Ctrl *>(wsb + pl.off_ctrl);
+  a.tokens = tokens;
+  a.logprobs = logprobs;
+  a.status = status;
+  for (int b0 = 0; b0 < d.batch; b0 += pl.wave) {
+    a.b0 = b0;
+    a.nb = (d.batch - b0) < pl.wave ? (d.batch - b0) : pl.wave;
+    if (cudaMemsetAsync(wsb + pl.off_ctrl, 0, sizeof(dt::Ctrl), st) != cudaSuccess)
+      return DT_ERR_CUDA;
+    if (dt::launch_decode(pl, a, st) != cudaSuccess) return DT_ERR_CUDA;
+  }
   return DT_OK;
 }
 

@@ -93,6 +93,38 @@ struct ChainArgs {
 };
 cudaError_t launch_chain(const Plan &p, const ChainArgs &a, void *ws, cudaStream_t st);
 
+// Domino chain decoding (dt_decode.cu): sizes of the two tensor-core GEMMs,
+// wave size (requests per launch) and the workspace carve-up.
+struct DecodePlan {
+  dt_dims dims;
+  int num_sms, grid, wave;
+  int R, n_tA, nchA, n_kz, n_tV, nchV, kb;
+  size_t smem;
+  int proj_ksplit;
+  size_t off_ctrl, off_U, off_upart, off_ypart, off_S, off_X, off_stm, off_sts, off_sta,
+      off_flags, off_end;
+};
+struct DecodeArgs {
+  const void *chain_prepared;  // dt_prepare_chain output
+  const float *G;              // dt_prepare_weights output [V][3 d_s]
+  const float *b_hh, *U, *base, *state0, *temperature, *uniforms;
+  const int32_t *anchor;
+  float *ypart, *S, *X, *st_m, *st_s;
+  int32_t *st_a;
+  int *flags;
+  Ctrl *ctrl;
+  int32_t *tokens;
+  float *logprobs;
+  int32_t *status;
+  int b0, nb;
+};
+void decode_shape(const dt_dims &d, DecodePlan *p);
+size_t decode_prepared_bytes(const dt_dims &d);
+int decode_plan(const dt_dims &d, int num_sms, int smem_optin, DecodePlan *p);
+cudaError_t launch_decode_prepare(const dt_dims &d, const dt_weights *w, void *out,
+                                  cudaStream_t st);
+cudaError_t launch_decode(const DecodePlan &pl, const DecodeArgs &a, cudaStream_t st);
+
 // Marginal-score trees (DT_OPT_MARGINAL): one block per request over the top-M
 // kernel's candidates (cand_id / cand_val [batch][D][M], req_flags [batch]).
 size_t marginal_smem_bytes(const dt_dims &d);

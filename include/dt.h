@@ -223,6 +223,51 @@ int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *pr
 int dt_select_topm_noalloc(const float *base_logits, int batch, int D, int V, int M,
                            int32_t *topm, int32_t *status, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Domino chain decoding: the released Domino decoder, a single draft chain per
+ * request with the correction over the whole vocabulary ("Domino：在投机解码中将因果建模与自回归草稿解耦",
+ * method steps, inference, and core method; "Riassunto Tecnico: DominoTree",
+ * Definizione del Problema: the released decoder is chain-only). Per request:
+ *   S_0 = GRU(state0, E[anchor])
+ *   for i = 1..D:  h = SiLU(W1 [H_i; S_{i-1}])
+ *                  x_v = (L_base^i[v] + W2[v,:] . h) / T       for every token v
+ *                  T = 0: d_i = argmax_v x_v (lowest id on ties), x taken at T = 1
+ *                  T > 0: d_i = the smallest v whose cumulative softmax(x) mass
+ *                         in token-id order exceeds u_i (inverse CDF)
+ *                  logprob_i = log softmax(x)[d_i]
+ *                  S_i = GRU(S_{i-1}, E[d_i])
+ * Weights must be bf16 (the two products run on the tensor cores with the fp32
+ * states and h split into three bf16 terms each); f32 weights give
+ * DT_ERR_UNSUPPORTED. dims->M, k and N are not used (any valid values).
+ *
+ * dt_prepare_chain: once per set of weights, [W_hh; W1[:, d:]] and W2 re-laid
+ * out in 128-row tensor-core tiles (dt_chain_prepared_bytes bytes, 256-byte
+ * aligned device buffer, caller-owned). The GRU input table comes from
+ * dt_prepare_weights (`prepared`).
+ *
+ * dt_decode_chains: one decoding round for dims->batch requests (device
+ * pointers; inputs as for dt_build_trees):
+ *   uniforms   [batch][D] fp32 draws for T > 0 (u outside [0, 1) is clamped into
+ *              it, NaN reads as 0; NULL reads as 0); unused where T = 0
+ *   tokens     [batch][D] int32 output: d_1..d_D (-1 on a non-OK status)
+ *   logprobs   [batch][D] fp32 output (NaN on a non-OK status)
+ *   status     [batch] DT_OK, DT_ERR_NONFINITE, DT_ERR_BAD_TEMPERATURE or
+ *              DT_ERR_TIMEOUT
+ *   workspace  dt_chain_workspace_bytes bytes, 256-byte aligned
+ * Asynchronous on `stream`; requests run in waves of up to 80 per launch.
+ * dt_chain_kernel_launches gives the launches of one call (projection, its
+ * split-K sum when K is split, one decoding launch per wave). */
+size_t dt_chain_prepared_bytes(const dt_dims *dims);
+int dt_prepare_chain(const dt_dims *dims, const dt_weights *w, void *chain_prepared,
+                     size_t chain_prepared_bytes, void *stream);
+size_t dt_chain_workspace_bytes(const dt_dims *dims);
+int dt_chain_kernel_launches(const dt_dims *dims);
+int dt_decode_chains(const dt_dims *dims, const dt_weights *w, const void *prepared,
+                     const void *chain_prepared, const float *base_logits, const float *H,
+                     const float *state0, const int32_t *anchor_tok, const float *temperature,
+                     const float *uniforms, void *workspace, size_t workspace_bytes,
+                     int32_t *tokens, float *logprobs, int32_t *status, void *stream);
+
 /* Static description of a status code. */
 const char *dt_status_string(int code);
 

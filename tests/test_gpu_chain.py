@@ -1,0 +1,160 @@
+"""Domino chain decoding (dt_decode_chains) against the oracle (needs a GB300).
+
+Each GPU chain is replayed by the oracle along the GPU's own tokens (``forced``),
+so every position is judged on its own: the token must be the oracle's decision
+unless the oracle's margin there is below TOL_TIE (the best and second-best
+values for greedy positions, the distance of u Z from an end of the chosen
+token's CDF interval, relative to Z, for sampled ones), and the log-probability
+of the token must agree within TOL_LP.
+
+Tolerances from the arithmetic: both GEMMs take exact products of bf16 weights
+and the three-term split of the fp32 operand, accumulated in fp32 (relative
+error about 1e-6 of the dot products' magnitude), and the softmax sums run in
+fp32 over at most 152K terms in 32-token groups (relative error near 1e-6);
+the oracle accumulates in fp64. 1e-4 on lp and on the decision margins leaves
+two orders of magnitude of room.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import dt_workloads as W
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+dt = pytest.importorskip("conditional_draft_tree_gb300")
+
+TOL_LP = 1e-4
+TOL_TIE = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from conditional_draft_tree_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def run_gpu(wl, uniforms=None, decoder=None, temperature=None):
+    dec = decoder or dt.ChainDecoder.from_numpy(wl)
+    inp = dec.inputs_to_device(wl, uniforms)
+    if temperature is not None:
+        inp["temperature"] = torch.as_tensor(temperature, dtype=torch.float32, device="cuda")
+    out = dec.run(**inp)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def compare(wl, g, reqs, uniforms=None, max_near=None):
+    """Replays the oracle along the GPU tokens; returns the number of near ties."""
+    refs = oracle.chains(wl, reqs, uniforms, forced=np.where(g["tokens"] >= 0, g["tokens"], 0),
+                         threads=8)
+    near = 0
+    for b, ref in zip(reqs, refs):
+        assert ref["status"] == 0
+        assert g["status"][b] == dt.OK
+        for i in range(wl.D):
+            tok = g["tokens"][b, i]
+            assert 0 <= tok < wl.V
+            if tok != ref["decided"][i]:
+                assert ref["margin"][i] < TOL_TIE, (b, i, tok, ref["decided"][i], ref["margin"][i])
+                near += 1
+            if np.isneginf(ref["lp"][i]):
+                assert np.isneginf(g["logprobs"][b, i])
+            else:
+                assert abs(float(g["logprobs"][b, i]) - float(ref["lp"][i])) <= TOL_LP, \
+                    (b, i, g["logprobs"][b, i], ref["lp"][i])
+    print(f"{wl.name}: {len(reqs)} chains x {wl.D} positions, {near} near ties")
+    if max_near is not None:
+        assert near <= max_near
+    return near
+
+
+BASE = dict(V=3000, d=64, d_s=32, r=24, D=7, M=20, k=4, N=48, batch=4, wdtype="bf16",
+            logits="zipf", zipf=(0.8, 1.6))
+SHAPES = {
+    "greedy": dict(BASE, seed=71, temperature=0.0),
+    "sampled": dict(BASE, seed=72, temperature=[0.5, 1.0, 1.5, 2.0]),
+    "mixed-bias-state0": dict(BASE, seed=73, temperature=[0.0, 1.0, 0.0, 0.7], biases=True,
+                              state0_std=0.5),
+    "ragged-V": dict(V=1001, d=32, d_s=40, r=40, D=5, M=12, k=3, N=20, batch=3, wdtype="bf16",
+                     seed=74, logits="spiked", e_std=0.3, temperature=[0.0, 1.0, 0.6]),
+    "two-K-ranges": dict(V=5000, d=48, d_s=320, r=136, D=4, M=16, k=4, N=20, batch=5,
+                         wdtype="bf16", seed=75, logits="zipf", zipf=(0.9, 1.4),
+                         temperature=[0.0, 1.0, 0.0, 1.0, 0.5]),
+    "big-ds": dict(V=2048, d=64, d_s=1280, r=64, D=4, M=16, k=4, N=24, batch=2, wdtype="bf16",
+                   seed=76, logits="zipf", zipf=(1.0, 1.2), temperature=[0.0, 1.0]),
+    "batch1": dict(BASE, seed=77, batch=1, temperature=1.0),
+    "two-waves": dict(V=2000, d=32, d_s=32, r=32, D=3, M=8, k=2, N=10, batch=100, wdtype="bf16",
+                      seed=78, logits="zipf", zipf=(0.8, 1.6), temperature="cycle"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_custom_shapes(name):
+    wl = W.custom_workload(name=name, **SHAPES[name])
+    u = W.chain_uniforms(wl.batch, wl.D, seed=SHAPES[name]["seed"])
+    g = run_gpu(wl, u)
+    reqs = list(range(wl.batch)) if wl.batch <= 8 else [0, 1, 79, 80, 81, 99]
+    compare(wl, g, reqs, u, max_near=1)
+
+
+def test_two_waves_launch_count():
+    wl = W.custom_workload(name="two-waves", **SHAPES["two-waves"])
+    dec = dt.ChainDecoder.from_numpy(wl)
+    assert dt.chain_kernel_launches(dec.dims) >= 3   # projection + two decoding waves
+
+
+def test_uniforms_null_reads_as_zero():
+    wl = W.custom_workload(name="sampled", **SHAPES["sampled"])
+    g = run_gpu(wl, None)
+    compare(wl, g, list(range(wl.batch)), np.zeros((wl.batch, wl.D), np.float32), max_near=1)
+
+
+def test_status_codes():
+    wl = W.custom_workload(name="status", **dict(BASE, seed=79, batch=5,
+                                                 temperature=[1.0, -1.0, 1.0, 1.0, 0.0]))
+    base = wl.base_logits.copy()
+    base[2, 3, 17] = np.nan
+    base[3, 0, 5] = np.inf
+    base[4, 1, :] = -np.inf            # request 4: an all -inf position (token 0, lp -inf)
+    wl = dataclasses.replace(wl, base_logits=base)
+    u = W.chain_uniforms(wl.batch, wl.D, seed=79)
+    g = run_gpu(wl, u)
+    assert list(g["status"]) == [dt.OK, dt.ERR_BAD_TEMPERATURE, dt.ERR_NONFINITE,
+                                 dt.ERR_NONFINITE, dt.OK]
+    for b in (1, 2, 3):
+        assert (g["tokens"][b] == -1).all() and np.isnan(g["logprobs"][b]).all()
+    assert g["tokens"][4, 1] == 0 and np.isneginf(g["logprobs"][4, 1])
+    compare(wl, g, [0, 4], u)
+
+
+def test_deterministic():
+    wl = W.custom_workload(name="sampled", **SHAPES["sampled"])
+    u = W.chain_uniforms(wl.batch, wl.D, seed=72)
+    dec = dt.ChainDecoder.from_numpy(wl)
+    a, b = run_gpu(wl, u, dec), run_gpu(wl, u, dec)
+    for key in ("tokens", "logprobs", "status"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_config3_qwen3_8b_b32():
+    """Batch 32 at the Qwen3-8B shape (V = 151936, d_s = 1024, r = 256, D = 15),
+    sampled at T = 1 and greedy: every chain valid, three of each against the oracle."""
+    wl = W.make_workload(3)
+    u = W.chain_uniforms(wl.batch, wl.D, seed=3)
+    dec = dt.ChainDecoder.from_numpy(wl)
+    for T in (None, np.zeros(wl.batch, np.float32)):
+        g = run_gpu(wl, u, dec, temperature=T)
+        assert (g["status"] == dt.OK).all()
+        assert ((g["tokens"] >= 0) & (g["tokens"] < wl.V)).all()
+        assert (g["logprobs"] <= 1e-6).all()
+        w = wl if T is None else dataclasses.replace(wl, temperature=T)
+        compare(w, g, [0, 13, 31], u, max_near=1)

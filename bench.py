@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--spec", type=int, default=0, help="speculative expansions per step (0=default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="skip the Domino chain-decoding leg")
     ap.add_argument("--no-marginal", action="store_true",
                     help="skip the marginal-score (W2 = 0 ablation) leg")
     ap.add_argument("--flags", type=int, default=0,
@@ -237,6 +239,59 @@ def marginal_leg(wl, dt, torch, dev, flush, st, K, Wm, inp):
             "ok": bool((out["status"] == 0).all().item())}
 
 
+def chain_leg(wl, W, dt, torch, dev, flush, st, K, Wm, inp, greedy):
+    """Domino chain decoding (dt_decode_chains) on the same workload: D draft
+    tokens per request with the correction over the whole vocabulary, sampled
+    at the workload's temperatures with seeded uniform draws, or greedy.
+    Device-timed per round (L2 flushed before each); block 0's phase split."""
+    import numpy as np
+    dec = dt.ChainDecoder(dt.dims_of(wl.V, wl.d, wl.d_s, wl.r, wl.D, wl.M, wl.k, wl.N, wl.batch),
+                          TreeWeights.get(), device=dev)
+    u = torch.from_numpy(W.chain_uniforms(wl.batch, wl.D, seed=3)).to(dev)
+    T = torch.zeros_like(inp["temperature"]) if greedy else inp["temperature"]
+    out = dec.alloc_outputs()
+    run = lambda: dec.run(inp["base_logits"], inp["H"], inp["state0"], inp["anchor_tok"], T, u,
+                          out=out)
+    for _ in range(Wm):
+        flush.fill_(1)
+        run()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xff)
+        ev[i][0].record(st)
+        run()
+        ev[i][1].record(st)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    # block 0's phase times of the last round (the control block is zeroed per call)
+    t_ns = dec.workspace[32:32 + 8 * 4].view(torch.int64).cpu().tolist()
+    split = {k: v / 1000.0 for k, v in zip(["state_gemm", "vocab_gemm", "token_and_gru",
+                                            "barriers"], t_ns)}
+    flops = 2.0 * wl.V * wl.r * wl.batch * wl.D        # useful W2 h products of one round
+    pk = peaks()
+    vocab_s = split["vocab_gemm"] * 1e-6 if split["vocab_gemm"] > 0 else None
+    return {"us_per_round": 1000.0 * ms, "chains_per_s": wl.batch / (ms * 1e-3),
+            "draft_tokens_per_s": wl.batch * wl.D / (ms * 1e-3),
+            "block0_us_per_round": split,
+            "vocab_gemm_useful_tflops": (flops / vocab_s / 1e12) if vocab_s else None,
+            "base_logit_gbs": wl.base_logits.nbytes / (ms * 1e-3) / 1e9,
+            "base_logit_hbm_frac": wl.base_logits.nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "kernel_launches_per_round": dt.chain_kernel_launches(dec.dims),
+            "ok": bool((out["status"] == 0).all().item()),
+            "sampling": "greedy (T = 0)" if greedy else "inverse CDF at the workload's T"}
+
+
+class TreeWeights:
+    """The device weights of the main leg, shared with the chain leg."""
+    w = None
+
+    @classmethod
+    def get(cls):
+        return cls.w
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -265,6 +320,7 @@ def main():
 
     t0 = time.perf_counter()
     tb = dt.TreeBuilder.from_numpy(wl, spec_width=args.spec, device=dev, flags=args.flags)
+    TreeWeights.w = tb.w
     torch.cuda.synchronize()
     prep = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     prep[0].record()
@@ -336,6 +392,10 @@ def main():
     marginal = None
     if not args.no_marginal:
         marginal = marginal_leg(wl, dt, torch, dev, flush, st, K, Wm, inp)
+    chain = None
+    if not args.no_chain:
+        chain = {"sampled": chain_leg(wl, W, dt, torch, dev, flush, st, K, Wm, inp, False),
+                 "greedy": chain_leg(wl, W, dt, torch, dev, flush, st, K, Wm, inp, True)}
     if rank == 0:
         o = {k: v.cpu().numpy() for k, v in out.items() if v is not None}
         cnt = algorithmic_counts(wl, o["tokens"], o["depths"])
@@ -372,6 +432,7 @@ def main():
                        "search_block0_gemm_issuer_cycles": gemm_cycles,
                        "roofline_topm": roof_topm,
                        "marginal_mode": marginal,
+                       "chain_decoding": chain,
                        "round_algorithmic_bytes": round_bytes,
                        "round_hbm_frac": round_bytes / (total_ms / K * 1e-3) / 1e9 / pk["hbm_gbs"],
                        "peaks": pk["source"], "wall_s": wall},

@@ -56,6 +56,7 @@ constexpr int kRangeK = 256;                        // K columns of one state-GE
 constexpr int kMaxBpad = 80;                        // 3 terms x 80 = 240 accumulator columns
 constexpr uint32_t kAccCols = 256;                  // TMEM columns per accumulator
 constexpr uint64_t kLimitNs = 2000000000ull;        // 2 s per wait
+constexpr int kKzBatch = 8;                         // K-range partials loaded together
 
 struct DecodeParams {
   int V, d, d_s, r, D;
@@ -185,20 +186,32 @@ __device__ bool state_gemm(const DecodeParams &p, unsigned char *ring, unsigned 
     const int kz = it / p.n_tA, t = it - kz * p.n_tA;
     // B: the states' K range [256 kz, 256 kz + 256), zero past d_s and nb
     if (threadIdx.x < kWork) {
-      for (int u = threadIdx.x; u < p.bpad * (kRangeK / 8); u += kWork) {
-        const int b = u / (kRangeK / 8), kg = u - b * (kRangeK / 8);
-        const int k0 = kz * kRangeK + kg * 8;
-        float v[8];
-        if (b < p.nb && k0 < p.d_s) {
-          const float4 *src = reinterpret_cast<const float4 *>(p.S + static_cast<size_t>(b) * p.d_s + k0);
-          const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
-          v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
-          v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
-        } else {
+      constexpr int kU = 4;   // units of 8 K values per thread with loads in flight together
+      const int units = p.bpad * (kRangeK / 8);
+      for (int u0 = threadIdx.x; u0 < units; u0 += kU * kWork) {
+        float4 x[kU][2];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+        for (int j = 0; j < kU; ++j) {
+          const int u = u0 + j * kWork;
+          const int b = u / (kRangeK / 8), kg = u - b * (kRangeK / 8);
+          const int k0 = kz * kRangeK + kg * 8;
+          x[j][0] = x[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (u < units && b < p.nb && k0 < p.d_s) {
+            const float4 *src =
+                reinterpret_cast<const float4 *>(p.S + static_cast<size_t>(b) * p.d_s + k0);
+            x[j][0] = __ldcg(src);
+            x[j][1] = __ldcg(src + 1);
+          }
         }
-        put_b8(sB, p, b, kg, v);
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+          const int u = u0 + j * kWork;
+          if (u >= units) break;
+          const int b = u / (kRangeK / 8), kg = u - b * (kRangeK / 8);
+          const float v[8] = {x[j][0].x, x[j][0].y, x[j][0].z, x[j][0].w,
+                              x[j][1].x, x[j][1].y, x[j][1].z, x[j][1].w};
+          put_b8(sB, p, b, kg, v);
+        }
       }
     }
     fence_async_smem();
@@ -249,14 +262,36 @@ __device__ bool vocab_gemm(const DecodeParams &p, int i, unsigned char *ring, un
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] = 0.0f;
       if (b < p.nb && k0 < p.r) {
-        const float *U = p.U + (static_cast<size_t>(p.b0 + b) * p.D + i) * p.r + k0;
+        const float4 *U = reinterpret_cast<const float4 *>(
+            p.U + (static_cast<size_t>(p.b0 + b) * p.D + i) * p.r + k0);
+        float acc[8];
+        const float4 u0 = __ldg(U), u1 = __ldg(U + 1);
+        acc[0] = u0.x; acc[1] = u0.y; acc[2] = u0.z; acc[3] = u0.w;
+        acc[4] = u1.x; acc[5] = u1.y; acc[6] = u1.z; acc[7] = u1.w;
+        // W1_S S: the K-range partial sums, in K-range order (kKzBatch loads in flight)
+        float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int kz0 = 0; kz0 < p.n_kz; kz0 += kKzBatch) {
+          float4 q[kKzBatch][2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float s = 0.0f;
-          for (int kz = 0; kz < p.n_kz; ++kz)
-            s += __ldcg(p.ypart + (static_cast<size_t>(kz) * p.bpad + b) * p.R + 3 * p.d_s + k0 + j);
-          v[j] = siluf_(__ldg(U + j) + s);
+          for (int z = 0; z < kKzBatch; ++z) {
+            if (kz0 + z < p.n_kz) {
+              const float4 *src = reinterpret_cast<const float4 *>(
+                  p.ypart + (static_cast<size_t>(kz0 + z) * p.bpad + b) * p.R + 3 * p.d_s + k0);
+              q[z][0] = __ldcg(src);
+              q[z][1] = __ldcg(src + 1);
+            } else {
+              q[z][0] = q[z][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+#pragma unroll
+          for (int z = 0; z < kKzBatch; ++z) {
+            if (kz0 + z >= p.n_kz) break;
+            s[0] += q[z][0].x; s[1] += q[z][0].y; s[2] += q[z][0].z; s[3] += q[z][0].w;
+            s[4] += q[z][1].x; s[5] += q[z][1].y; s[6] += q[z][1].z; s[7] += q[z][1].w;
+          }
         }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = siluf_(acc[j] + s[j]);
       }
       put_b8(sB, p, b, kg, v);
     }
@@ -265,29 +300,52 @@ __device__ bool vocab_gemm(const DecodeParams &p, int i, unsigned char *ring, un
   __syncthreads();
   bool ok = true;
   const float ninf = -__int_as_float(0x7f800000);
+  // Each work warp owns 32 tokens of a tile (its TMEM lane quarter) and half
+  // of the requests. The base logits of a tile's requests are loaded together,
+  // one tile ahead, so that their HBM latency overlaps the previous tile.
+  constexpr int kHalf = kMaxBpad / 2;
+  const int quarter = warp & 3, half = warp >> 2, hb = p.bpad >> 1;
+  const int my0 = half * hb;
+  const int myn = max(0, min(hb, p.nb - my0));
+  float pre[kHalf];
+  auto load_base = [&](int tt) {
+    const int v = tt * 128 + quarter * 32 + lane;
+    const bool in = v < p.V;
+    const float *src = p.base + (static_cast<size_t>(p.b0 + my0) * p.D + i) * p.V + v;
+    const size_t step = static_cast<size_t>(p.D) * p.V;
+#pragma unroll
+    for (int j = 0; j < kHalf; ++j)
+      pre[j] = (in && j < myn) ? __ldcs(src + j * step) : 0.0f;
+  };
+  if (threadIdx.x < kWork && blockIdx.x < p.n_tV) load_base(blockIdx.x);
   for (int t = blockIdx.x; t < p.n_tV; t += gridDim.x) {
     issue_item(p, p.w2 + static_cast<size_t>(t) * p.nchV * kChunkBytes, p.nchV, ring,
                smem_u32(sB), full, empty, accf, acce, tmem, pp, s_fail);
     if (threadIdx.x < kWork) {
       ok &= wait_acc(accf, pp);
-      const int quarter = warp & 3, half = warp >> 2, hb = p.bpad >> 1;
+      float cur[kHalf];
+#pragma unroll
+      for (int j = 0; j < kHalf; ++j) cur[j] = pre[j];
+      if (t + static_cast<int>(gridDim.x) < p.n_tV) load_base(t + gridDim.x);
       const int v = t * 128 + quarter * 32 + lane;
       const int grp = t * 4 + quarter;
       const bool valid = v < p.V;
       const uint32_t ta = tmem + ((quarter * 32u) << 16) + (pp.q & 1u) * kAccCols;
-      for (int b0 = half * hb; b0 < (half + 1) * hb && b0 < p.nb; b0 += 8) {
+#pragma unroll
+      for (int c = 0; c < kHalf; c += 8) {
+        if (c >= myn) break;
         float a[8], m[8], l[8];
-        tmem_ld8(ta + b0, a);
-        tmem_ld8(ta + p.bpad + b0, m);
-        tmem_ld8(ta + 2 * p.bpad + b0, l);
+        tmem_ld8(ta + my0 + c, a);
+        tmem_ld8(ta + p.bpad + my0 + c, m);
+        tmem_ld8(ta + 2 * p.bpad + my0 + c, l);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int b = b0 + j;
-          if (b >= p.nb) break;
+          if (c + j >= myn) break;
+          const int b = my0 + c + j;
           float x = ninf;
           if (valid) {
-            const float bv = __ldcs(p.base + (static_cast<size_t>(p.b0 + b) * p.D + i) * p.V + v);
+            const float bv = cur[c + j];
             if (bv != bv || bv == __int_as_float(0x7f800000)) atomicOr(&p.flags[b], 1);
             x = __fdiv_rn(bv + ((a[j] + m[j]) + l[j]), s_T[b]);
             __stcs(p.X + static_cast<size_t>(b) * p.n_tV * 128 + v, x);
@@ -320,20 +378,33 @@ __device__ void gru_request(const DecodeParams &p, int b, int tok) {
   const int ds = p.d_s;
   const float *gi = p.G + static_cast<size_t>(tok) * 3 * ds;
   for (int k = threadIdx.x; k < ds; k += kWork) {
-    float gh[3];
+    const float gir = __ldg(gi + k), giz = __ldg(gi + ds + k), gin = __ldg(gi + 2 * ds + k);
+    float *sp = p.S + static_cast<size_t>(b) * ds + k;
+    const float old = __ldcg(sp);
+    float gh[3] = {0.f, 0.f, 0.f};
+    // the K-range partial sums of the three gates, in K-range order
+    for (int kz0 = 0; kz0 < p.n_kz; kz0 += kKzBatch) {
+      float q[kKzBatch][3];
 #pragma unroll
-    for (int g = 0; g < 3; ++g) {
-      float s = 0.0f;
-      for (int kz = 0; kz < p.n_kz; ++kz)
-        s += __ldcg(p.ypart + (static_cast<size_t>(kz) * p.bpad + b) * p.R + g * ds + k);
-      gh[g] = s + (p.b_hh ? p.b_hh[g * ds + k] : 0.0f);
+      for (int z = 0; z < kKzBatch; ++z)
+#pragma unroll
+        for (int g = 0; g < 3; ++g)
+          q[z][g] = kz0 + z < p.n_kz
+                        ? __ldcg(p.ypart + (static_cast<size_t>(kz0 + z) * p.bpad + b) * p.R + g * ds + k)
+                        : 0.0f;
+#pragma unroll
+      for (int z = 0; z < kKzBatch; ++z) {
+        if (kz0 + z >= p.n_kz) break;
+#pragma unroll
+        for (int g = 0; g < 3; ++g) gh[g] += q[z][g];
+      }
     }
-    const float rr = sigmoidf_(__ldg(gi + k) + gh[0]);
-    const float z = sigmoidf_(__ldg(gi + ds + k) + gh[1]);
-    const float n = tanhf(__ldg(gi + 2 * ds + k) + rr * gh[2]);
-    float *s = p.S + static_cast<size_t>(b) * ds + k;
-    const float old = __ldcg(s);
-    __stcg(s, (1.0f - z) * n + z * old);
+#pragma unroll
+    for (int g = 0; g < 3; ++g) gh[g] += p.b_hh ? p.b_hh[g * ds + k] : 0.0f;
+    const float rr = sigmoidf_(gir + gh[0]);
+    const float z = sigmoidf_(giz + gh[1]);
+    const float n = tanhf(gin + rr * gh[2]);
+    __stcg(sp, (1.0f - z) * n + z * old);
   }
 }
 
@@ -353,12 +424,23 @@ __device__ void choose_token(const DecodeParams &p, int i, int b) {
   const int cpt = (p.Gn + kWork - 1) / kWork;
   const int g0 = work ? min(p.Gn, tid * cpt) : p.Gn, g1 = min(p.Gn, g0 + cpt);
   // 1. maximum, its first group, the last group with mass
+  // a thread's group records are loaded kG at a time, all in flight together
+  constexpr int kG = 24;
   float mt = ninf;
   int gt = 0x7fffffff, lastpos = -1;
-  for (int g = g0; g < g1; ++g) {
-    const float v = __ldcg(m + g);
-    if (gt == 0x7fffffff || v > mt) { mt = v; gt = g; }   // first group of the maximum
-    if (__ldcg(sg + g) > 0.0f) lastpos = g;
+  for (int gb0 = g0; gb0 < g1; gb0 += kG) {
+    float mv[kG], sv[kG];
+#pragma unroll
+    for (int j = 0; j < kG; ++j) {
+      mv[j] = gb0 + j < g1 ? __ldcg(m + gb0 + j) : ninf;
+      sv[j] = gb0 + j < g1 ? __ldcg(sg + gb0 + j) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < kG; ++j) {
+      if (gb0 + j >= g1) break;
+      if (gt == 0x7fffffff || mv[j] > mt) { mt = mv[j]; gt = gb0 + j; }   // first group of the maximum
+      if (sv[j] > 0.0f) lastpos = gb0 + j;
+    }
   }
   // reduce (max, first group) and last positive group over the block
   for (int o = 16; o; o >>= 1) {
@@ -386,9 +468,16 @@ __device__ void choose_token(const DecodeParams &p, int i, int b) {
   // 2. Z = sum over groups of s_g e^{m_g - M}, per thread then over the block
   float zt = 0.0f;
   if (M != ninf)
-    for (int g = g0; g < g1; ++g) {
-      const float mg = __ldcg(m + g);
-      if (mg != ninf) zt += __ldcg(sg + g) * expf(mg - M);
+    for (int gb0 = g0; gb0 < g1; gb0 += kG) {
+      float mv[kG], sv[kG];
+#pragma unroll
+      for (int j = 0; j < kG; ++j) {
+        mv[j] = gb0 + j < g1 ? __ldcg(m + gb0 + j) : ninf;
+        sv[j] = gb0 + j < g1 ? __ldcg(sg + gb0 + j) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kG; ++j)
+        if (mv[j] != ninf) zt += sv[j] * expf(mv[j] - M);
     }
   // exclusive scan of the thread sums (id order) and the total
   float incl = zt;
@@ -427,11 +516,21 @@ __device__ void choose_token(const DecodeParams &p, int i, int b) {
     if (tid == s_i[2]) {
       float cum = P;
       int gsel = -1;
-      for (int g = g0; g < g1; ++g) {
-        const float mg = __ldcg(m + g);
-        const float w = (mg == ninf) ? 0.0f : __ldcg(sg + g) * expf(mg - M);
-        if (cum + w > target) { gsel = g; break; }
-        cum += w;
+      for (int gb0 = g0; gb0 < g1 && gsel < 0; gb0 += kG) {
+        float mv[kG], sv[kG];
+#pragma unroll
+        for (int j = 0; j < kG; ++j) {
+          mv[j] = gb0 + j < g1 ? __ldcg(m + gb0 + j) : ninf;
+          sv[j] = gb0 + j < g1 ? __ldcg(sg + gb0 + j) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kG; ++j) {
+          const float w = (mv[j] == ninf) ? 0.0f : sv[j] * expf(mv[j] - M);
+          if (gsel < 0 && gb0 + j < g1) {
+            if (cum + w > target) gsel = gb0 + j;
+            else cum += w;
+          }
+        }
       }
       s_i[3] = gsel >= 0 ? gsel : glast;
       s_f[1] = gsel >= 0 ? cum : __int_as_float(0x7f800000);   // +inf: take the last token with mass

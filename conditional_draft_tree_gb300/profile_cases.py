@@ -9,6 +9,10 @@
         R whole dt_build_trees rounds of the workload (weights, prepared table
         and workspace on the device: about 3.5 GB for the default workload);
         F = dt_options flags (default 0).
+    python -m conditional_draft_tree_gb300.profile_cases chain [--reps R] [--cfg C] [--greedy]
+        R Domino chain-decoding rounds (dt_decode_chains) of the workload,
+        sampled at its temperatures with seeded uniform draws, or greedy: one
+        projection launch and one decoding launch per round.
 
 Each case does one untimed launch first, then R timed ones (CUDA events on the
 current stream, L2 flushed by a 256 MB write before each), and prints one line
@@ -69,9 +73,24 @@ def case_round(cfg, reps, dev, flags=0):
           f"trees/s={wl.batch / (ms * 1e-3):.0f}")
 
 
+def case_chain(cfg, reps, dev, greedy=False):
+    wl = W.make_workload(cfg)
+    dec = dt.ChainDecoder.from_numpy(wl, device=dev)
+    inp = dec.inputs_to_device(wl, W.chain_uniforms(wl.batch, wl.D, seed=cfg))
+    if greedy:
+        inp["temperature"] = torch.zeros_like(inp["temperature"])
+    out = dec.alloc_outputs()
+    ms = _timed(lambda: dec.run(**inp, out=out), reps, dev)
+    if not bool((out["status"] == 0).all()):
+        raise dt.DtError("chain decoding reported a non-OK status")
+    print(f"chain {wl.name}: batch={wl.batch} D={wl.D} mean_us={1000 * ms:.1f} "
+          f"chains/s={wl.batch / (ms * 1e-3):.0f}")
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["topm", "round"])
+    ap.add_argument("case", choices=["topm", "round", "chain"])
+    ap.add_argument("--greedy", action="store_true")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--cfg", type=int, default=3)
     ap.add_argument("--flags", type=int, default=0)
@@ -81,6 +100,8 @@ def main():
     build.build()
     if args.case == "round":
         case_round(args.cfg, args.reps, dev, args.flags)
+    elif args.case == "chain":
+        case_chain(args.cfg, args.reps, dev, args.greedy)
     else:
         case_topm(args.cfg, args.reps, dev)
 

@@ -79,3 +79,52 @@ def test_package_refuses_to_run_without_library(dt, monkeypatch, tmp_path):
     monkeypatch.setattr(dt, "_lib", None)
     with pytest.raises(dt.DtError):
         dt.lib()
+
+
+def _no_gpu():
+    import torch
+    return not torch.cuda.is_available()
+
+
+@pytest.mark.skipif(not _no_gpu(), reason="passes unusable pointers; host-only check")
+def test_marginal_mode_reads_no_weights(dt):
+    """DT_OPT_MARGINAL reads no weights, prepared table, H or state0: NULL passes
+    the argument checks (the call then stops at the device query on a host
+    without a GPU); without the flag the same call is an invalid argument."""
+    dims = dt.dims_of(V=1024, d=64, d_s=32, r=32, D=7, M=16, k=4, N=32, batch=1)
+    out = dt.DtTreeOut(16, 16, 16, 16, None, None, 16)
+    opt = dt.options(0, flags=dt.OPT_MARGINAL)
+    call = lambda o: dt.lib().dt_build_trees(C.byref(dims), None, None, 256, None, None, 256, None,
+                                             256, 1 << 20, C.byref(out), o, None)
+    assert call(None) == dt.ERR_INVALID_ARG
+    assert call(C.byref(opt)) in (dt.ERR_CUDA, dt.ERR_UNSUPPORTED)
+
+
+def test_chain_entry_points_validate_before_device_work(dt):
+    L = dt.lib()
+    dims = dt.dims_of(V=151936, d=4096, d_s=1024, r=256, D=15, M=64, k=8, N=64, batch=32)
+    # tiles of 128 rows x 64-wide K chunks, 16 KB each: [W_hh; W1_S] (3328 rows, K 1024)
+    # and W2 (151936 rows, K 256)
+    assert dt.chain_prepared_bytes(dims) == (26 * 16 + 1187 * 4) * 16384
+    bad = dt.dims_of(V=1024, d=64, d_s=32, r=7, D=7, M=16, k=4, N=32, batch=1)
+    assert dt.chain_prepared_bytes(bad) == 0
+    w32 = dt.DtWeights(16, 16, 16, None, None, 16, 16, 0)
+    w16 = dt.DtWeights(16, 16, 16, None, None, 16, 16, 1)
+    assert L.dt_prepare_chain(C.byref(dims), C.byref(w32), 256, 1 << 30, None) == \
+        dt.ERR_UNSUPPORTED
+    assert L.dt_prepare_chain(C.byref(dims), C.byref(w16), 256, 16, None) == dt.ERR_INVALID_ARG
+    # prepared, chain_prepared, base, H, state0, anchor, temperature, uniforms, workspace,
+    # workspace_bytes, tokens, logprobs, status, stream
+    args = [256, 256, 256, 256, 256, 256, None, None, 256, 1 << 30, 256, 256, 256, None]
+    assert len(args) == len(L.dt_decode_chains.argtypes) - 2
+
+    def decode(w, **over):
+        a = list(args)
+        for i, v in over.items():
+            a[int(i[1:])] = v
+        return L.dt_decode_chains(C.byref(dims), C.byref(w), *a)
+    assert decode(w32) == dt.ERR_UNSUPPORTED              # f32 weights
+    assert decode(w16, a2=None) == dt.ERR_INVALID_ARG      # no base logits
+    assert decode(w16, a10=None) == dt.ERR_INVALID_ARG     # no token output
+    assert decode(w16, a8=255) == dt.ERR_INVALID_ARG       # misaligned workspace
+    assert decode(w16, a3=258) == dt.ERR_INVALID_ARG       # H not 16-byte aligned

@@ -228,3 +228,56 @@ def chains(w, requests=None, uniforms=None, forced=None, *, threads: int | None 
         return [run(b) for b in reqs]
     with ThreadPoolExecutor(max_workers=threads) as ex:
         return list(ex.map(run, reqs))
+
+
+# ------------------------------------------------ verify-side consumption
+# "Riassunto Tecnico: DominoTree", Componenti Core 5: the target model checks
+# every drafted node in one forward pass with tree attention, each node seeing
+# the verified prefix and its own ancestors (the ancestor mask of the tree).
+
+def tree_positions(depths: np.ndarray, prefix_len: np.ndarray) -> np.ndarray:
+    """Position ids of the tree rows. The prefix cache holds the prefix_len[b]
+    tokens before the anchor (positions 0 .. prefix_len - 1); the anchor is
+    tree row 0 at position prefix_len and a node at depth j sits j places
+    after it: prefix_len[b] + depth. Empty rows (depth -1) get -1."""
+    depths = np.asarray(depths)
+    out = np.full(depths.shape, -1, dtype=np.int32)
+    for b in range(depths.shape[0]):
+        for i in range(depths.shape[1]):
+            if depths[b, i] >= 0:
+                out[b, i] = int(prefix_len[b]) + int(depths[b, i])
+    return out
+
+
+def tree_attention(q, k, v, mask, prefix_len, scale) -> np.ndarray:
+    """Attention of the tree rows, in fp64, written from the definition.
+
+    q [batch][H][N1][dh], k and v [batch][Hkv][P + N1][dh] (the first P keys
+    are the prefix cache, key P + t is tree row t), mask [batch][N1][N1] (row i
+    may see tree row t iff mask[i][t]), prefix_len [batch] (prefix keys
+    p < prefix_len[b] are visible to every row; the rest are padding). Query
+    head h reads key/value head h // (H / Hkv). For row i of head h:
+        s_j = scale * q_i . k_j   over the visible keys j
+        out_i = sum_j softmax(s)_j v_j,   0 when no key is visible.
+    Returns float64 [batch][H][N1][dh]."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, N1, dh = q.shape
+    Hkv, L = k.shape[1], k.shape[2]
+    P = L - N1
+    group = H // Hkv
+    out = np.zeros((B, H, N1, dh))
+    for b in range(B):
+        for h in range(H):
+            kh, vh = k[b, h // group], v[b, h // group]
+            for i in range(N1):
+                vis = [j for j in range(int(prefix_len[b]))] + \
+                      [P + t for t in range(N1) if mask[b, i, t]]
+                if not vis:
+                    continue
+                s = np.array([scale * np.dot(q[b, h, i], kh[j]) for j in vis])
+                w = np.exp(s - s.max())
+                w /= w.sum()
+                out[b, h, i] = sum(w[n] * vh[j] for n, j in enumerate(vis))
+    return out

@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--spec", type=int, default=0, help="speculative expansions per step (0=default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
+    ap.add_argument("--no-verify", action="store_true",
+                    help="skip the verify-side tree-attention leg")
     ap.add_argument("--no-chain", action="store_true",
                     help="skip the Domino chain-decoding leg")
     ap.add_argument("--no-marginal", action="store_true",
@@ -283,6 +285,40 @@ def chain_leg(wl, W, dt, torch, dev, flush, st, K, Wm, inp, greedy):
             "sampling": "greedy (T = 0)" if greedy else "inverse CDF at the workload's T"}
 
 
+def verify_leg(W, dt, torch, np, dev, flush, st, K, Wm, mask):
+    """Verify-side tree attention (dt_tree_attention) over the trees of the main
+    leg: Qwen3-8B attention shape (32 query heads, 8 key/value heads, dh 128),
+    one layer, prefix cache padded to 1024 keys with lengths in [512, 1024],
+    synthetic bf16 Q/K/V. Device-timed per call, L2 flushed before each."""
+    B, n1 = mask.shape[0], mask.shape[1]
+    H, Hkv, P, dh = 32, 8, 1024, 128
+    q, k, v, plen = W.verify_inputs(B, H, Hkv, n1, P, dh, seed=3, min_prefix=512)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+    qd, kd, vd, pd = t(q), t(k), t(v), torch.from_numpy(plen).to(dev)
+    out = torch.empty((B, H, n1, dh), dtype=torch.float32, device=dev)
+    for _ in range(Wm):
+        flush.fill_(1)
+        dt.tree_attention(qd, kd, vd, mask, pd, out=out)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xff)
+        ev[i][0].record(st)
+        dt.tree_attention(qd, kd, vd, mask, pd, out=out)
+        ev[i][1].record(st)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    seen = mask.to(torch.int64).sum(-1).cpu().numpy() + plen[:, None]   # visible keys per row
+    flops = 4.0 * dh * H * float(seen.sum())           # q.k and p.v, 2 flops per product
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12                # FP32 FMA lanes x clock (alu bound)
+    ach = flops / (ms * 1e-3) / 1e12
+    return {"us_per_layer": 1000.0 * ms, "shape": f"batch {B}, H {H}, Hkv {Hkv}, n1 {n1}, "
+            f"prefix <= {P}, dh {dh}", "roofline": {"bound": "alu", "achieved": ach, "peak": peak,
+            "unit": "TFLOP/s", "frac": ach / peak, "peak_kind": "FP32 FMA, 152 SMs x 128 lanes x "
+            "2.07 GHz"}, "finite": bool(torch.isfinite(out).all().item())}
+
+
 class TreeWeights:
     """The device weights of the main leg, shared with the chain leg."""
     w = None
@@ -392,6 +428,9 @@ def main():
     marginal = None
     if not args.no_marginal:
         marginal = marginal_leg(wl, dt, torch, dev, flush, st, K, Wm, inp)
+    verify = None
+    if not args.no_verify:
+        verify = verify_leg(W, dt, torch, np, dev, flush, st, K, Wm, out["mask"])
     chain = None
     if not args.no_chain:
         chain = {"sampled": chain_leg(wl, W, dt, torch, dev, flush, st, K, Wm, inp, False),
@@ -433,6 +472,7 @@ def main():
                        "roofline_topm": roof_topm,
                        "marginal_mode": marginal,
                        "chain_decoding": chain,
+                       "verify_tree_attention": verify,
                        "round_algorithmic_bytes": round_bytes,
                        "round_hbm_frac": round_bytes / (total_ms / K * 1e-3) / 1e9 / pk["hbm_gbs"],
                        "peaks": pk["source"], "wall_s": wall},

@@ -31,7 +31,8 @@ EXPORTS = ("dt_abi_version", "dt_status_string", "dt_prepared_bytes", "dt_prepar
            "dt_workspace_bytes", "dt_build_trees", "dt_host_workspace_bytes",
            "dt_build_trees_host", "dt_select_topm_noalloc", "dt_kernel_launches",
            "dt_chain_prepared_bytes", "dt_prepare_chain", "dt_chain_workspace_bytes",
-           "dt_chain_kernel_launches", "dt_decode_chains")
+           "dt_chain_kernel_launches", "dt_decode_chains", "dt_tree_positions",
+           "dt_tree_attention")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -99,6 +100,10 @@ def lib():
         L.dt_chain_kernel_launches.argtypes = [C.POINTER(DtDims)]
         L.dt_decode_chains.argtypes = [C.POINTER(DtDims), C.POINTER(DtWeights)] + \
             [C.c_void_p] * 9 + [C.c_size_t] + [C.c_void_p] * 4
+        L.dt_tree_positions.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p,
+                                        C.c_void_p]
+        L.dt_tree_attention.argtypes = [C.c_void_p] * 5 + [C.c_int] * 6 + [C.c_float, C.c_void_p,
+                                                                          C.c_void_p]
         _lib = L
     return _lib
 
@@ -423,3 +428,33 @@ class ChainDecoder:
         if uniforms is not None:
             d["uniforms"] = f(uniforms, np.float32)
         return d
+
+
+
+# ------------------------------------------------ verify-side consumption
+
+def tree_positions(depths, prefix_len, out=None, stream=None):
+    """dt_tree_positions on device tensors: depths [batch][n1] int32, prefix_len
+    [batch] int32 -> position ids [batch][n1] int32."""
+    batch, n1 = depths.shape
+    if out is None:
+        out = torch.empty_like(depths)
+    _check(lib().dt_tree_positions(_ptr(depths), _ptr(prefix_len), batch, n1, _ptr(out),
+                                   _stream(stream)), "dt_tree_positions")
+    return out
+
+
+def tree_attention(q, k, v, mask, prefix_len, scale=None, out=None, stream=None):
+    """dt_tree_attention on device tensors: q [batch][H][n1][dh], k and v
+    [batch][Hkv][P + n1][dh] (bf16, or int16/uint16 holding bf16 bits), mask
+    [batch][n1][n1] uint8, prefix_len [batch] int32 -> fp32 [batch][H][n1][dh]."""
+    batch, H, n1, dh = q.shape
+    Hkv, L = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = dh ** -0.5
+    if out is None:
+        out = torch.empty((batch, H, n1, dh), dtype=torch.float32, device=q.device)
+    _check(lib().dt_tree_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(prefix_len), batch,
+                                   H, Hkv, n1, L - n1, dh, float(scale), _ptr(out),
+                                   _stream(stream)), "dt_tree_attention")
+    return out

@@ -26,12 +26,13 @@ import dataclasses
 import numpy as np
 
 __all__ = ["Workload", "CONFIGS", "make_workload", "custom_workload", "f32_to_bf16_bits",
-           "bf16_bits_to_f32", "chain_uniforms"]
+           "bf16_bits_to_f32", "chain_uniforms", "verify_inputs"]
 
 # Index of each tensor's child seed. Fixed forever: changing it changes every input.
 _SEED_SLOTS = {
     "base": 0, "spikes": 1, "H": 2, "E": 3, "W_ih": 4, "W_hh": 5, "W1": 6, "W2": 7,
     "anchor": 8, "zipf_s": 9, "state0": 10, "b_ih": 11, "b_hh": 12, "chain_u": 13,
+    "verify": 14,
 }
 _N_SLOTS = 16
 
@@ -214,3 +215,19 @@ def chain_uniforms(batch: int, D: int, seed: int = 0) -> np.ndarray:
     stream, so they never change another tensor of the same seed."""
     kid = np.random.SeedSequence(seed).spawn(_N_SLOTS)[_SEED_SLOTS["chain_u"]]
     return np.random.default_rng(kid).random((batch, D), dtype=np.float32)
+
+
+def verify_inputs(batch: int, H: int, Hkv: int, n1: int, P: int, dh: int, seed: int = 0,
+                  min_prefix: int = 0):
+    """Synthetic per-layer tensors of the target model for tree verification:
+    q [batch][H][n1][dh], k and v [batch][Hkv][P + n1][dh] as bf16 bits
+    (uint16, N(0, 1) values rounded to bf16), and prefix lengths [batch] int32
+    uniform in [min_prefix, P] (the cache is padded to P keys). The target model
+    itself is not available; these stand in for its projections."""
+    kid = np.random.SeedSequence(seed).spawn(_N_SLOTS)[_SEED_SLOTS["verify"]]
+    rng = np.random.default_rng(kid)
+    q = f32_to_bf16_bits(rng.standard_normal((batch, H, n1, dh), dtype=np.float32))
+    k = f32_to_bf16_bits(rng.standard_normal((batch, Hkv, P + n1, dh), dtype=np.float32))
+    v = f32_to_bf16_bits(rng.standard_normal((batch, Hkv, P + n1, dh), dtype=np.float32))
+    plen = rng.integers(min_prefix, P + 1, batch).astype(np.int32)
+    return q, k, v, plen

@@ -268,6 +268,41 @@ int dt_decode_chains(const dt_dims *dims, const dt_weights *w, const void *prepa
                      const float *uniforms, void *workspace, size_t workspace_bytes,
                      int32_t *tokens, float *logprobs, int32_t *status, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Verify-side consumption of a tree ("Riassunto Tecnico: DominoTree",
+ * Componenti Core 5: the target model checks every node in one pass with tree
+ * attention, each node seeing the verified prefix and its ancestors). The
+ * target model is not part of this library; these calls take its tensors.
+ *
+ * dt_tree_positions: position ids of the tree rows. The prefix cache holds the
+ * prefix_len[b] tokens before the anchor; the anchor (row 0) sits at position
+ * prefix_len[b] and a row of depth j at prefix_len[b] + j; rows with depth -1
+ * (empty) get -1.
+ *   depths     [batch][n1] int32 (dt_tree_out.depths), device
+ *   prefix_len [batch] int32, device
+ *   positions  [batch][n1] int32 output, device
+ *
+ * dt_tree_attention: one attention layer over the tree rows (device pointers):
+ *   q    [batch][H][n1][dh]        bf16 bits, 16-byte aligned
+ *   k, v [batch][Hkv][P + n1][dh]  bf16 bits: keys 0..P-1 are the prefix cache
+ *                                  (only p < prefix_len[b] are attended; the rest
+ *                                  is padding), key P + t is tree row t
+ *   mask [batch][n1][n1]           row i sees tree row t iff mask[i][t] != 0
+ *                                  (dt_tree_out.mask)
+ *   prefix_len [batch]             clamped into [0, P]
+ *   out  [batch][H][n1][dh]        fp32 output, 16-byte aligned:
+ *        out_i = sum_j softmax_j(scale q_i . k_j) v_j over the visible keys j,
+ *        0 for a row that sees no key
+ * Query head h reads key/value head h / (H / Hkv) (H % Hkv == 0). dh is 64, 128
+ * or 256; n1 <= DT_MAX_N + 1. fp32 arithmetic on the CUDA cores. Both calls
+ * return DT_ERR_INVALID_ARG for bad sizes or pointers and are asynchronous on
+ * `stream`. */
+int dt_tree_positions(const int32_t *depths, const int32_t *prefix_len, int batch, int n1,
+                      int32_t *positions, void *stream);
+int dt_tree_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const uint8_t *mask, const int32_t *prefix_len, int batch, int H, int Hkv,
+                      int n1, int P, int dh, float scale, float *out, void *stream);
+
 /* Static description of a status code. */
 const char *dt_status_string(int code);
 

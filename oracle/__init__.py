@@ -281,3 +281,40 @@ def tree_attention(q, k, v, mask, prefix_len, scale) -> np.ndarray:
                 w /= w.sum()
                 out[b, h, i] = sum(w[n] * vh[j] for n, j in enumerate(vis))
     return out
+
+
+# ------------------------------------------------- CondAdaptive budget
+# "Riassunto Tecnico: DominoTree", Componenti Core 4: a cost-aware adaptive
+# budget (CaDDTree's rule: stop growing the tree when the throughput gain
+# fades) tried on the conditional tree, found to saturate at the maximum budget.
+
+def adaptive_count(scores: np.ndarray, tokens: np.ndarray, c_fixed: float, c_node: float) -> int:
+    """Nodes kept by the cost-aware rule on one tree (rows in pop order, row 0
+    the root). Expected accepted length A(n) = 1 + sum_{i<=n} exp(score_i) (the
+    drafter's path probabilities), round cost C(n) = c_fixed + c_node n;
+    node n is kept while A(n) / C(n) > A(n - 1) / C(n - 1), i.e. while
+    exp(score_n) C(n - 1) > A(n - 1) c_node, all in fp64, in pop order; growth
+    stops at the first node that fails or at the first empty row."""
+    A, C, n_keep = 1.0, float(c_fixed), 0
+    for n in range(1, len(scores)):
+        if tokens[n] < 0:
+            break
+        e = float(np.exp(np.float64(scores[n])))
+        if e * C > A * float(c_node):
+            A += e
+            C += float(c_node)
+            n_keep = n
+        else:
+            break
+    return n_keep
+
+
+def truncate_tree(tree: dict, n_keep: int) -> dict:
+    """The tree cut to its first n_keep + 1 rows (a prefix of the pop order is
+    a subtree: every ancestor of a row has a lower index); later rows empty."""
+    out = {k: np.array(v, copy=True) for k, v in tree.items() if isinstance(v, np.ndarray)}
+    for key, fill in (("tokens", -1), ("parents", -1), ("depths", -1), ("scores", -np.inf)):
+        out[key][n_keep + 1:] = fill
+    if "mask" in out:
+        out["mask"][n_keep + 1:] = 0
+    return out

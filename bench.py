@@ -319,6 +319,26 @@ def verify_leg(W, dt, torch, np, dev, flush, st, K, Wm, mask):
             "2.07 GHz"}, "finite": bool(torch.isfinite(out).all().item())}
 
 
+def adaptive_leg(dt, torch, dev, st, K, out, N, c_fixed=1.0, c_node=1.0 / 256):
+    """CondAdaptive (dt_adaptive_budget) on copies of the main leg's trees: the
+    kept node counts under a round cost c_fixed + c_node n (a verification pass
+    whose cost grows by 1/256 of its fixed cost per tree node; the pages give no
+    cost figures) and how often the rule runs to the full budget."""
+    ms = []
+    for _ in range(K):
+        o = {k: (v.clone() if v is not None else None) for k, v in out.items()}
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        counts = dt.adaptive_budget(o, N, c_fixed, c_node)
+        b.record(st)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    c = counts.cpu()
+    return {"us_per_call": 1000.0 * statistics.mean(ms), "c_fixed": c_fixed, "c_node": c_node,
+            "mean_nodes_kept": float(c.float().mean()), "budget": N,
+            "share_at_full_budget": float((c == N).float().mean())}
+
+
 class TreeWeights:
     """The device weights of the main leg, shared with the chain leg."""
     w = None
@@ -428,6 +448,7 @@ def main():
     marginal = None
     if not args.no_marginal:
         marginal = marginal_leg(wl, dt, torch, dev, flush, st, K, Wm, inp)
+    adaptive = adaptive_leg(dt, torch, dev, st, K, out, wl.N)
     verify = None
     if not args.no_verify:
         verify = verify_leg(W, dt, torch, np, dev, flush, st, K, Wm, out["mask"])
@@ -473,6 +494,7 @@ def main():
                        "marginal_mode": marginal,
                        "chain_decoding": chain,
                        "verify_tree_attention": verify,
+                       "cond_adaptive": adaptive,
                        "round_algorithmic_bytes": round_bytes,
                        "round_hbm_frac": round_bytes / (total_ms / K * 1e-3) / 1e9 / pk["hbm_gbs"],
                        "peaks": pk["source"], "wall_s": wall},

@@ -32,7 +32,7 @@ EXPORTS = ("dt_abi_version", "dt_status_string", "dt_prepared_bytes", "dt_prepar
            "dt_build_trees_host", "dt_select_topm_noalloc", "dt_kernel_launches",
            "dt_chain_prepared_bytes", "dt_prepare_chain", "dt_chain_workspace_bytes",
            "dt_chain_kernel_launches", "dt_decode_chains", "dt_tree_positions",
-           "dt_tree_attention")
+           "dt_tree_attention", "dt_adaptive_budget")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -100,6 +100,8 @@ def lib():
         L.dt_chain_kernel_launches.argtypes = [C.POINTER(DtDims)]
         L.dt_decode_chains.argtypes = [C.POINTER(DtDims), C.POINTER(DtWeights)] + \
             [C.c_void_p] * 9 + [C.c_size_t] + [C.c_void_p] * 4
+        L.dt_adaptive_budget.argtypes = [C.POINTER(DtTreeOut), C.c_int, C.c_int, C.c_double,
+                                         C.c_double, C.c_void_p, C.c_void_p]
         L.dt_tree_positions.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p,
                                         C.c_void_p]
         L.dt_tree_attention.argtypes = [C.c_void_p] * 5 + [C.c_int] * 6 + [C.c_float, C.c_void_p,
@@ -458,3 +460,16 @@ def tree_attention(q, k, v, mask, prefix_len, scale=None, out=None, stream=None)
                                    H, Hkv, n1, L - n1, dh, float(scale), _ptr(out),
                                    _stream(stream)), "dt_tree_attention")
     return out
+
+
+
+def adaptive_budget(out: dict, N: int, c_fixed: float, c_node: float, counts=None, stream=None):
+    """dt_adaptive_budget: cut the trees of ``out`` (alloc_outputs layout, on
+    the device) in place by the cost-aware rule; returns counts [batch] int32."""
+    batch = out["tokens"].shape[0]
+    if counts is None:
+        counts = torch.empty(batch, dtype=torch.int32, device=out["tokens"].device)
+    o = _out_struct(out)
+    _check(lib().dt_adaptive_budget(C.byref(o), batch, int(N), float(c_fixed), float(c_node),
+                                    _ptr(counts), _stream(stream)), "dt_adaptive_budget")
+    return counts

@@ -303,6 +303,22 @@ int dt_tree_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       const uint8_t *mask, const int32_t *prefix_len, int batch, int H, int Hkv,
                       int n1, int P, int dh, float scale, float *out, void *stream);
 
+/* ------------------------------------------------------------------------
+ * CondAdaptive: the cost-aware adaptive node budget ("Riassunto Tecnico:
+ * DominoTree", Componenti Core 4, reported there as a negative result: with
+ * the corrected path probabilities the rule saturates at the maximum budget).
+ * Applied in place to the trees of a dt_build_trees call (device pointers of
+ * dt_tree_out; status is not read, mask may be NULL), N = the call's budget.
+ * Expected accepted length A(n) = 1 + sum_{i<=n} exp(score_i) over the rows in
+ * pop order, round cost C(n) = c_fixed + c_node n; row n is kept while
+ * A(n) / C(n) rises, i.e. while exp(score_n) C(n-1) > A(n-1) c_node (fp64, pop
+ * order), so the kept rows are a prefix of the tree (a subtree: every ancestor
+ * has a lower index). Later rows become empty (token, parent, depth -1, score
+ * -inf, mask rows 0); counts[b] = rows kept besides the root.
+ * c_fixed, c_node > 0 and finite, else DT_ERR_INVALID_ARG. Asynchronous. */
+int dt_adaptive_budget(const dt_tree_out *out, int batch, int N, double c_fixed, double c_node,
+                       int32_t *counts, void *stream);
+
 /* Static description of a status code. */
 const char *dt_status_string(int code);
 

@@ -128,3 +128,24 @@ def test_chain_entry_points_validate_before_device_work(dt):
     assert decode(w16, a10=None) == dt.ERR_INVALID_ARG     # no token output
     assert decode(w16, a8=255) == dt.ERR_INVALID_ARG       # misaligned workspace
     assert decode(w16, a3=258) == dt.ERR_INVALID_ARG       # H not 16-byte aligned
+
+
+def test_verify_and_adaptive_entry_points_validate_before_device_work(dt):
+    L = dt.lib()
+    # dt_tree_positions: sizes and pointers
+    assert L.dt_tree_positions(None, 256, 1, 65, 256, None) == dt.ERR_INVALID_ARG
+    assert L.dt_tree_positions(256, 256, 0, 65, 256, None) == dt.ERR_INVALID_ARG
+    assert L.dt_tree_positions(256, 256, 1, 2000, 256, None) == dt.ERR_INVALID_ARG
+    # dt_tree_attention: q k v mask prefix_len batch H Hkv n1 P dh scale out stream
+    ok = [256, 256, 256, 256, 256, 2, 32, 8, 65, 1024, 128, 0.088, 256, None]
+    for i, bad in ((6, 30), (7, 0), (10, 96), (8, 0), (9, -1), (11, float("inf")), (0, 258),
+                   (12, 260), (3, None)):
+        a = list(ok)
+        a[i] = bad
+        assert L.dt_tree_attention(*a) == dt.ERR_INVALID_ARG, (i, bad)
+    # dt_adaptive_budget: costs and sizes
+    out = dt.DtTreeOut(256, 256, 256, 256, None, None, 256)
+    for batch, N, cf, cn in ((1, 64, 0.0, 1.0), (1, 64, 1.0, -1.0), (1, 64, float("nan"), 1.0),
+                             (0, 64, 1.0, 1.0), (1, 5000, 1.0, 1.0)):
+        assert L.dt_adaptive_budget(C.byref(out), batch, N, cf, cn, 256, None) == \
+            dt.ERR_INVALID_ARG

@@ -171,6 +171,20 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(ms, torch, dist, world, dev):
+    """The slowest rank's time: every rank ends with the maximum of the ranks'
+    `ms` (replicas only, so this reduction of the timer is the one collective)."""
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, batch, K, total_ms):
+    """Units all ranks processed per second: world x batch per step, K steps."""
+    return world * batch * K / (total_ms / 1000.0)
+
+
 def e2e_leg(args, tb, wl, dt, np, torch, dist, world, dev, flush, st, K, Wm):
     """Same metric through dt_build_trees_host: pinned host inputs copied in and
     the trees copied back inside the timed region."""
@@ -199,10 +213,7 @@ def e2e_leg(args, tb, wl, dt, np, torch, dist, world, dev, flush, st, K, Wm):
         eb.record(st)
         eb.synchronize()
         e_ms += ea.elapsed_time(eb)
-    te = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = world * wl.batch * K / (float(te.item()) / 1000.0)
+    e2e_value = whole_job_rate(world, wl.batch, K, max_over_ranks(e_ms, torch, dist, world, dev))
     ok_e2e = bool((hout["status"] == 0).all())
 
     return e2e_value, h2d, d2h, ok_e2e
@@ -432,12 +443,8 @@ def main():
     topm_ms = [ph[i][0].elapsed_time(ph[i][1]) for i in range(K)]
     proj_ms = [ph[i][1].elapsed_time(ph[i][2]) for i in range(K)]
     search_ms = [ph[i][2].elapsed_time(ph[i][3]) for i in range(K)]
-    total_ms = sum(per)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
-    value = world * wl.batch * K / (total_ms / 1000.0)
+    total_ms = max_over_ranks(sum(per), torch, dist, world, dev)
+    value = whole_job_rate(world, wl.batch, K, total_ms)
     launches_per_round = dt.kernel_launches(tb.dims, tb.w.wdtype, tb.opt)
 
     # end to end through the host-buffer entry point: pinned inputs in, results out

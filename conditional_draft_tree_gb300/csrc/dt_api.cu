@@ -334,7 +334,7 @@ cudaStream_t side_stream() {
   return streams[dev];
 }
 
-// fork/join events of one call (released when the call returns; the driver
+// fork/join events of one call (released when the call returns; the CUDA driver
 // frees them once the recorded work has completed)
 struct Events {
   cudaEvent_t fork = nullptr, join = nullptr;

@@ -47,13 +47,13 @@ extern "C" {
 /* ------------------------------------------------------------ status codes */
 #define DT_OK 0
 #define DT_ERR_INVALID_ARG (-1)   /* bad size, null pointer, misalignment, limit exceeded */
-#define DT_ERR_UNSUPPORTED (-2)   /* no sm_103a device, or a shape beyond this build's kernels */
+#define DT_ERR_UNSUPPORTED (-2)   /* no sm_103a device, or a shape beyond this library's kernels */
 #define DT_ERR_CUDA (-3)          /* a CUDA runtime call or kernel launch failed */
 #define DT_ERR_NONFINITE (-4)     /* device: a base logit of the request is NaN or +inf */
 #define DT_ERR_TIMEOUT (-5)       /* device: a bounded inter-block wait expired; request output invalid */
 #define DT_ERR_BAD_TEMPERATURE (-6) /* device: temperature < 0 or not finite */
 
-/* Hard limits of this build (checked by every entry point). */
+/* Hard limits of this library (checked by every entry point). */
 #define DT_MAX_M 256        /* candidates per depth */
 #define DT_MAX_K 32         /* children per node */
 #define DT_MAX_D 64         /* draft depths (block size - 1) */

@@ -58,23 +58,29 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def load(path: str):
+    """A ctypes handle on an oracle build at ``path`` with the argument types
+    set (``lib()`` loads the default build; the mutation tests load others)."""
+    L = C.CDLL(path)
+    L.orc_topm.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p]
+    L.orc_gru_step.argtypes = [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
+                               C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+    L.orc_gru_step.restype = None
+    L.orc_build_tree.argtypes = [C.POINTER(_Model), C.POINTER(_Request), C.POINTER(_Tree)]
+    L.orc_children.argtypes = [C.POINTER(_Model), C.POINTER(_Request), C.c_void_p, C.c_int,
+                               C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+    L.orc_score_path.argtypes = [C.POINTER(_Model), C.POINTER(_Request), C.c_void_p, C.c_int,
+                                 C.c_void_p, C.c_void_p]
+    L.orc_chain.argtypes = [C.POINTER(_Model), C.POINTER(_Request), C.c_void_p, C.c_void_p,
+                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
         build()
-        L = C.CDLL(_LIB)
-        L.orc_topm.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p]
-        L.orc_gru_step.argtypes = [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
-                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
-        L.orc_gru_step.restype = None
-        L.orc_build_tree.argtypes = [C.POINTER(_Model), C.POINTER(_Request), C.POINTER(_Tree)]
-        L.orc_children.argtypes = [C.POINTER(_Model), C.POINTER(_Request), C.c_void_p, C.c_int,
-                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
-        L.orc_score_path.argtypes = [C.POINTER(_Model), C.POINTER(_Request), C.c_void_p, C.c_int,
-                                     C.c_void_p, C.c_void_p]
-        L.orc_chain.argtypes = [C.POINTER(_Model), C.POINTER(_Request), C.c_void_p, C.c_void_p,
-                                C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
-        _lib = L
+        _lib = load(_LIB)
     return _lib
 
 

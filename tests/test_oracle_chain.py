@@ -152,3 +152,26 @@ def test_uniform_clamping():
     for u, want in ((0.0, first), (-3.0, first), (np.nan, first), (1.0, last), (7.0, last)):
         o = oracle.chain(wl, 0, uniforms=np.array([[u]], np.float32))
         assert o["tokens"][0] == want, (u, o["tokens"][0], want)
+
+
+def test_temperature_half_equals_doubled_logits_and_w2():
+    """x = (L_base + W2 h) / T: T = 0.5 and T = 1 with L_base and W2 doubled give
+    the same x exactly (scaling by 2 is exact), so the same chains bit for bit."""
+    wl = small(69, T=0.5, batch=2)
+    u = W.chain_uniforms(2, wl.D, seed=69)
+    doubled = dataclasses.replace(wl, base_logits=wl.base_logits * 2, W2=wl.W2 * 2,
+                                  temperature=np.ones(2, np.float32))
+    for b in range(2):
+        a, c = oracle.chain(wl, b, uniforms=u), oracle.chain(doubled, b, uniforms=u)
+        for key in ("tokens", "lp", "margin"):
+            np.testing.assert_array_equal(a[key], c[key])
+
+
+def test_greedy_ties_take_the_lowest_id():
+    wl = small(70, T=0.0, batch=1)
+    wl = dataclasses.replace(wl, W2=np.zeros_like(wl.W2))
+    base = wl.base_logits.copy()
+    base[0, :, :] = -5.0
+    base[0, :, [11, 40, 3]] = 2.0            # three tied maxima per depth
+    o = oracle.chain(dataclasses.replace(wl, base_logits=base), 0)
+    assert (o["tokens"] == 3).all() and (o["margin"] == 0).all()

@@ -9,6 +9,13 @@
         R whole dt_build_trees rounds of the workload (weights, prepared table
         and workspace on the device: about 3.5 GB for the default workload);
         F = dt_options flags (default 0).
+    python -m conditional_draft_tree_gb300.profile_cases marginal [--reps R] [--cfg C]
+        R marginal-score rounds (DT_OPT_MARGINAL): top-M and the marginal tree
+        kernel, no weights on the device.
+    python -m conditional_draft_tree_gb300.profile_cases verify [--reps R] [--cfg C]
+        R launches of one tree-attention layer over the workload's trees
+        (32 query heads, 8 key/value heads, dh 128, prefix cache of 1024 keys
+        with lengths in [512, 1024]; synthetic bf16 Q/K/V).
     python -m conditional_draft_tree_gb300.profile_cases chain [--reps R] [--cfg C] [--greedy]
         R Domino chain-decoding rounds (dt_decode_chains) of the workload,
         sampled at its temperatures with seeded uniform draws, or greedy: one
@@ -87,9 +94,33 @@ def case_chain(cfg, reps, dev, greedy=False):
           f"chains/s={wl.batch / (ms * 1e-3):.0f}")
 
 
+def case_marginal(cfg, reps, dev):
+    wl = W.make_workload(cfg)
+    mb = dt.MarginalTreeBuilder.from_workload(wl, device=dev)
+    inp = mb.inputs_to_device(wl)
+    out = dt.alloc_outputs(mb.dims, dev)
+    ms = _timed(lambda: mb.run(**inp, out=out), reps, dev)
+    print(f"marginal {wl.name}: batch={wl.batch} mean_us={1000 * ms:.1f} "
+          f"trees/s={wl.batch / (ms * 1e-3):.0f}")
+
+
+def case_verify(cfg, reps, dev):
+    import numpy as np
+    wl = W.make_workload(cfg)
+    tb = dt.TreeBuilder.from_numpy(wl, device=dev)
+    trees = tb.run(**tb.inputs_to_device(wl))
+    q, k, v, plen = W.verify_inputs(wl.batch, 32, 8, wl.N + 1, 1024, 128, seed=cfg,
+                                    min_prefix=512)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+    qd, kd, vd, pd = t(q), t(k), t(v), torch.from_numpy(plen).to(dev)
+    out = torch.empty((wl.batch, 32, wl.N + 1, 128), dtype=torch.float32, device=dev)
+    ms = _timed(lambda: dt.tree_attention(qd, kd, vd, trees["mask"], pd, out=out), reps, dev)
+    print(f"verify {wl.name}: batch={wl.batch} n1={wl.N + 1} mean_us={1000 * ms:.1f}")
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["topm", "round", "chain"])
+    ap.add_argument("case", choices=["topm", "round", "chain", "marginal", "verify"])
     ap.add_argument("--greedy", action="store_true")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--cfg", type=int, default=3)
@@ -102,6 +133,10 @@ def main():
         case_round(args.cfg, args.reps, dev, args.flags)
     elif args.case == "chain":
         case_chain(args.cfg, args.reps, dev, args.greedy)
+    elif args.case == "marginal":
+        case_marginal(args.cfg, args.reps, dev)
+    elif args.case == "verify":
+        case_verify(args.cfg, args.reps, dev)
     else:
         case_topm(args.cfg, args.reps, dev)
 

@@ -177,7 +177,8 @@ int dt_kernel_launches(const dt_dims *dims, int wdtype, const dt_options *opt);
  * floats. Returns DT_OK when the work was enqueued. Part of the work (the
  * projection) runs on a library-owned stream of the current device, forked from
  * and joined back into `stream` with events, so every result is ordered on
- * `stream` as usual (also under CUDA-graph capture of `stream`). */
+ * `stream` as usual. (The fork and join are events, as stream capture into a
+ * CUDA graph requires; capture is not covered by a test yet.) */
 int dt_build_trees(const dt_dims *dims, const dt_weights *w, const void *prepared,
                    const float *base_logits, const float *H, const float *state0,
                    const int32_t *anchor_tok, const float *temperature,

@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--no-marginal", action="store_true",
                     help="skip the marginal-score (W2 = 0 ablation) leg")
     ap.add_argument("--flags", type=int, default=0,
-                    help="dt_options flags (e.g. 1 = K-chunk sums in thread-block clusters)")
+                    help="dt_options flags (DT_OPT_* bits of include/dt.h)")
     return ap.parse_args()
 
 
@@ -429,13 +429,11 @@ def main():
     ctrl = tb.workspace[:32].view(torch.int32).cpu().tolist()   # search counters of the last round
     search_steps, search_expansions = ctrl[4], ctrl[5]
     t_ns = tb.workspace[32:32 + 8 * 32].view(torch.int64).cpu().tolist()
-    search_split_us = dict(zip(["gemm", "barrier1", "score_reduce", "barrier2", "tail",
-                                "barrier3", "tail_children", "tail_pop_select", "gru",
-                                "gemm_mma", "gemm_epilogue", "gemm_wait_copies", "gemm_wait_mma",
-                                "score1_h", "score1_candidates", "score1_softmax_sort",
-                                "barrier4", "csum_sync1", "csum_send", "csum_sync2",
-                                "csum_add"],
-                               [x / 1000.0 for x in t_ns]))
+    search_split_us = {k: t_ns[i] / 1000.0 for i, k in enumerate(
+        ["gemm", "barrier_after_gemm", "request_score", "request_gather_children",
+         "request_pop_select", "request_gru", "gh_sums_after", "barrier_after_request",
+         "gru_wait_parent_gh", "gemm_mma", "gemm_epilogue", None, "gemm_wait_mma", "score_h",
+         "score_candidates", "score_softmax_sort"]) if k}
     gemm_cycles = dict(zip(["wait_free_buffer", "wait_landed_copy", "copy_issue", "mma_issue",
                             "pop_iterations", "pop_cycles", "select_iterations",
                             "select_cycles"], t_ns[24:32]))

@@ -21,7 +21,6 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, -1, -2, -3
 ERR_NONFINITE, ERR_TIMEOUT, ERR_BAD_TEMPERATURE = -4, -5, -6
 F32, BF16 = 0, 1
 NUM_PHASE_EVENTS = 4
-OPT_CLUSTER_SUM = 1          # dt_options.flags: K-chunk sums in distributed shared memory
 OPT_TEST_BARRIER_TIMEOUT = 2  # dt_options.flags: failure-detection test hook
 OPT_MARGINAL = 8             # dt_options.flags: marginal (path-independent) scores
 MAX_SPEC = 16

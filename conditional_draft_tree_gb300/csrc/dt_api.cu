@@ -115,84 +115,39 @@ int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, P
       q->chain_smem = static_cast<size_t>(smem);
       return true;
     };
-    bool placed = false;
     p->umma = 0;
-    p->cluster = 0;
     if (wdtype == DT_BF16) {
       // search GEMM on the tensor cores: 128-row tiles of [W_hh; W1_S] times K
-      // chunks, one (tile, chunk) per block, at most 512 K columns per chunk.
-      // On request (DT_OPT_CLUSTER_SUM) the K chunks of a tile form one
-      // thread-block cluster and sum their partial products in distributed
-      // shared memory; the cluster size is the largest whose clusters all fit on
-      // the GPU at once. By default the partials are summed through global memory.
+      // chunks, one (tile, chunk) per block, at most 512 K columns per chunk;
+      // the K-chunk partials are summed through global memory
       const int R = 3 * d.d_s + d.r;
       const int n_mt = (R + 127) / 128;
-      const bool allow_cluster = opt && (opt->flags & DT_OPT_CLUSTER_SUM);
-      for (int cs = 8; allow_cluster && cs >= 2 && !placed; --cs) {
-        const int kc = ((d.d_s + cs - 1) / cs + 15) / 16 * 16;
-        if (kc > 512 || (d.d_s + kc - 1) / kc != cs) continue;
-        Plan q = *p;
-        q.umma = 1; q.cluster = cs; q.n_mt = n_mt; q.ks = cs; q.kc = kc;
-        int wave = wave0;
-        if (!fit_smem(&q, wave)) continue;
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(q.chain_smem)) != cudaSuccess)
-          return DT_ERR_CUDA;
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = cs;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(cs * n_mt);
-        cfg.blockDim = dim3(256);
-        cfg.dynamicSmemBytes = q.chain_smem;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        int nclusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&nclusters, fn, &cfg) != cudaSuccess) {
-          cudaGetLastError();
-          continue;
-        }
-        if (nclusters < n_mt) continue;
-        q.chain_grid = cs * nclusters;
-        if (wave > q.chain_grid) wave = q.chain_grid;
-        q.wave = wave;
-        if (!fit_smem(&q, wave)) continue;
-        *p = q;
-        placed = true;
-      }
-      if (!placed) {
-        // without clusters: K-chunk partials are summed through global memory
-        int ks = p->num_sms / n_mt;
-        if (ks >= 1) {
-          int kc = ((d.d_s + ks - 1) / ks + 15) / 16 * 16;
-          ks = (d.d_s + kc - 1) / kc;
-          if (kc <= 512 && n_mt * ks <= p->num_sms) {
-            p->umma = 1;
-            p->n_mt = n_mt;
-            p->ks = ks;
-            p->kc = kc;
-          }
+      int ks = p->num_sms / n_mt;
+      if (ks >= 1) {
+        int kc = ((d.d_s + ks - 1) / ks + 15) / 16 * 16;
+        ks = (d.d_s + kc - 1) / kc;
+        if (kc <= 512 && n_mt * ks <= p->num_sms) {
+          p->umma = 1;
+          p->n_mt = n_mt;
+          p->ks = ks;
+          p->kc = kc;
         }
       }
     }
-    if (!placed) {
-      int wave = wave0;
-      if (!fit_smem(p, wave)) return DT_ERR_UNSUPPORTED;
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(p->chain_smem)) != cudaSuccess)
-        return DT_ERR_CUDA;
-      int per_sm = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256,
-                                                        static_cast<int>(p->chain_smem)) !=
-          cudaSuccess)
-        return DT_ERR_CUDA;
-      if (per_sm < 1) return DT_ERR_UNSUPPORTED;
-      p->chain_grid = per_sm * p->num_sms;
-      if (wave > p->chain_grid) wave = p->chain_grid;
-      p->wave = wave;
-    }
+    int wave = wave0;
+    if (!fit_smem(p, wave)) return DT_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(p->chain_smem)) != cudaSuccess)
+      return DT_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256,
+                                                      static_cast<int>(p->chain_smem)) !=
+        cudaSuccess)
+      return DT_ERR_CUDA;
+    if (per_sm < 1) return DT_ERR_UNSUPPORTED;
+    p->chain_grid = per_sm * p->num_sms;
+    if (wave > p->chain_grid) wave = p->chain_grid;
+    p->wave = wave;
   }
   const int wave = p->wave;
   const int e_cap = p->e_cap;
@@ -217,7 +172,8 @@ int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, P
   p->off_cand_val = off;  off = al(off + sizeof(float) * rows * d.M);
   if (p->marginal) {
     p->off_U = p->off_S = p->off_gh = p->off_gin = p->off_p = p->off_colexp = p->off_colinfo =
-        p->off_kids = p->off_upart = p->off_partial = p->off_gin16 = p->off_end = off;
+        p->off_kids = p->off_ghflag = p->off_upart = p->off_partial = p->off_gin16 = p->off_end =
+            off;
     return DT_OK;
   }
   p->off_U = off;         off = al(off + sizeof(float) * rows * d.r);
@@ -230,10 +186,13 @@ int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, P
   p->off_colexp = off;    off = al(off + sizeof(int) * (cols + wave));
   p->off_colinfo = off;   off = al(off + (3 * sizeof(int) + sizeof(float)) * cols);
   p->off_kids = off;      off = al(off + (sizeof(float) + sizeof(int32_t)) * cols * d.k);
+  // marks: per column, per request, per (request, expansion slot)
+  p->off_ghflag = off;
+  off = al(off + sizeof(unsigned) * (cols + wave + slots_e));
   p->off_upart = off;
   off = al(off + (p->proj_ksplit > 1 ? sizeof(float) * p->proj_ksplit * rows * d.r : 0));
   p->off_partial = off;
-  off = al(off + (p->umma && !p->cluster ? sizeof(float) * p->ks * cols * (3 * d.d_s + d.r) : 0));
+  off = al(off + (p->umma ? sizeof(float) * p->ks * cols * (3 * d.d_s + d.r) : 0));
   p->off_gin16 = off;
   // B operand of the tensor-core GEMM: passes of 256 columns, K padded to ks * kc
   const size_t cols256 = (cols + 255) / 256 * 256;

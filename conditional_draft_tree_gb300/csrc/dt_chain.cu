@@ -12,27 +12,33 @@
 // until N nodes are out; a popped node gets the state S = GRU(S_parent, E[tok])
 // and is expanded unless it is at depth D or is the N-th pop.
 //
-// How (GB300 design): the requests advance in lockstep steps. A step is
-//   GEMM phase  (all blocks): [gh_x; p_x] = [W_hh; W1_S] S_x (+[b_hh; 0]) for the
-//               nodes x of every request that were chosen for expansion;
-//   grid barrier;
-//   tail phase  (block b = request b): score the children of those nodes, pop
-//               as far as the exact best-first order allows, choose the next
-//               nodes to expand, advance their GRU states;
-//   grid barrier.
+// How (GB300 design): the requests advance in lockstep steps of two phases,
+// each ended by a grid barrier:
+//   GEMM phase    (tensor-core blocks): [gh_x; p_x] = [W_hh; W1_S] S_x for the
+//                 nodes x of every request chosen at the last step, as partial
+//                 products over K chunks;
+//   request phase (block b = request b): score the children of its nodes from
+//                 the p partials, pop as far as the exact best-first order
+//                 allows, choose the next nodes to expand and run their GRU
+//                 cells, writing the next GEMM's input columns. Meanwhile every
+//                 other block sums the gh partials of the step's columns
+//                 (+ b_hh) into the per-node store, one column at a time from a
+//                 shared counter, and marks each column done; a request block
+//                 that needs the gh of a parent expanded in this step waits for
+//                 its mark and sums columns itself while it waits.
 // The GRU input half W_ih E[tok] + b_ih is a row of the prepared table G, and
 // the recurrent half gh of a node is produced by the GEMM of the step that
 // expanded its parent, so the per-node GRU is elementwise.
 //
 // Exact speculative expansion: the order in which nodes are popped depends only
 // on scores, so expanding a node earlier than the one-at-a-time builder would
-// changes nothing but the time at which its children become known. The tail
-// replays the canonical best-first order over the discovered nodes and stops at
-// the first popped node that still needs its children ("stall"). It then expands
-// that node together with up to P-1 of the next best unexpanded frontier nodes
-// (P = spec width). Each step therefore pops at least one node, the trees are
-// identical for every P, and the number of lockstep steps drops from about N
-// to about the depth of the tree when the tree is bushy.
+// changes nothing but the time at which its children become known. The request
+// phase replays the canonical best-first order over the discovered nodes and
+// stops at the first popped node that still needs its children ("stall"). It
+// then expands that node together with up to P-1 of the next best unexpanded
+// frontier nodes (P = spec width). Each step therefore pops at least one node,
+// the trees are identical for every P, and the number of lockstep steps drops
+// from about N to about the depth of the tree when the tree is bushy.
 //
 // Frontier representation: the children of an expanded node are stored sorted
 // (their scores are non-increasing in rank), so the frontier is a set of sorted
@@ -54,8 +60,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kGemmCols = 8;     // columns per GEMM work unit
-constexpr int kGemmKC = 1024;    // K chunk staged in shared memory
+constexpr int kGemmCols = 8;     // columns per GEMM work unit (fp32 path)
+constexpr int kGemmKC = 1024;    // K chunk staged in shared memory (fp32 path)
 constexpr int kState0 = -2;      // column code: the state0 column of the first step
 
 struct ChainParams {
@@ -72,15 +78,19 @@ struct ChainParams {
   const float *U;
   float *S_store, *gh_store, *gin, *pbuf;
   int *col_count;
-  // per GEMM column (slot): its record (written with the selection, see
-  // col_record) and its k children once scored
+  // per GEMM column (slot = request * P + rank): its record (see col_record)
+  // and, when a member of the request's group scored it, its k children
   int4 *col_rec;
   float *kid_score;
   int32_t *kid_tok;
+  // marks (release / acquire, zeroed at launch): per slot, step + 1 once its
+  // children are out; per request, step + 1 once its selection is out; per
+  // (request, expansion), nonzero once the expansion's gh is in gh_store
+  unsigned *scored, *sel_mark, *gh_mark;
+  int grp;             // blocks per request group (leader = member 0)
   // tensor-core GEMM path (bf16 weights): A tiles of 128 rows x kc K stay in
   // shared memory; the input columns arrive as three bf16 terms per state
   int umma, n_mt, ks, kc, cols_cap;
-  int cluster;         // 0, or the cluster size (= ks): K chunks summed in distributed shared memory
   float *partial;      // [ks][cols_cap][R] per-K-chunk partial products, by slot
   uint16_t *gin16;     // B operand in tile layout (bcol_index)
   Ctrl *ctrl;
@@ -93,7 +103,8 @@ struct ChainParams {
   int test_skip;       // failure-detection test: the last block skips its first arrival
   // dynamic shared memory carve-up (byte offsets)
   int sm_child_score, sm_child_tok, sm_child_exp, sm_exp_depth, sm_exp_parent, sm_exp_score,
-      sm_exp_tok, sm_run_e, sm_run_head, sm_run_pos, sm_vhead, sm_par, sm_scratch, sm_total;
+      sm_exp_tok, sm_run_e, sm_run_head, sm_run_pos, sm_vhead, sm_par, sm_slots, sm_recs,
+      sm_scratch, sm_total;
   int sm_A, sm_B, sm_mbar, sm_tmem, sm_run_hs, sm_vhs;
 };
 
@@ -104,12 +115,23 @@ struct TailState {
   int done;
   int n_sel;
   int spec_used;  // speculative (non-stall) expansions made so far
-  int sel_e[DT_MAX_SPEC];
+  int sel_e[DT_MAX_SPEC];    // expansions chosen at the last selection (the next GEMM's columns)
   float T;
   int status;
 };
 
 __device__ __forceinline__ float ldcg(const float *p) { return __ldcg(p); }
+
+// ---------------------------------------------------------------- GEMM phase
+
+// Record of one GEMM column: the expansion e it computes (kState0: the state0
+// column of the first step), its parent expansion (-1: the root, whose input
+// state is state0), the depth of its children, its token (the GRU input) and
+// its path score. One 16-byte word so that a column's facts arrive together.
+__device__ __forceinline__ int4 col_record(int e, int parent, int child_depth, int tok,
+                                           float score) {
+  return make_int4(e, (parent + 1) | (child_depth << 16), tok, __float_as_int(score));
+}
 
 // Sum of v[i] over the 32 lanes, scattered: lane l returns the total of v[l].
 __device__ __forceinline__ float reduce_scatter32(float v[32], int lane) {
@@ -126,26 +148,19 @@ __device__ __forceinline__ float reduce_scatter32(float v[32], int lane) {
   return v[0];
 }
 
-// ---------------------------------------------------------------- GEMM phase
+// Active GEMM columns in (request, rank) order: slot ids written to `slots`,
+// count returned. With `cl` also their records (taken before the request
+// phase reassigns them) and, per request, the index of its first column and
+// its column count. nb <= 256 requests per wave: one thread per request reads
+// its count and, in the same round trip, the records of all its P slots; then
+// a block-wide exclusive scan.
+struct ColList {
+  int4 *recs;        // [cols_cap] records of the listed columns
+  int *req_first;    // [nb]
+  int *req_cnt;      // [nb]
+};
 
-// Record of one GEMM column: the expansion e it computes (kState0: the state0
-// column of the first step), its parent expansion (-1: the root, whose input
-// state is state0), the depth of its children, its token (the GRU input) and
-// its path score. One 16-byte word so that a column's facts arrive together.
-__device__ __forceinline__ int4 col_record(int e, int parent, int child_depth, int tok,
-                                           float score) {
-  return make_int4(e, (parent + 1) | (child_depth << 16), tok, __float_as_int(score));
-}
-__device__ __forceinline__ int rec_parent(const int4 &r) { return (r.y & 0xffff) - 1; }
-__device__ __forceinline__ int rec_child_depth(const int4 &r) {
-  return static_cast<int>(static_cast<unsigned>(r.y) >> 16);
-}
-
-// Active GEMM columns in (request, rank) order: slot ids written to `slots` and
-// (when `recs` is given) their records, count returned. nb <= 256 requests per
-// wave: one thread per request reads its count and, in the same round trip,
-// the records of all its P slots; then a block-wide exclusive scan.
-__device__ int compact_slots(const ChainParams &p, int *slots, int4 *recs = nullptr) {
+__device__ int compact_slots(const ChainParams &p, int *slots, const ColList *cl = nullptr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ int s_warp_sum[kWarps];
   __shared__ int s_total;
@@ -153,7 +168,7 @@ __device__ int compact_slots(const ChainParams &p, int *slots, int4 *recs = null
   const bool mine = b_me < p.nb;
   const int c_me = mine ? __ldcg(p.col_count + b_me) : 0;
   int4 r8[8];
-  if (recs) {
+  if (cl) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       r8[i] = (mine && i < p.P) ? __ldcg(p.col_rec + b_me * p.P + i) : make_int4(0, 0, 0, 0);
@@ -171,11 +186,15 @@ __device__ int compact_slots(const ChainParams &p, int *slots, int4 *recs = null
   if (threadIdx.x == kThreads - 1) s_total = base + incl;
   const int first = base + incl - c_me;
   for (int i = 0; i < c_me; ++i) slots[first + i] = b_me * p.P + i;
-  if (recs) {
+  if (cl) {
+    if (mine) {
+      cl->req_first[b_me] = first;
+      cl->req_cnt[b_me] = c_me;
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (i < c_me) recs[first + i] = r8[i];
-    for (int i = 8; i < c_me; ++i) recs[first + i] = __ldcg(p.col_rec + b_me * p.P + i);
+      if (i < c_me) cl->recs[first + i] = r8[i];
+    for (int i = 8; i < c_me; ++i) cl->recs[first + i] = __ldcg(p.col_rec + b_me * p.P + i);
   }
   __syncthreads();
   return s_total;
@@ -343,139 +362,25 @@ __device__ __forceinline__ size_t bcol_index(const ChainParams &p, int slot, int
 struct UmmaState {
   uint32_t tmem;      // TMEM base column address
   uint32_t next;      // global index of the next B slice (buffer = next % kBufs)
-  uint32_t cphase;    // uses of the cluster barrier so far
 };
 
-// Bounded barrier of the CTAs of one cluster: every CTA arrives on every CTA's
-// barrier (count = cluster size) and waits on its own, with a time limit.
-__device__ bool cluster_sync(uint64_t *cbar, int cs, uint32_t &phase, uint64_t limit_ns) {
-  __shared__ int s_cok;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t a = smem_u32(cbar);
-    for (int q = 0; q < cs; ++q) mbar_arrive_remote(mapa_u32(a, q));
-    s_cok = mbar_wait_cluster(cbar, phase & 1u, limit_ns) ? 1 : 0;
-  }
-  ++phase;
-  __syncthreads();
-  return s_cok != 0;
-}
-
-// The K-chunk sum of one pass inside the cluster of an M tile, in rounds of 128
-// columns. CTA q owns the columns [q * owned, (q + 1) * owned) of a round.
-// Every CTA reads its accumulator columns from TMEM (one row per lane) and
-// stores them, four columns per 16-byte store, into the owner's receive
-// buffer [sender rank][row][column] in distributed shared memory; after a
-// cluster barrier each owner sums its columns over the senders in chunk order
-// (the order of the global-memory path) and writes [gh; p] (+ [b_hh; 0]).
-__device__ bool cluster_reduce(const ChainParams &p, unsigned char *sB, uint64_t *cbar,
-                               UmmaState &u, int pass, int hi, const uint32_t *mask, int mt,
-                               int rank) {
-  __shared__ long long s_ghoff[256];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int cs = p.cluster, ds = p.d_s, R = 3 * ds + p.r;
-  const int owned = ((128 + cs - 1) / cs + 3) & ~3;   // columns per owner and round
-  float *recv = reinterpret_cast<float *>(sB);        // [cs][128][owned]
-  const uint32_t recv_a = smem_u32(recv);
-  for (int c = threadIdx.x; c < 256; c += kThreads) {
-    long long off = -1;
-    if (c < hi && ((mask[c >> 5] >> (c & 31)) & 1u)) {
-      const int slot = pass * 256 + c;
-      const int e = __ldcg(p.col_rec + slot).x;
-      const int e_slot = (e == kState0) ? p.e_cap : e;
-      off = (static_cast<long long>(slot / p.P) * (p.e_cap + 1) + e_slot) * 3 * ds;
-    }
-    s_ghoff[c] = off;
-  }
-  bool ok = true;
-  const int quarter = warp & 3, half = warp >> 2;
-  const int row_l = quarter * 32 + lane;              // this lane's TMEM lane = tile row
-  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
-  uint64_t tc = clock_me ? global_ns() : 0;
-  auto lap = [&](int k) {
-    if (clock_me) {
-      const uint64_t n = global_ns();
-      p.ctrl->t_ns[k] += n - tc;
-      tc = n;
-    }
-  };
-  for (int r0 = 0; r0 < hi; r0 += 128) {
-    // the receive buffers alias the B slices: every CTA's MMAs (round 0) and
-    // sums (later rounds) must be done before the stores
-    ok &= cluster_sync(cbar, cs, u.cphase, p.limit_ns);
-    lap(17);
-    // send: warp (quarter, half) covers columns r0 + 64 half + [0, 64)
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      const int c32 = r0 + 64 * half + 32 * g;
-      if (c32 < hi && mask[c32 >> 5] != 0u) {
-        float v[32];
-        tmem_ld32(u.tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const int cl = c32 - r0 + j;                 // column within the round
-          const int owner = cl / owned, co = cl - owner * owned;
-          const uint32_t off = static_cast<uint32_t>(((rank * 128 + row_l) * owned + co) * 4);
-          st_cluster_f4(mapa_u32(recv_a + off, owner), v[j], v[j + 1], v[j + 2], v[j + 3]);
-        }
-      }
-    }
-    lap(18);
-    ok &= cluster_sync(cbar, cs, u.cphase, p.limit_ns);
-    lap(19);
-    // sum: item = (column group of 4, row); lanes take consecutive rows
-    const int c_beg = r0 + rank * owned;
-    for (int it = threadIdx.x; it < (owned / 4) * 128; it += kThreads) {
-      const int g4 = it >> 7, rl = it & 127;
-      const int row = mt * 128 + rl;
-      if (row >= R) continue;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int z = 0; z < cs; ++z) {
-        const float4 v = *reinterpret_cast<const float4 *>(recv + (z * 128 + rl) * owned + 4 * g4);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
-      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-      const float bias = (row < 3 * ds && p.b_hh) ? p.b_hh[row] : 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c = c_beg + 4 * g4 + q;
-        if (c - r0 >= 128 || c >= hi || s_ghoff[c] < 0) continue;
-        if (row < 3 * ds) p.gh_store[s_ghoff[c] + row] = a4[q] + bias;
-        else p.pbuf[static_cast<size_t>(pass * 256 + c) * p.r + (row - 3 * ds)] = a4[q];
-      }
-    }
-    lap(20);
-  }
-  return ok;
-}
-
 // Partial products of this block's (M tile, K chunk) for every active column,
-// written to p.partial[kz][slot][row]. D (TMEM, 128 rows x up to 256 node
+// written to p.partial[kz][slot][row]. Every block also lists the active
+// columns and their records (slots, cl): the request phase reassigns the
+// columns' records while their gh sums and scores are still being made. D (TMEM, 128 rows x up to 256 node
 // columns) = A B^T, A = 128 weight rows (K-major, resident), B = the node
 // columns as hi / mid / lo bf16 terms; one MMA per (K step, term) covers a
 // whole pass of 256 columns, since an MMA costs about the same for any N up to
-// 256. Thread 0 runs the pipeline (bulk copies into kBufs slice buffers, MMAs,
-// commits); all warps read the accumulators back.
-__device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsigned char *scratch,
-                                UmmaState &u, int known_total, int &total_out) {
+// 256. Thread 0 issues the bulk copies into kBufs slice buffers, thread 32 the
+// MMAs and commits; all warps read the accumulators back. Every block lists
+// the active columns (slots, count in total_out) for the request phase.
+__device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, int *slots,
+                                const ColList &cl, UmmaState &u, int &total_out) {
   __shared__ int s_hi[16];           // per pass: last active column + 1
   __shared__ uint32_t s_mask[16][8]; // per pass: active columns
   __shared__ int s_fail;              // a bounded wait of an issuing thread ran out
-  int *slots = reinterpret_cast<int *>(scratch);
   if (threadIdx.x == 0) s_fail = 0;
-  int total = known_total;
-  if (total < 0) {
-    total = compact_slots(p, slots);   // (synchronises the block)
-    // the columns' records, for the scoring phase that follows: loaded by
-    // warps 2..7 while the issuing threads run the pipeline
-    int4 *recs = reinterpret_cast<int4 *>(scratch + ((p.cols_cap * 4 + 15) & ~15));
-    if (threadIdx.x >= 64)
-      for (int c = static_cast<int>(threadIdx.x) - 64; c < total; c += kThreads - 64)
-        recs[c] = __ldcg(p.col_rec + slots[c]);
-  } else {
-    __syncthreads();   // the GRU phase listed the columns and records already
-  }
+  const int total = compact_slots(p, slots, &cl);   // (synchronises the block)
   total_out = total;
   if (total == 0 || blockIdx.x >= p.n_mt * p.ks) return true;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -500,7 +405,6 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
   uint64_t *empty = full + kBufs;
   const int nkb = p.kc >> 4;
   const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
-  bool ok = true;
   for (int pass = 0; pass < n_pass; ++pass) {
     const int hi = s_hi[pass];
     if (hi == 0) continue;
@@ -577,18 +481,6 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
     tmem_fence_after();
     const uint64_t t1 = clock_me ? global_ns() : 0;
     if (clock_me) p.ctrl->t_ns[9] += t1 - t0;
-    if (p.cluster) {
-      fence_async_smem();
-      ok &= cluster_reduce(p, sB, full + 2 * kBufs, u, pass, hi, s_mask[pass], mt, kz);
-      bool more = false;
-      for (int q = pass + 1; q < n_pass; ++q) more |= s_hi[q] > 0;
-      // the next pass's copies overwrite the stages: every CTA must be done reading
-      if (more) ok &= cluster_sync(full + 2 * kBufs, p.cluster, u.cphase, p.limit_ns);
-      tmem_fence_before();
-      __syncthreads();
-      if (clock_me) p.ctrl->t_ns[10] += global_ns() - t1;
-      continue;
-    }
     // epilogue: TMEM lane = row of the tile; warps w and w+4 share a lane quarter
     const int quarter = warp & 3;
     const int row = mt * 128 + quarter * 32 + lane;
@@ -611,74 +503,128 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, unsig
     if (clock_me) p.ctrl->t_ns[10] += global_ns() - t1;
   }
   __syncthreads();
-  return ok && s_fail == 0;
+  return s_fail == 0;
 }
 
-// Sum of the K-chunk partials (fixed order) + b_hh into gh_store, for the
-// columns of the last GEMM (`slots` and `recs`, taken before the tails
-// reassign the columns). It runs beside the tails: one
-// column per chunk, chunks handed out by a global counter, so that the blocks
-// without a request start at once and the tails join when they are done. Every
-// block calls this once per step and makes exactly one failing grab, so the
-// counter of the next step starts at base + columns + gridDim.
-__device__ void gh_reduce(const ChainParams &p, const int *slots, const int4 *recs, int total,
-                          unsigned &base) {
-  __shared__ int s_idx;
+// ------------------------------------------------------------ gh sums
+
+__device__ __forceinline__ unsigned *gh_mark_of(const ChainParams &p, int b, int e) {
+  return p.gh_mark + static_cast<size_t>(b) * (p.e_cap + 1) + (e < 0 ? p.e_cap : e);
+}
+
+// Sum of the K-chunk partials (fixed order) + b_hh of the column in `slot`
+// (record rec) into the per-node store; then the expansion's gh mark
+// (release, gpu scope), read by the blocks that run the GRU of its children.
+__device__ void gh_column(const ChainParams &p, int slot, const int4 &rec) {
   const int ds = p.d_s, R = 3 * ds + p.r, n4 = 3 * ds / 4;
   const size_t plane = static_cast<size_t>(p.cols_cap) * R;
+  const int b = slot / p.P, e = rec.x == kState0 ? -1 : rec.x;
+  float *dst = p.gh_store +
+               (static_cast<size_t>(b) * (p.e_cap + 1) + (e < 0 ? p.e_cap : e)) * 3 * ds;
+  const float *src = p.partial + static_cast<size_t>(slot) * R;
   constexpr int IT = 3;
-  while (true) {
-    if (threadIdx.x == 0)
-      s_idx = static_cast<int>(atomicAdd(&p.ctrl->red_next, 1u) - base);
-    __syncthreads();
-    const int col = s_idx;
-    __syncthreads();
-    if (col >= total) break;
-    const int slot = slots[col];
-    float *dst = p.gh_store +
-                 (static_cast<size_t>(slot / p.P) * (p.e_cap + 1) +
-                  (recs[col].x == kState0 ? p.e_cap : recs[col].x)) * 3 * ds;
-    const float *src = p.partial + static_cast<size_t>(slot) * R;
-    for (int i0 = threadIdx.x; i0 < n4; i0 += IT * kThreads) {
-      float4 acc[IT];
+  for (int i0 = threadIdx.x; i0 < n4; i0 += IT * kThreads) {
+    float4 acc[IT];
 #pragma unroll
-      for (int q = 0; q < IT; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int z0 = 0; z0 < p.ks; z0 += 4) {
-        float4 v[4][IT];
+    for (int q = 0; q < IT; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int z0 = 0; z0 < p.ks; z0 += 4) {
+      float4 v[4][IT];
 #pragma unroll
-        for (int z = 0; z < 4; ++z)
+      for (int z = 0; z < 4; ++z)
 #pragma unroll
-          for (int q = 0; q < IT; ++q) {
-            const int i = i0 + q * kThreads;
-            v[z][q] = (z0 + z < p.ks && i < n4)
-                          ? __ldcg(reinterpret_cast<const float4 *>(src + (z0 + z) * plane) + i)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-        for (int z = 0; z < 4; ++z)
-#pragma unroll
-          for (int q = 0; q < IT; ++q) {
-            acc[q].x += v[z][q].x; acc[q].y += v[z][q].y;
-            acc[q].z += v[z][q].z; acc[q].w += v[z][q].w;
-          }
-      }
-#pragma unroll
-      for (int q = 0; q < IT; ++q) {
-        const int i = i0 + q * kThreads;
-        if (i >= n4) continue;
-        float4 a = acc[q];
-        if (p.b_hh) {   // 4-byte aligned only
-          a.x += p.b_hh[4 * i]; a.y += p.b_hh[4 * i + 1];
-          a.z += p.b_hh[4 * i + 2]; a.w += p.b_hh[4 * i + 3];
+        for (int q = 0; q < IT; ++q) {
+          const int i = i0 + q * kThreads;
+          v[z][q] = (z0 + z < p.ks && i < n4)
+                        ? __ldcg(reinterpret_cast<const float4 *>(src + (z0 + z) * plane) + i)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        reinterpret_cast<float4 *>(dst)[i] = a;
+#pragma unroll
+      for (int z = 0; z < 4; ++z)
+#pragma unroll
+        for (int q = 0; q < IT; ++q) {
+          acc[q].x += v[z][q].x; acc[q].y += v[z][q].y;
+          acc[q].z += v[z][q].z; acc[q].w += v[z][q].w;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < IT; ++q) {
+      const int i = i0 + q * kThreads;
+      if (i >= n4) continue;
+      float4 a = acc[q];
+      if (p.b_hh) {   // 4-byte aligned only
+        a.x += p.b_hh[4 * i]; a.y += p.b_hh[4 * i + 1];
+        a.z += p.b_hh[4 * i + 2]; a.w += p.b_hh[4 * i + 3];
       }
+      reinterpret_cast<float4 *>(dst)[i] = a;
     }
   }
-  base += static_cast<unsigned>(total) + gridDim.x;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    st_release_u32(gh_mark_of(p, b, e), 1u);
+  }
 }
 
-// ---------------------------------------------------------------- tail phase
+// One grab from the step's column counter: the index of a column to sum, or
+// a value >= total when none is left. Block-wide.
+__device__ __forceinline__ int gh_grab(unsigned *counter) {
+  __shared__ int s_idx;
+  if (threadIdx.x == 0) s_idx = static_cast<int>(atomicAdd(counter, 1u));
+  __syncthreads();
+  const int col = s_idx;
+  __syncthreads();
+  return col;
+}
+
+// The step's gh sums, handed out one column at a time.
+struct GhWork {
+  const int *slots;
+  const int4 *recs;
+  int total;
+  unsigned *counter;
+};
+
+// Sums this step's columns until the counter runs out.
+__device__ void gh_help(const ChainParams &p, const GhWork &w) {
+  while (true) {
+    const int col = gh_grab(w.counter);
+    if (col >= w.total) break;
+    gh_column(p, w.slots[col], w.recs[col]);
+  }
+}
+
+// Bounded wait, block-wide, until ready() (evaluated by thread 0, with
+// acquire loads) holds. With `help` the block sums gh columns while it waits,
+// so a wait on gh marks ends even when no other block is free to sum. False
+// when the limit passes or another block aborted.
+template <typename Ready>
+__device__ bool wait_for(const ChainParams &p, const GhWork *help, Ready ready) {
+  __shared__ int s_state;   // 0: wait, 1: ready, 2: give up
+  uint64_t t0 = 0;
+  bool idle = help == nullptr;
+  for (uint32_t it = 0;; ++it) {
+    if (threadIdx.x == 0) {
+      int st = ready() ? 1 : 0;
+      if (st == 0 && idle && (it & 15u) == 0u) {
+        const uint64_t now = global_ns();
+        if (t0 == 0) t0 = now;
+        else if (now - t0 > p.limit_ns || ld_acquire_s32(&p.ctrl->abort)) st = 2;
+      }
+      s_state = st;
+    }
+    __syncthreads();
+    const int st = s_state;
+    __syncthreads();
+    if (st) return st == 1;
+    if (help) {
+      const int col = gh_grab(help->counter);
+      idle = col >= help->total;
+      if (!idle) gh_column(p, help->slots[col], help->recs[col]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- request tables
 
 struct Tables {
   float *child_score;    // [e_cap][k]
@@ -795,157 +741,118 @@ __device__ __forceinline__ void write_column4(const ChainParams &p, int slot, in
   }
 }
 
-// GRU cells of the nodes chosen for expansion, spread over the grid:
-// S_e = GRU(S_parent, x = E[tok]) with the input half taken from the prepared
-// table row G[tok] (= W_ih E[tok] + b_ih) and the recurrent half gh_parent
-// (= W_hh S_parent + b_hh) from an earlier GEMM (the root: state0 and the gh of
-// the state0 column). Four units per item, two items per thread in flight; the
-// new state goes to S_store and, as the next GEMM's input, to its column.
-__device__ __forceinline__ float gru_unit(float gir, float giz, float gin, float ghr, float ghz,
-                                          float ghn, float sp) {
-  const float r = sigmoidf_(gir + ghr);
-  const float z = sigmoidf_(giz + ghz);
-  const float n = tanhf(gin + r * ghn);
-  return (1.f - z) * n + z * sp;
-}
+// ------------------------------------------------------------ request phase
 
-__device__ void gru_phase(const ChainParams &p, const int *slots, const int4 *recs, int total) {
-  const int ds = p.d_s, q4 = ds / 4;
-  const int items = total * q4;
-  const int stride = gridDim.x * kThreads;
-  constexpr int IT = 2;
-  for (int i0 = blockIdx.x * kThreads + threadIdx.x; i0 < items; i0 += IT * stride) {
-    float4 gi[IT][3], gh[IT][3], sp[IT];
-    int slot[IT], u[IT];
-    size_t so[IT];
-#pragma unroll
-    for (int k = 0; k < IT; ++k) {
-      const int i = i0 + k * stride;
-      slot[k] = -1;
-      if (i < items) {
-        const int c = i / q4;
-        u[k] = (i - c * q4) * 4;
-        slot[k] = slots[c];
-        const int b = slot[k] / p.P;
-        const int4 rec = recs[c];
-        const int e = rec.x, pe = rec_parent(rec), tok = rec.z;
-        const size_t ebase = static_cast<size_t>(b) * (p.e_cap + 1);
-        const float *g = p.G + static_cast<size_t>(tok) * 3 * ds + u[k];
-        const float *ghp = p.gh_store + (ebase + (pe < 0 ? p.e_cap : pe)) * 3 * ds + u[k];
-        const float *spp = pe < 0 ? p.state0 + static_cast<size_t>(p.b0 + b) * ds + u[k]
-                                  : p.S_store + (ebase + pe) * ds + u[k];
-        so[k] = (ebase + e) * ds + u[k];
-#pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          gi[k][q] = __ldg(reinterpret_cast<const float4 *>(g + q * ds));
-          gh[k][q] = __ldcg(reinterpret_cast<const float4 *>(ghp + q * ds));
-        }
-        sp[k] = __ldcg(reinterpret_cast<const float4 *>(spp));
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < IT; ++k) {
-      if (slot[k] < 0) continue;
-      float4 s;
-      s.x = gru_unit(gi[k][0].x, gi[k][1].x, gi[k][2].x, gh[k][0].x, gh[k][1].x, gh[k][2].x, sp[k].x);
-      s.y = gru_unit(gi[k][0].y, gi[k][1].y, gi[k][2].y, gh[k][0].y, gh[k][1].y, gh[k][2].y, sp[k].y);
-      s.z = gru_unit(gi[k][0].z, gi[k][1].z, gi[k][2].z, gh[k][0].z, gh[k][1].z, gh[k][2].z, sp[k].z);
-      s.w = gru_unit(gi[k][0].w, gi[k][1].w, gi[k][2].w, gh[k][0].w, gh[k][1].w, gh[k][2].w, sp[k].w);
-      *reinterpret_cast<float4 *>(p.S_store + so[k]) = s;
-      write_column4(p, slot[k], u[k], s);
-    }
-  }
-  if (p.umma) fence_async_global();   // the columns are read by bulk copies next
-}
-
-// Children of every node expanded by the last GEMM, spread over the grid. A
-// node (GEMM column `slot`, children at depth j, request b) gets kWPN warps of
-// one block: each forms h = SiLU(U_j + p) (p summed over the K-chunk partials
-// in fixed order) and the corrected logits L_c = (L_base^j[c] + W2[c,:] h) / T
-// of its share of the M candidates; then one of them takes the log-sum-exp
-// over the M values and the k best (L desc, id asc) as the children, with
-// scores score(node) + L_c - lse, and warms L2 with the prepared rows of the two
-// best (the likeliest next expansions).
-constexpr int kWPN = 4;                // warps per node
-constexpr int kNPB = kWarps / kWPN;    // nodes per block and round
-
+// Children of the nodes the last GEMM expanded for request b: the columns
+// c = g, g + G, ... of the request (member g of its group of G blocks), one
+// warp per node. A warp forms h = SiLU(U_j + p) (p summed over the K-chunk
+// partials in fixed order) and the corrected logits L_c = (L_base^j[c] +
+// W2[c,:] h) / T of the M candidates, then the log-sum-exp over them and the k
+// best (L desc, id asc) as the node's children, with scores score(node) + L_c
+// - lse: into the request's shared tables when this block is the group's
+// leader (t != nullptr), else to global memory with the column's mark. The
+// prepared rows of the two best children (the likeliest next expansions) are
+// fetched into L2.
 template <int WDT, int SLOTS, bool SMALL_R>
-__device__ void score_phase(const ChainParams &p, const int *slots, const int4 *recs, int total,
-                            float *sm) {
+__device__ void score_cols(const ChainParams &p, const Tables *t, int b, int g, const ColList &cl,
+                           const int *slots, float T, unsigned mark, float *sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int node_in_block = warp / kWPN, wq = warp % kWPN;
-  float *Lsm = sm + node_in_block * p.M;
-  float *hbuf = sm + kNPB * p.M + warp * p.r;   // used only when r > 256
   const int nq = p.r / 8;
   const int R = 3 * p.d_s + p.r;
   const size_t plane = static_cast<size_t>(p.cols_cap) * R;
   const float ninf = -__int_as_float(0x7f800000);
-  const int mq = (p.M + kWPN - 1) / kWPN;
   constexpr int G = WDT == 1 ? 16 : 8;   // candidate rows in flight
+  const int first = cl.req_first[b], cnt = cl.req_cnt[b];
+  const int nmine = cnt > g ? (cnt - g + p.grp - 1) / p.grp : 0;
+  if (nmine == 0) return;
+  // wpn warps share a node (a power of two): every node's candidates take one
+  // round of row loads when the member has few nodes
+  int wpn = kWarps;
+  while (wpn > 1 && wpn * nmine > kWarps) wpn >>= 1;
+  const int npr = kWarps / wpn;               // nodes per round
+  const int wq = warp % wpn, slot_in_round = warp / wpn;
+  const int mq = (p.M + wpn - 1) / wpn;       // candidates per warp
+  float *Lw = sm + slot_in_round * p.M;
+  float *hbuf = sm + kWarps * p.M + warp * p.r;   // used only when r > 256
   const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
-  const bool psum = p.umma && !p.cluster;   // p still split over K chunks
-  for (int n0 = blockIdx.x * kNPB; n0 < total; n0 += gridDim.x * kNPB) {
-    const int n = n0 + node_in_block;
-    const bool any = n < total;
-    const int slot = any ? slots[n] : 0;
-    uint64_t t_in = clock_me ? global_ns() : 0;
-    // 1. everything indexed by the column alone, issued together: the
-    //    expansion, the children's depth and this lane's share of p
-    int e = -1, j = 1;
-    float pa[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) pa[i] = 0.f;
-    if (any) {
-      e = recs[n].x;
-      j = rec_child_depth(recs[n]);
-      if (SMALL_R && lane < nq) {
-        if (psum) {
-          const float *src = p.partial + static_cast<size_t>(slot) * R + 3 * p.d_s + 8 * lane;
-          for (int z0 = 0; z0 < p.ks; z0 += 4) {
-            float4 v[4][2];
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-              const bool ok = z0 + z < p.ks;
-              const float4 *q = reinterpret_cast<const float4 *>(src + (z0 + z) * plane);
-              v[z][0] = ok ? __ldcg(q) : make_float4(0.f, 0.f, 0.f, 0.f);
-              v[z][1] = ok ? __ldcg(q + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-              pa[0] += v[z][0].x; pa[1] += v[z][0].y; pa[2] += v[z][0].z; pa[3] += v[z][0].w;
-              pa[4] += v[z][1].x; pa[5] += v[z][1].y; pa[6] += v[z][1].z; pa[7] += v[z][1].w;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            pa[i] = ldcg(p.pbuf + static_cast<size_t>(slot) * p.r + 8 * lane + i);
-        }
-      }
-    }
-    const bool live = any && e >= 0;
-    const int b = slot / p.P;
+  for (int r0 = 0; r0 < nmine; r0 += npr) {
+    const int i = r0 + slot_in_round;
+    const int c = g + i * p.grp;
+    const int4 rec = i < nmine ? cl.recs[first + c] : make_int4(kState0, 0, 0, 0);
+    const bool live = rec.x != kState0;   // (the state0 column of the first step is not scored)
+    const int e = rec.x;
+    const int slot = live ? slots[first + c] : 0;
+    const int j = live ? static_cast<int>(static_cast<unsigned>(rec.y) >> 16) : 1;
+    const float base_score = __int_as_float(rec.w);
     const size_t row = static_cast<size_t>(p.b0 + b) * p.D + (j - 1);
     const int32_t *cid = p.cand_id + row * p.M;
     const float *cval = p.cand_val + row * p.M;
-    float T = p.temperature ? p.temperature[p.b0 + b] : 1.0f;
-    T = (T == 0.0f) ? 1.0f : T;
-    // the finishing warp's candidate ids, loaded early
+    const float *U = p.U + row * p.r;
+    uint64_t t_in = clock_me ? global_ns() : 0;
+    // the candidate ids of the finishing pass, loaded early
     int fid[SLOTS];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
-      const int c = s * 32 + lane;
-      fid[s] = (live && wq == 0 && c < p.M) ? __ldg(cid + c) : -1;
+      const int ci = s * 32 + lane;
+      fid[s] = (live && wq == 0 && ci < p.M) ? __ldg(cid + ci) : -1;
     }
     if (live) {
-      const float *U = p.U + row * p.r;
-      // 2. U_j and the first candidate group (ids, base values, W2 rows) before
-      //    h is formed, so that the row gathers overlap the U loads
-      const int c_beg = wq * mq, c_end = min(p.M, c_beg + mq);
       float h[8];
-      float uu[8];
+      if (SMALL_R) {
+        float pa[8], uu[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) uu[i] = (SMALL_R && lane < nq) ? __ldg(U + 8 * lane + i) : 0.f;
+        for (int q = 0; q < 8; ++q) {
+          pa[q] = 0.f;
+          uu[q] = lane < nq ? __ldg(U + 8 * lane + q) : 0.f;
+        }
+        if (lane < nq) {
+          if (p.umma) {
+            const float *src = p.partial + static_cast<size_t>(slot) * R + 3 * p.d_s + 8 * lane;
+            for (int z0 = 0; z0 < p.ks; z0 += 4) {
+              float4 v[4][2];
+#pragma unroll
+              for (int z = 0; z < 4; ++z) {
+                const bool ok = z0 + z < p.ks;
+                const float4 *q = reinterpret_cast<const float4 *>(src + (z0 + z) * plane);
+                v[z][0] = ok ? __ldcg(q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[z][1] = ok ? __ldcg(q + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+              for (int z = 0; z < 4; ++z) {
+                pa[0] += v[z][0].x; pa[1] += v[z][0].y; pa[2] += v[z][0].z; pa[3] += v[z][0].w;
+                pa[4] += v[z][1].x; pa[5] += v[z][1].y; pa[6] += v[z][1].z; pa[7] += v[z][1].w;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              pa[q] = ldcg(p.pbuf + static_cast<size_t>(slot) * p.r + 8 * lane + q);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) h[q] = (lane < nq) ? siluf_(uu[q] + pa[q]) : 0.f;
+      } else {
+        // h in shared memory (r > 256): p summed over the chunks here
+        for (int q = lane; q < p.r; q += 32) {
+          float a = 0.f;
+          if (p.umma) {
+            for (int z = 0; z < p.ks; ++z)
+              a += ldcg(p.partial + z * plane + static_cast<size_t>(slot) * R + 3 * p.d_s + q);
+          } else {
+            a = ldcg(p.pbuf + static_cast<size_t>(slot) * p.r + q);
+          }
+          hbuf[q] = siluf_(__ldg(U + q) + a);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) h[q] = 0.f;
+      }
+      if (clock_me) {
+        const uint64_t now = global_ns();
+        p.ctrl->t_ns[13] += now - t_in;
+        t_in = now;
+      }
+      const int c_beg = wq * mq, c_end = min(p.M, c_beg + mq);
       for (int c0 = c_beg; c0 < c_end; c0 += G) {
         const int my_c = c0 + lane;
         const bool mine = lane < G && my_c < c_end;
@@ -954,100 +861,73 @@ __device__ void score_phase(const ChainParams &p, const int *slots, const int4 *
         float acc[G];
         int ids[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          ids[g] = __shfl_sync(kFull, my_id, g);
-          acc[g] = 0.f;
+        for (int q = 0; q < G; ++q) {
+          ids[q] = __shfl_sync(kFull, my_id, q);
+          acc[q] = 0.f;
         }
         if (SMALL_R && WDT == 1) {
           uint4 raw[G];                      // eight bf16 weights per row and lane
 #pragma unroll
-          for (int g = 0; g < G; ++g)
-            raw[g] = (ids[g] >= 0 && lane < nq)
+          for (int q = 0; q < G; ++q)
+            raw[q] = (ids[q] >= 0 && lane < nq)
                          ? __ldg(reinterpret_cast<const uint4 *>(
                                static_cast<const uint16_t *>(p.W2) +
-                               static_cast<size_t>(ids[g]) * p.r + 8 * lane))
+                               static_cast<size_t>(ids[q]) * p.r + 8 * lane))
                          : make_uint4(0u, 0u, 0u, 0u);
-          if (c0 == c_beg) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) h[i] = (lane < nq) ? siluf_(uu[i] + pa[i]) : 0.f;
-          }
+          for (int q = 0; q < G; ++q) {
+            const uint32_t w4[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const uint32_t w4[4] = {raw[g].x, raw[g].y, raw[g].z, raw[g].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              acc[g] = fmaf(__uint_as_float(w4[i] << 16), h[2 * i], acc[g]);
-              acc[g] = fmaf(__uint_as_float(w4[i] & 0xffff0000u), h[2 * i + 1], acc[g]);
+            for (int x = 0; x < 4; ++x) {
+              acc[q] = fmaf(__uint_as_float(w4[x] << 16), h[2 * x], acc[q]);
+              acc[q] = fmaf(__uint_as_float(w4[x] & 0xffff0000u), h[2 * x + 1], acc[q]);
             }
           }
         } else if (SMALL_R) {
           float wf[G][8];
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            if (ids[g] >= 0 && lane < nq) {
-              load8<WDT>(p.W2, static_cast<size_t>(ids[g]) * p.r + 8 * lane, wf[g]);
+          for (int q = 0; q < G; ++q) {
+            if (ids[q] >= 0 && lane < nq) {
+              load8<WDT>(p.W2, static_cast<size_t>(ids[q]) * p.r + 8 * lane, wf[q]);
             } else {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) wf[g][i] = 0.f;
+              for (int x = 0; x < 8; ++x) wf[q][x] = 0.f;
             }
           }
-          if (c0 == c_beg) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) h[i] = (lane < nq) ? siluf_(uu[i] + pa[i]) : 0.f;
-          }
+          for (int q = 0; q < G; ++q)
 #pragma unroll
-          for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[g] = fmaf(wf[g][i], h[i], acc[g]);
+            for (int x = 0; x < 8; ++x) acc[q] = fmaf(wf[q][x], h[x], acc[q]);
         } else {
-          if (c0 == c_beg) {
-            // h in shared memory (r > 256): p summed over the chunks here
-            for (int q = lane; q < p.r; q += 32) {
-              float a = 0.f;
-              if (psum) {
-                for (int z = 0; z < p.ks; ++z)
-                  a += ldcg(p.partial + z * plane + static_cast<size_t>(slot) * R + 3 * p.d_s + q);
-              } else {
-                a = ldcg(p.pbuf + static_cast<size_t>(slot) * p.r + q);
-              }
-              hbuf[q] = siluf_(__ldg(U + q) + a);
-            }
-            __syncwarp();
-          }
 #pragma unroll 1
           for (int q = lane; q - lane < nq; q += 32) {
             if (q < nq) {
               float hq[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) hq[i] = hbuf[8 * q + i];
+              for (int x = 0; x < 8; ++x) hq[x] = hbuf[8 * q + x];
 #pragma unroll
-              for (int g = 0; g < G; ++g) {
-                if (ids[g] >= 0) {
+              for (int y = 0; y < G; ++y) {
+                if (ids[y] >= 0) {
                   float wf[8];
-                  load8<WDT>(p.W2, static_cast<size_t>(ids[g]) * p.r + 8 * q, wf);
+                  load8<WDT>(p.W2, static_cast<size_t>(ids[y]) * p.r + 8 * q, wf);
 #pragma unroll
-                  for (int i = 0; i < 8; ++i) acc[g] = fmaf(wf[i], hq[i], acc[g]);
+                  for (int x = 0; x < 8; ++x) acc[y] = fmaf(wf[x], hq[x], acc[y]);
                 }
               }
             }
           }
         }
-        if (clock_me && c0 == c_beg) {
-          const uint64_t now = global_ns();
-          p.ctrl->t_ns[13] += now - t_in;
-          t_in = now;
-        }
         float my_dl = 0.f;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float dl = warp_sum(acc[g]);
-          if (g == lane) my_dl = dl;
+        for (int q = 0; q < G; ++q) {
+          const float dl = warp_sum(acc[q]);
+          if (q == lane) my_dl = dl;
         }
-        if (mine) Lsm[my_c] = my_id >= 0 ? __fdiv_rn(my_base + my_dl, T) : ninf;
+        if (mine) Lw[my_c] = my_id >= 0 ? __fdiv_rn(my_base + my_dl, T) : ninf;
       }
     }
     __syncthreads();
-    if (clock_me && live) {
+    if (clock_me) {
       const uint64_t now = global_ns();
       p.ctrl->t_ns[14] += now - t_in;
       t_in = now;
@@ -1057,35 +937,40 @@ __device__ void score_phase(const ChainParams &p, const int *slots, const int4 *
       float Lv[SLOTS];
       float mx = ninf;
 #pragma unroll
-      for (int s = 0; s < SLOTS; ++s) {
-        const int c = s * 32 + lane;
-        key[s] = 0ull;
-        Lv[s] = ninf;
-        if (c < p.M && fid[s] >= 0) {
-          Lv[s] = Lsm[c];
-          key[s] = make_key(Lv[s], static_cast<uint32_t>(fid[s]));
+      for (int s2 = 0; s2 < SLOTS; ++s2) {
+        const int ci = s2 * 32 + lane;
+        key[s2] = 0ull;
+        Lv[s2] = ninf;
+        if (ci < p.M && fid[s2] >= 0) {
+          Lv[s2] = Lw[ci];
+          key[s2] = make_key(Lv[s2], static_cast<uint32_t>(fid[s2]));
         }
-        mx = fmaxf(mx, Lv[s]);
+        mx = fmaxf(mx, Lv[s2]);
       }
       mx = warp_max(mx);
       float sum = 0.f;
 #pragma unroll
-      for (int s = 0; s < SLOTS; ++s)
-        if (s * 32 + lane < p.M) sum += expf(Lv[s] - mx);
+      for (int s2 = 0; s2 < SLOTS; ++s2)
+        if (s2 * 32 + lane < p.M) sum += expf(Lv[s2] - mx);
       sum = warp_sum(sum);
       const float lse = (mx == ninf) ? ninf : mx + logf(sum);
       warp_sort_desc<SLOTS>(key, lane);
-      const float base_score = __int_as_float(recs[n].w);
 #pragma unroll
-      for (int s = 0; s < SLOTS; ++s) {
-        const int i = s * 32 + lane;
-        if (i < p.k) {
-          const float L = key_value(key[s]);
+      for (int s2 = 0; s2 < SLOTS; ++s2) {
+        const int x = s2 * 32 + lane;
+        if (x < p.k) {
+          const float L = key_value(key[s2]);
           const float lp = (lse == ninf) ? ninf : L - lse;
-          const int tok = static_cast<int32_t>(key_id(key[s]));
-          p.kid_score[static_cast<size_t>(slot) * p.k + i] = base_score + lp;
-          p.kid_tok[static_cast<size_t>(slot) * p.k + i] = tok;
-          if (i < 2 && j < p.D)
+          const int tok = static_cast<int32_t>(key_id(key[s2]));
+          if (t) {
+            t->child_score[e * p.k + x] = base_score + lp;
+            t->child_tok[e * p.k + x] = tok;
+            t->child_exp[e * p.k + x] = -1;
+          } else {
+            p.kid_score[static_cast<size_t>(slot) * p.k + x] = base_score + lp;
+            p.kid_tok[static_cast<size_t>(slot) * p.k + x] = tok;
+          }
+          if (x < 2 && j < p.D)
             prefetch_l2(p.G + static_cast<size_t>(tok) * 3 * p.d_s,
                         static_cast<uint32_t>(12u * p.d_s));
         }
@@ -1094,6 +979,100 @@ __device__ void score_phase(const ChainParams &p, const int *slots, const int4 *
     }
     __syncthreads();
   }
+  if (!t && threadIdx.x == 0) {   // the scored columns' marks, after every warp's writes
+    __threadfence();
+    for (int c = g; c < cnt; c += p.grp)
+      if (cl.recs[first + c].x != kState0) st_release_u32(p.scored + slots[first + c], mark);
+  }
+}
+
+// GRU cells of member g's share of the request's chosen nodes (columns c = g,
+// g + G, ... of its new selection): S_e = GRU(S_parent, x = E[tok]) with the
+// input half the prepared row G[tok] (= W_ih E[tok] + b_ih) and the recurrent
+// half gh_parent (= W_hh S_parent + b_hh) from the GEMM that expanded the
+// parent (the root: state0 and the gh of the state0 column), once its gh mark
+// is set. The new state goes to the node store and, as the next GEMM's input,
+// to column b * P + c. Two items per thread in flight. False when a bounded
+// wait ran out.
+__device__ __forceinline__ float gru_unit(float gir, float giz, float gin, float ghr, float ghz,
+                                          float ghn, float sp) {
+  const float r = sigmoidf_(gir + ghr);
+  const float z = sigmoidf_(giz + ghz);
+  const float n = tanhf(gin + r * ghn);
+  return (1.f - z) * n + z * sp;
+}
+
+__device__ bool gru_cols(const ChainParams &p, int b, int g, const GhWork &help) {
+  __shared__ int4 s_rec[DT_MAX_SPEC];
+  __shared__ int s_n;
+  if (threadIdx.x == 0) {
+    const int n = __ldcg(p.col_count + b);
+    int m = 0;
+    for (int c = g; c < n; c += p.grp) s_rec[m++] = __ldcg(p.col_rec + b * p.P + c);
+    s_n = m;
+  }
+  __syncthreads();
+  const int mine = s_n;
+  if (mine == 0) return true;
+  // the parents' gh must be summed (tensor-core path: from this or an earlier step)
+  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
+  const uint64_t tw = clock_me ? global_ns() : 0;
+  if (p.umma &&
+      !wait_for(p, &help, [&] {
+        for (int i = 0; i < mine; ++i) {
+          const int r = s_rec[i].y & 0xffff;   // parent + 1
+          if (ld_acquire_u32(gh_mark_of(p, b, r - 1)) == 0u) return false;
+        }
+        return true;
+      }))
+    return false;
+  if (clock_me) p.ctrl->t_ns[8] += global_ns() - tw;
+  const int ds = p.d_s, q4 = ds / 4;
+  const int items = mine * q4;
+  const size_t ebase = static_cast<size_t>(b) * (p.e_cap + 1);
+  constexpr int IT = 2;
+  for (int i0 = threadIdx.x; i0 < items; i0 += IT * kThreads) {
+    float4 gi[IT][3], gh[IT][3], sp[IT];
+    int col[IT], u[IT];
+    size_t so[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      const int i = i0 + k * kThreads;
+      col[k] = -1;
+      if (i < items) {
+        const int m = i / q4;
+        u[k] = (i - m * q4) * 4;
+        col[k] = g + m * p.grp;
+        const int4 rec = s_rec[m];
+        const int e = rec.x, pe = (rec.y & 0xffff) - 1, tok = rec.z;
+        const float *gp = p.G + static_cast<size_t>(tok) * 3 * ds + u[k];
+        const float *ghp = p.gh_store + (ebase + (pe < 0 ? p.e_cap : pe)) * 3 * ds + u[k];
+        const float *spp = pe < 0 ? p.state0 + static_cast<size_t>(p.b0 + b) * ds + u[k]
+                                  : p.S_store + (ebase + pe) * ds + u[k];
+        so[k] = (ebase + e) * ds + u[k];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          gi[k][q] = __ldg(reinterpret_cast<const float4 *>(gp + q * ds));
+          gh[k][q] = __ldcg(reinterpret_cast<const float4 *>(ghp + q * ds));
+        }
+        sp[k] = __ldcg(reinterpret_cast<const float4 *>(spp));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      if (col[k] < 0) continue;
+      float4 v;
+      v.x = gru_unit(gi[k][0].x, gi[k][1].x, gi[k][2].x, gh[k][0].x, gh[k][1].x, gh[k][2].x, sp[k].x);
+      v.y = gru_unit(gi[k][0].y, gi[k][1].y, gi[k][2].y, gh[k][0].y, gh[k][1].y, gh[k][2].y, sp[k].y);
+      v.z = gru_unit(gi[k][0].z, gi[k][1].z, gi[k][2].z, gh[k][0].z, gh[k][1].z, gh[k][2].z, sp[k].z);
+      v.w = gru_unit(gi[k][0].w, gi[k][1].w, gi[k][2].w, gh[k][0].w, gh[k][1].w, gh[k][2].w, sp[k].w);
+      *reinterpret_cast<float4 *>(p.S_store + so[k]) = v;
+      write_column4(p, b * p.P + col[k], u[k], v);
+    }
+  }
+  if (p.umma) fence_async_global();   // the columns are read by bulk copies next
+  __syncthreads();
+  return true;
 }
 
 __device__ void write_row(const ChainParams &p, int b, int pos, int tok, int par, int dep,
@@ -1504,52 +1483,101 @@ __device__ void tail_init(const ChainParams &p, const Tables &t, TailState &ts, 
   __syncthreads();
 }
 
+// The request phase of one step, member g of request b's group (the leader,
+// g = 0, holds the request's tables): score the member's share of the last
+// GEMM's nodes; the leader gathers the members' children (waiting for their
+// marks), pops, chooses the next nodes and publishes them (the request's
+// mark); then every member runs the GRU of its share of them. False when a
+// bounded wait ran out.
 template <int WDT, int SLOTS>
-__device__ void tail_step(const ChainParams &p, const Tables &t, TailState &ts, int b) {
+__device__ bool group_step(const ChainParams &p, const Tables &t, TailState &ts, int b, int g,
+                           float *sm, const int *slots, const ColList &cl, const GhWork &help,
+                           unsigned mark) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ncols = ts.n_sel;
-  if (ts.e_count == 0) {
-    // the root: S_0 = GRU(state0, E[anchor]); its recurrent half came from the state0 column
+  const int first = cl.req_first[b], cnt = cl.req_cnt[b];
+  if (cnt == 0) return true;   // the request is done (or never started)
+  const bool leader = g == 0;
+  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
+  uint64_t t0 = clock_me ? global_ns() : 0;
+  auto lap = [&](int k) {
+    if (clock_me) {
+      const uint64_t now = global_ns();
+      p.ctrl->t_ns[k] += now - t0;
+      t0 = now;
+    }
+  };
+  if (leader && ts.e_count == 0) {
+    // the root: expansion 0, S_0 = GRU(state0, E[anchor]); its recurrent half
+    // comes from the state0 column of this step
     const int anchor = p.anchor[p.b0 + b];
     if (threadIdx.x == 0) {
       t.exp_depth[0] = 0; t.exp_parent[0] = -1; t.exp_score[0] = 0.0f; t.exp_tok[0] = anchor;
       ts.e_count = 1;
       ts.n_sel = 1;
-      atomicAdd(&p.ctrl->expansions, 1u);
       ts.sel_e[0] = 0;
+      atomicAdd(&p.ctrl->expansions, 1u);
       p.col_rec[b * p.P] = col_record(0, -1, 1, anchor, 0.0f);
       p.col_count[b] = 1;
     }
+  } else {
+    // 1. children of this member's nodes
+    float T = p.temperature ? p.temperature[p.b0 + b] : 1.0f;
+    T = (T == 0.0f) ? 1.0f : T;
+    if (p.r <= 256) score_cols<WDT, SLOTS, true>(p, leader ? &t : nullptr, b, g, cl, slots, T, mark, sm);
+    else score_cols<WDT, SLOTS, false>(p, leader ? &t : nullptr, b, g, cl, slots, T, mark, sm);
+    lap(2);
+    if (leader) {
+      // 2. the other members' children, once their marks are set
+      if (p.grp > 1 && cnt > 1 &&
+          !wait_for(p, nullptr, [&] {
+            for (int c = 1; c < cnt; ++c)
+              if (c % p.grp != 0 && cl.recs[first + c].x != kState0 &&
+                  ld_acquire_u32(p.scored + slots[first + c]) != mark)
+                return false;
+            return true;
+          }))
+        return false;
+      for (int i = threadIdx.x; i < cnt * p.k; i += kThreads) {
+        const int c = i / p.k, rank = i - c * p.k;
+        if (c % p.grp == 0) continue;
+        const int e = cl.recs[first + c].x;
+        if (e == kState0) continue;
+        const size_t src = static_cast<size_t>(slots[first + c]) * p.k + rank;
+        t.child_score[e * p.k + rank] = __ldcg(p.kid_score + src);
+        t.child_tok[e * p.k + rank] = __ldcg(p.kid_tok + src);
+        t.child_exp[e * p.k + rank] = -1;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0 && ts.n_runs == 0) {  // the root's children form the first run
+        t.run_e[0] = 0; t.run_head[0] = 0; t.run_pos[0] = 0;
+        t.run_hs[0] = head_score(p, t, 0, 0);
+        ts.n_runs = 1;
+      }
+      __syncthreads();
+      lap(3);
+      // 3. canonical pops, then the next expansions
+      if (warp == 0) {
+        if (p.N + 1 <= 128) replay_and_select_reg<4>(p, t, ts, b, lane);
+        else replay_and_select(p, t, ts, b, lane);
+      }
+      __syncthreads();
+      lap(4);
+      if (ts.done == 2) finalize(p, t, ts, b, true);   // (col_count[b] is 0)
+    }
+  }
+  // 4. the selection out (leader) or in (members), then the GRU cells
+  if (leader) {
     __syncthreads();
-    return;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      st_release_u32(p.sel_mark + b, mark);
+    }
+  } else if (!wait_for(p, &help, [&] { return ld_acquire_u32(p.sel_mark + b) == mark; })) {
+    return false;
   }
-  const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
-  uint64_t t0 = clock_me ? global_ns() : 0;
-  // 1. children of the nodes expanded by the last GEMM (scored grid-wide)
-  for (int i = threadIdx.x; i < ncols * p.k; i += kThreads) {
-    const int c = i / p.k, rank = i - c * p.k;
-    const int e = ts.sel_e[c];
-    const size_t src = static_cast<size_t>(b * p.P + c) * p.k + rank;
-    t.child_score[e * p.k + rank] = __ldcg(p.kid_score + src);
-    t.child_tok[e * p.k + rank] = __ldcg(p.kid_tok + src);
-    t.child_exp[e * p.k + rank] = -1;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && ts.n_runs == 0) {  // the root's children form the first run
-    t.run_e[0] = 0; t.run_head[0] = 0; t.run_pos[0] = 0;
-    t.run_hs[0] = head_score(p, t, 0, 0);
-    ts.n_runs = 1;
-  }
-  __syncthreads();
-  if (clock_me) { const uint64_t n = global_ns(); p.ctrl->t_ns[6] += n - t0; t0 = n; }
-  // 2. canonical pops, then the next expansions
-  if (warp == 0) {
-    if (p.N + 1 <= 128) replay_and_select_reg<4>(p, t, ts, b, lane);
-    else replay_and_select(p, t, ts, b, lane);
-  }
-  __syncthreads();
-  if (clock_me) { const uint64_t n = global_ns(); p.ctrl->t_ns[7] += n - t0; t0 = n; }
-  if (ts.done == 2) { finalize(p, t, ts, b, true); return; }
+  const bool ok = gru_cols(p, b, g, help);
+  lap(5);
+  return ok;
 }
 
 template <int WDT, int SLOTS>
@@ -1558,21 +1586,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
   __shared__ TailState ts;
   __shared__ int s_active;
   const Tables t = tables(p, smem);
-  const int b = blockIdx.x;
-  const bool tail = b < p.nb;
-  // tensor-core blocks: stationary A tile, two mbarriers, 256 TMEM columns
+  // request groups: blocks [b G, b G + G) serve request b; member 0 leads
+  const int b = blockIdx.x / p.grp, g = blockIdx.x % p.grp;
+  const bool grouped = b < p.nb;
+  const bool tail = grouped && g == 0;
+  // tensor-core blocks: stationary A tile, the slice mbarriers, 256 TMEM columns
   const bool mma_block = p.umma && blockIdx.x < p.n_mt * p.ks;
   UmmaState u;
   u.tmem = 0;
   u.next = 0;
-  u.cphase = 0;
   if (mma_block) {
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + p.sm_tmem);
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0)
       for (int i = 0; i < 2 * kBufs; ++i) mbar_init(&mbar[i], 1);   // full, empty
-      if (p.cluster) mbar_init(&mbar[2 * kBufs], static_cast<uint32_t>(p.cluster));
-    }
     load_a_tile(p, smem + p.sm_A);
     fence_async_smem();   // generic stores of the A tile -> tensor-core reads
     if ((threadIdx.x >> 5) == 0) tmem_alloc(tslot, kTmemCols);
@@ -1592,11 +1619,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     }
     fence_async_global();
   }
-  // every CTA's cluster barrier is initialised before any CTA arrives on it
-  if (p.cluster) cluster_sync_all();
+  // marks of an earlier launch must not read as this launch's
+  {
+    const int nm = p.cols_cap + p.cols_cap / p.P + (p.cols_cap / p.P) * (p.e_cap + 1);
+    for (int i = blockIdx.x * kThreads + threadIdx.x; i < nm; i += gridDim.x * kThreads)
+      p.scored[i] = 0u;   // scored, sel_mark and gh_mark are consecutive
+  }
   if (tail) tail_init(p, t, ts, b);
-  unsigned bar_target = 0, red_base = 0;
-  int next_total = -1;   // columns of the next GEMM when already listed in shared memory
+  unsigned bar_target = 0;
   bool ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
                          false, p.test_skip && blockIdx.x == gridDim.x - 1);
   // block 0 accounts its time per phase (for profiling; a few timer reads a step)
@@ -1609,55 +1639,53 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
       t_prev = now;
     }
   };
+  int *slots = reinterpret_cast<int *>(smem + p.sm_slots);
+  ColList cl;
+  cl.recs = reinterpret_cast<int4 *>(smem + p.sm_recs);
+  cl.req_first = slots + p.cols_cap;
+  cl.req_cnt = cl.req_first + p.nb;
+  float *scratch = reinterpret_cast<float *>(smem + p.sm_scratch);
   for (int step = 0; ok && step < p.N + 3; ++step) {
     if (clock_me) p.ctrl->steps = static_cast<unsigned>(step + 1);
     bool gemm_ok = true;
     int total = 0;
-    if (p.umma) gemm_ok = gemm_phase_umma(p, smem, smem + p.sm_scratch, u, next_total, total);
-    else gemm_phase<WDT>(p, smem + p.sm_scratch);
+    if (p.umma) {
+      gemm_ok = gemm_phase_umma(p, smem, slots, cl, u, total);
+    } else {
+      gemm_phase<WDT>(p, smem + p.sm_scratch);
+      total = compact_slots(p, slots, &cl);
+    }
     lap(0);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
                       !gemm_ok);
     lap(1);
     if (!ok) break;
-    // children of the new expansions (their p summed by the scorers), for the
-    // columns listed by the GEMM phase (the fp32 GEMM's staging overwrote them)
-    int *slots = reinterpret_cast<int *>(smem + p.sm_scratch);
-    int4 *recs = reinterpret_cast<int4 *>(smem + p.sm_scratch + ((p.cols_cap * 4 + 15) & ~15));
-    if (!p.umma) total = compact_slots(p, slots, recs);
-    {
-      float *sc = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(recs) +
-                                            static_cast<size_t>(p.cols_cap) * 16);
-      if (p.r <= 256) score_phase<WDT, SLOTS, true>(p, slots, recs, total, sc);
-      else score_phase<WDT, SLOTS, false>(p, slots, recs, total, sc);
+    // the column counter of the next step starts from zero (this one's was
+    // last used before the previous barrier)
+    unsigned *counter = (step & 1) ? &p.ctrl->red_next_odd : &p.ctrl->red_next;
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      *((step & 1) ? &p.ctrl->red_next : &p.ctrl->red_next_odd) = 0u;
+    const unsigned mark = static_cast<unsigned>(step + 1);
+    GhWork help;
+    help.slots = slots;
+    help.recs = cl.recs;
+    help.total = p.umma ? total : 0;   // (the CUDA-core GEMM writes gh itself)
+    help.counter = counter;
+    bool req_ok = true;
+    if (grouped) {
+      req_ok = group_step<WDT, SLOTS>(p, t, ts, b, g, scratch, slots, cl, help, mark);
+      if (clock_me) t_prev = global_ns();
     }
-    lap(2);
+    if (!req_ok && threadIdx.x == 0) atomicExch(&p.ctrl->abort, 1);
+    if (p.umma) gh_help(p, help);
+    lap(6);
     ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
-                      false);
-    lap(3);
-    if (!ok) break;
-    if (tail && !ts.done) tail_step<WDT, SLOTS>(p, t, ts, b);
-    if (p.umma && !p.cluster) gh_reduce(p, slots, recs, total, red_base);
-    lap(4);
-    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
-                      false);
-    lap(5);
+                      !req_ok);
+    lap(7);
     if (!ok) break;
     if (threadIdx.x == 0) s_active = ld_acquire_s32(&p.ctrl->active);
     __syncthreads();
     if (s_active == 0) break;
-    {
-      int *gslots = reinterpret_cast<int *>(smem + p.sm_scratch);
-      int4 *grecs = reinterpret_cast<int4 *>(smem + p.sm_scratch + ((p.cols_cap * 4 + 15) & ~15));
-      const int gtotal = compact_slots(p, gslots, grecs);
-      gru_phase(p, gslots, grecs, gtotal);
-      next_total = gtotal;   // the next GEMM's columns (col_count does not change before it)
-    }
-    lap(8);
-    ok = grid_barrier(&p.ctrl->bar_count, &p.ctrl->abort, gridDim.x, p.limit_ns, bar_target,
-                      false);
-    lap(16);
-    if (!ok) break;
   }
   if (tail && !ts.done) {
     if (threadIdx.x == 0) ts.status = DT_ERR_TIMEOUT;
@@ -1669,8 +1697,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     tmem_fence_after();
     if ((threadIdx.x >> 5) == 0) tmem_dealloc(u.tmem, kTmemCols);
   }
-  // no CTA leaves while another CTA of its cluster may still address its memory
-  if (p.cluster) cluster_sync_all();
 }
 
 }  // namespace
@@ -1699,13 +1725,14 @@ static int chain_smem_layout(const Plan &pl, int e_cap, int wave, ChainParams *c
   if (pl.umma) {
     cp->sm_A = off = al(off, 128);    off += 128 * pl.kc * 2;
     cp->sm_B = off = al(off, 128);    off += kBufs * kSliceBytes;
-    cp->sm_mbar = off = al(off, 16);  off += 16 * kBufs + 8;
+    cp->sm_mbar = off = al(off, 16);  off += 16 * kBufs;
     cp->sm_tmem = off;                off += 16;
   }
-  cp->sm_scratch = off = al(off, 16);   // holds int4 column records
+  cp->sm_slots = off = al(off, 16);   off += (wave * pl.spec + 2 * wave) * 4;   // slots, per request
+  cp->sm_recs = off = al(off, 16);    off += wave * pl.spec * 16;
+  cp->sm_scratch = off = al(off, 16);
   const int gemm_scratch = al(wave * pl.spec * 4, 16) + (pl.umma ? 0 : kGemmCols * kGemmKC * 4);
-  const int score_scratch = al(wave * pl.spec * 4, 16) + wave * pl.spec * 16 + kNPB * d.M * 4 +
-                            (d.r > 256 ? kWarps * d.r * 4 : 0);
+  const int score_scratch = kWarps * d.M * 4 + (d.r > 256 ? kWarps * d.r * 4 : 0);
   off += gemm_scratch > score_scratch ? gemm_scratch : score_scratch;
   cp->sm_total = off;
   return off;
@@ -1758,20 +1785,27 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.gin = reinterpret_cast<float *>(w + pl.off_gin);
   cp.pbuf = reinterpret_cast<float *>(w + pl.off_p);
   cp.col_rec = reinterpret_cast<int4 *>(w + pl.off_colinfo);
-  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc; cp.cluster = pl.cluster;
+  cp.kid_score = reinterpret_cast<float *>(w + pl.off_kids);
+  cp.kid_tok = reinterpret_cast<int32_t *>(cp.kid_score +
+                                           static_cast<size_t>(pl.wave) * pl.spec * d.k);
+  cp.scored = reinterpret_cast<unsigned *>(w + pl.off_ghflag);
+  cp.sel_mark = cp.scored + static_cast<size_t>(pl.wave) * pl.spec;
+  cp.gh_mark = cp.sel_mark + pl.wave;
+  {
+    const int gsz = pl.chain_grid / a.nb;
+    cp.grp = gsz < 1 ? 1 : (gsz > pl.spec ? pl.spec : gsz);
+  }
+  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc;
   cp.cols_cap = pl.wave * pl.spec;
   cp.partial = pl.umma ? reinterpret_cast<float *>(w + pl.off_partial) : nullptr;
   cp.gin16 = pl.umma ? reinterpret_cast<uint16_t *>(w + pl.off_gin16) : nullptr;
   cp.col_count = reinterpret_cast<int *>(w + pl.off_colexp);
-  cp.kid_score = reinterpret_cast<float *>(w + pl.off_kids);
-  cp.kid_tok = reinterpret_cast<int32_t *>(cp.kid_score +
-                                           static_cast<size_t>(pl.wave) * pl.spec * d.k);
   cp.ctrl = reinterpret_cast<Ctrl *>(w + pl.off_ctrl);
   cp.req_flags = reinterpret_cast<const int *>(w + pl.off_ctrl + kCtrlHeader +
                                                sizeof(unsigned) * static_cast<size_t>(d.batch) * d.D);
   cp.tokens = a.out->tokens; cp.parents = a.out->parents; cp.depths = a.out->depths;
   cp.scores = a.out->scores; cp.mask = a.out->mask; cp.status = a.out->status;
-  cp.limit_ns = pl.test_timeout ? 2000000ull : 10000000000ull;  // per bounded wait
+  cp.limit_ns = pl.test_timeout ? 2000000ull : 2000000000ull;  // per bounded wait
   cp.test_skip = pl.test_timeout;
   const void *fn = chain_kernel_ptr(pl.wdtype, d.M);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1780,29 +1814,9 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   // the barrier counters of the control block are re-zeroed for every wave
   e = cudaMemsetAsync(cp.ctrl, 0, sizeof(Ctrl), st);
   if (e != cudaSuccess) return e;
-  const int cdim = pl.cluster;
-  if (!cdim) {
-    void *args[] = {&cp};
-    return cudaLaunchCooperativeKernel(fn, dim3(pl.chain_grid), dim3(kThreads), args,
-                                       pl.chain_smem, st);
-  }
-  // cooperative (co-resident grid) and clustered: the K chunks of an M tile
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = static_cast<unsigned>(cdim);
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  at[1].id = cudaLaunchAttributeCooperative;
-  at[1].val.cooperative = 1;
-  cfg.gridDim = dim3(pl.chain_grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = pl.chain_smem;
-  cfg.stream = st;
-  cfg.attrs = at;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, reinterpret_cast<void (*)(ChainParams)>(const_cast<void *>(fn)),
-                            cp);
+  void *args[] = {&cp};
+  return cudaLaunchCooperativeKernel(fn, dim3(pl.chain_grid), dim3(kThreads), args,
+                                     pl.chain_smem, st);
 }
 
 }  // namespace dt

@@ -21,7 +21,6 @@ struct Plan {
   int proj_ksplit;     // K split of the projection GEMM
   int umma;            // search GEMM on tcgen05 (bf16 weights)
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
-  int cluster;         // 0, or the cluster size (= ks) of the search launch
   int test_timeout;    // DT_OPT_TEST_BARRIER_TIMEOUT
   int marginal;        // DT_OPT_MARGINAL: top-M, then the marginal tree kernel
   int num_sms;
@@ -30,31 +29,32 @@ struct Plan {
   size_t chain_smem;   // dynamic shared memory of the search kernel
   // workspace carve-up (byte offsets)
   size_t off_ctrl, off_part, off_cand_id, off_cand_val, off_U, off_S, off_gh, off_gin, off_p,
-      off_colexp, off_colinfo, off_kids, off_upart, off_partial, off_gin16, off_end;
+      off_colexp, off_colinfo, off_kids, off_ghflag, off_upart, off_partial, off_gin16, off_end;
   size_t off_gemm_tickets;  // inside the control region
 };
 
 // Control block at the start of the workspace; zeroed by every call.
 struct Ctrl {
   unsigned int bar_count;  // grid barrier arrivals (monotonic within a launch)
-  unsigned int red_next;   // chunk counter of the gh sums (monotonic within a launch)
+  unsigned int red_next;   // column counter of the gh sums of even steps
   int abort;           // set when a bounded wait expired
   int active;          // requests of the current wave still searching
   unsigned int steps;      // lockstep steps of the last search launch
   unsigned int expansions; // expansions of the last search launch
-  unsigned int pad[2];
-  // block 0 of the last search launch, ns summed over steps: [0] GEMM,
-  // [1] barrier, [2] scoring + reduction, [3] barrier, [4] tail, [5] barrier;
-  // tail parts: [6] reading the children, [7] pops and selection; [8] GRU
-  // phase; GEMM parts: [9] MMA loop, [10] epilogue, [11] waits for B copies,
-  // [12] waits for MMA completion; scoring of block 0's first node: [13] h,
-  // [14] candidate loop (incl. block sync), [15] softmax + sort + write;
-  // [16] barrier after the GRU phase; cluster sum of the GEMM: [17] barrier
-  // before the stores, [18] stores, [19] barrier after them, [20] sums;
-  // GEMM issuing thread, in SM cycles: [24] waits for free buffers, [25] waits
-  // for landed copies, [26] copy issue, [27] MMA issue; request 0's replay:
-  // [28] pop iterations, [29] their cycles, [30] selection iterations, [31]
-  // their cycles
+  unsigned int red_next_odd;  // column counter of the gh sums of odd steps
+  unsigned int pad;
+  // block 0 of the last search launch, ns summed over steps: [0] GEMM phase,
+  // [1] barrier after it; as request 0's leader: [2] scoring its nodes, [3]
+  // waiting for and gathering the other members' children, [4] pops and
+  // selection, [5] GRU cells (with the waits for the parents' gh); [6] gh
+  // sums after the request phase, [7] barrier after the request phase, [8]
+  // the part of [5] spent waiting for the parents' gh;
+  // GEMM parts: [9] MMA loop, [10] epilogue, [12] waits for MMA completion;
+  // scoring of block 0's nodes: [13] h, [14] candidate loop, [15] softmax +
+  // sort + children; GEMM issuing thread, in SM cycles: [24] waits for free
+  // buffers, [25] waits for landed copies, [26] copy issue, [27] MMA issue;
+  // request 0's replay: [28] pop iterations, [29] their cycles, [30] selection
+  // iterations, [31] their cycles
   unsigned long long t_ns[32];
   // followed by: unsigned row_ticket[batch * D]; int req_flags[batch]; gemm tickets
 };

@@ -111,13 +111,6 @@ typedef struct {
   int flags;          /* DT_OPT_* bits; 0 = defaults */
 } dt_options;
 
-/* dt_options.flags: sum the K chunks of the search GEMM inside thread-block
- * clusters, in distributed shared memory, instead of through global memory
- * (used only when the clusters fit on the GPU at once; measured slower than
- * the default at the shapes tested). The trees agree with the default path
- * up to the rounding of a different K split. */
-#define DT_OPT_CLUSTER_SUM 1
-
 /* dt_options.flags, test hook for failure detection: in the search launch the
  * last block skips its first grid-barrier arrival and every barrier wait is
  * limited to 2 ms, so the other blocks' bounded waits run out. Every request

@@ -225,28 +225,6 @@ def test_host_io_variant_matches_device():
         np.testing.assert_array_equal(out[key].numpy(), dev[key])
 
 
-# ------------------------------- search GEMM with cluster K-chunk sums
-
-@pytest.mark.parametrize("name", ["bf16-bias-state0-T", "big-ds", "wide-M100", "M256-k32"])
-def test_cluster_sum_path(name):
-    """The K-chunk sums in distributed shared memory (DT_OPT_CLUSTER_SUM)
-    against the oracle."""
-    wl = W.custom_workload(name=name, **SHAPES[name])
-    tb = dt.TreeBuilder.from_numpy(wl, flags=dt.OPT_CLUSTER_SUM)
-    g = run_gpu(wl, builder=tb)
-    check_against_oracle(wl, g, list(range(wl.batch)), max_near_ties=1)
-
-
-def test_config3_cluster_sum_sampled():
-    wl = workload(3)
-    tb = dt.TreeBuilder.from_numpy(wl, flags=dt.OPT_CLUSTER_SUM)
-    g = run_gpu(wl, builder=tb)
-    for b in range(wl.batch):
-        assert g["status"][b] == 0
-        check_structure(wl, b, g)
-    check_against_oracle(wl, g, [3, 17], max_near_ties=1)
-
-
 # --------------------------------------------- more requests than one wave
 
 def test_batch_beyond_one_wave():

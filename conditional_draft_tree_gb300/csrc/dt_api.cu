@@ -185,10 +185,10 @@ int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, P
   p->off_p = off;         off = al(off + sizeof(float) * cols * d.r);
   p->off_colexp = off;    off = al(off + sizeof(int) * (cols + wave));
   p->off_colinfo = off;   off = al(off + (3 * sizeof(int) + sizeof(float)) * cols);
-  p->off_kids = off;      off = al(off + (sizeof(float) + sizeof(int32_t)) * cols * d.k);
-  // marks: per column, per request, per (request, expansion slot)
+  p->off_kids = off;      off = al(off + sizeof(unsigned long long) * cols * d.k);
+  // marks: per request, per (request, expansion slot)
   p->off_ghflag = off;
-  off = al(off + sizeof(unsigned) * (cols + wave + slots_e));
+  off = al(off + sizeof(unsigned) * (wave + slots_e));
   p->off_upart = off;
   off = al(off + (p->proj_ksplit > 1 ? sizeof(float) * p->proj_ksplit * rows * d.r : 0));
   p->off_partial = off;

@@ -63,6 +63,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kGemmCols = 8;     // columns per GEMM work unit (fp32 path)
 constexpr int kGemmKC = 1024;    // K chunk staged in shared memory (fp32 path)
 constexpr int kState0 = -2;      // column code: the state0 column of the first step
+constexpr unsigned long long kEmptyKid = ~0ull;   // a child word not yet written
 
 struct ChainParams {
   int V, d, d_s, r, D, M, k, N;
@@ -79,14 +80,14 @@ struct ChainParams {
   float *S_store, *gh_store, *gin, *pbuf;
   int *col_count;
   // per GEMM column (slot = request * P + rank): its record (see col_record)
-  // and, when a member of the request's group scored it, its k children
+  // and, when a member of the request's group scored it, its k children as
+  // 64-bit words (token << 32 | score bits); kEmptyKid until written
   int4 *col_rec;
-  float *kid_score;
-  int32_t *kid_tok;
-  // marks (release / acquire, zeroed at launch): per slot, step + 1 once its
-  // children are out; per request, step + 1 once its selection is out; per
-  // (request, expansion), nonzero once the expansion's gh is in gh_store
-  unsigned *scored, *sel_mark, *gh_mark;
+  unsigned long long *kids;
+  // marks (release / acquire, zeroed at launch): per request, step + 1 once
+  // its selection is out; per (request, expansion), nonzero once the
+  // expansion's gh is in gh_store
+  unsigned *sel_mark, *gh_mark;
   int grp;             // blocks per request group (leader = member 0)
   // tensor-core GEMM path (bf16 weights): A tiles of 128 rows x kc K stay in
   // shared memory; the input columns arrive as three bf16 terms per state
@@ -558,11 +559,9 @@ __device__ void gh_column(const ChainParams &p, int slot, const int4 &rec) {
       reinterpret_cast<float4 *>(dst)[i] = a;
     }
   }
+  // the block barrier orders every thread's stores before thread 0's release
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    st_release_u32(gh_mark_of(p, b, e), 1u);
-  }
+  if (threadIdx.x == 0) st_release_u32(gh_mark_of(p, b, e), 1u);
 }
 
 // One grab from the step's column counter: the index of a column to sum, or
@@ -750,12 +749,12 @@ __device__ __forceinline__ void write_column4(const ChainParams &p, int slot, in
 // W2[c,:] h) / T of the M candidates, then the log-sum-exp over them and the k
 // best (L desc, id asc) as the node's children, with scores score(node) + L_c
 // - lse: into the request's shared tables when this block is the group's
-// leader (t != nullptr), else to global memory with the column's mark. The
-// prepared rows of the two best children (the likeliest next expansions) are
+// leader (t != nullptr), else to global memory as self-validating words. The
+// prepared rows of the four best children (the likeliest next expansions) are
 // fetched into L2.
 template <int WDT, int SLOTS, bool SMALL_R>
 __device__ void score_cols(const ChainParams &p, const Tables *t, int b, int g, const ColList &cl,
-                           const int *slots, float T, unsigned mark, float *sm) {
+                           const int *slots, float T, float *sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nq = p.r / 8;
   const int R = 3 * p.d_s + p.r;
@@ -797,6 +796,12 @@ __device__ void score_cols(const ChainParams &p, const Tables *t, int b, int g, 
       fid[s] = (live && wq == 0 && ci < p.M) ? __ldg(cid + ci) : -1;
     }
     if (live) {
+      const int c_beg = wq * mq, c_end = min(p.M, c_beg + mq);
+      // the first group's ids and base values, in the same round trip as the
+      // p partials and U below
+      const bool mine0 = lane < G && c_beg + lane < c_end;
+      const int id0 = mine0 ? __ldg(cid + c_beg + lane) : -1;
+      const float base0 = mine0 ? __ldg(cval + c_beg + lane) : 0.f;
       float h[8];
       if (SMALL_R) {
         float pa[8], uu[8];
@@ -852,12 +857,11 @@ __device__ void score_cols(const ChainParams &p, const Tables *t, int b, int g, 
         p.ctrl->t_ns[13] += now - t_in;
         t_in = now;
       }
-      const int c_beg = wq * mq, c_end = min(p.M, c_beg + mq);
       for (int c0 = c_beg; c0 < c_end; c0 += G) {
         const int my_c = c0 + lane;
         const bool mine = lane < G && my_c < c_end;
-        const int my_id = mine ? __ldg(cid + my_c) : -1;
-        const float my_base = mine ? __ldg(cval + my_c) : 0.f;
+        const int my_id = c0 == c_beg ? id0 : (mine ? __ldg(cid + my_c) : -1);
+        const float my_base = c0 == c_beg ? base0 : (mine ? __ldg(cval + my_c) : 0.f);
         float acc[G];
         int ids[G];
 #pragma unroll
@@ -967,10 +971,13 @@ __device__ void score_cols(const ChainParams &p, const Tables *t, int b, int g, 
             t->child_tok[e * p.k + x] = tok;
             t->child_exp[e * p.k + x] = -1;
           } else {
-            p.kid_score[static_cast<size_t>(slot) * p.k + x] = base_score + lp;
-            p.kid_tok[static_cast<size_t>(slot) * p.k + x] = tok;
+            // one 64-bit store per child: the leader sees it whole or not at all
+            const unsigned long long w =
+                (static_cast<unsigned long long>(static_cast<uint32_t>(tok)) << 32) |
+                __float_as_uint(base_score + lp);
+            st_relaxed_u64(p.kids + static_cast<size_t>(slot) * p.k + x, w);
           }
-          if (x < 2 && j < p.D)
+          if (x < 4 && j < p.D)
             prefetch_l2(p.G + static_cast<size_t>(tok) * 3 * p.d_s,
                         static_cast<uint32_t>(12u * p.d_s));
         }
@@ -978,11 +985,6 @@ __device__ void score_cols(const ChainParams &p, const Tables *t, int b, int g, 
       if (clock_me) p.ctrl->t_ns[15] += global_ns() - t_in;
     }
     __syncthreads();
-  }
-  if (!t && threadIdx.x == 0) {   // the scored columns' marks, after every warp's writes
-    __threadfence();
-    for (int c = g; c < cnt; c += p.grp)
-      if (cl.recs[first + c].x != kState0) st_release_u32(p.scored + slots[first + c], mark);
   }
 }
 
@@ -1002,18 +1004,35 @@ __device__ __forceinline__ float gru_unit(float gir, float giz, float gin, float
   return (1.f - z) * n + z * sp;
 }
 
-__device__ bool gru_cols(const ChainParams &p, int b, int g, const GhWork &help) {
+__device__ bool gru_cols(const ChainParams &p, int b, int g, const GhWork &help,
+                         const Tables *t, const TailState *ts) {
   __shared__ int4 s_rec[DT_MAX_SPEC];
   __shared__ int s_n;
   if (threadIdx.x == 0) {
-    const int n = __ldcg(p.col_count + b);
     int m = 0;
-    for (int c = g; c < n; c += p.grp) s_rec[m++] = __ldcg(p.col_rec + b * p.P + c);
+    if (t) {   // the leader: its own tables (ts->n_sel is 0 once it is done)
+      const int n = ts->done ? 0 : ts->n_sel;
+      for (int c = g; c < n; c += p.grp) {
+        const int e = ts->sel_e[c];
+        s_rec[m++] = col_record(e, t->exp_parent[e], 0, t->exp_tok[e], 0.0f);
+      }
+    } else {
+      const int n = __ldcg(p.col_count + b);
+      for (int c = g; c < n; c += p.grp) s_rec[m++] = __ldcg(p.col_rec + b * p.P + c);
+    }
     s_n = m;
   }
   __syncthreads();
   const int mine = s_n;
   if (mine == 0) return true;
+  if (threadIdx.x < mine) {   // the rows that do not wait for a gh sum, on their way to L2
+    const int4 rec = s_rec[threadIdx.x];
+    const int pe = (rec.y & 0xffff) - 1;
+    prefetch_l2(p.G + static_cast<size_t>(rec.z) * 3 * p.d_s, static_cast<uint32_t>(12u * p.d_s));
+    if (pe >= 0)
+      prefetch_l2(p.S_store + (static_cast<size_t>(b) * (p.e_cap + 1) + pe) * p.d_s,
+                  static_cast<uint32_t>(4u * p.d_s));
+  }
   // the parents' gh must be summed (tensor-core path: from this or an earlier step)
   const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
   const uint64_t tw = clock_me ? global_ns() : 0;
@@ -1483,6 +1502,54 @@ __device__ void tail_init(const ChainParams &p, const Tables &t, TailState &ts, 
   __syncthreads();
 }
 
+// The leader's gather of the other members' children (columns c of request b
+// with c % grp != 0): every thread polls its share of the child words until
+// each is written, copies them into the tables and empties them again. The
+// words were emptied at launch and after the previous step's gather, and the
+// grid barrier orders both before this step's writes. False when the limit
+// passes or another block aborted.
+__device__ bool gather_kids(const ChainParams &p, const Tables &t, int b, const ColList &cl,
+                            const int *slots) {
+  __shared__ int s_give_up;
+  const int first = cl.req_first[b], cnt = cl.req_cnt[b];
+  const int nent = cnt * p.k;
+  uint64_t t0 = 0;
+  if (threadIdx.x == 0) s_give_up = 0;
+  for (uint32_t it = 0;; ++it) {
+    bool ok = true;
+    for (int i = threadIdx.x; i < nent; i += kThreads) {
+      const int c = i / p.k, rank = i - c * p.k;
+      if (c % p.grp == 0) continue;
+      const int e = cl.recs[first + c].x;
+      if (e == kState0) continue;
+      const unsigned long long w =
+          ld_relaxed_u64(p.kids + static_cast<size_t>(slots[first + c]) * p.k + rank);
+      if (w == kEmptyKid) {
+        ok = false;
+      } else {
+        t.child_score[e * p.k + rank] = __uint_as_float(static_cast<uint32_t>(w));
+        t.child_tok[e * p.k + rank] = static_cast<int32_t>(w >> 32);
+        t.child_exp[e * p.k + rank] = -1;
+      }
+    }
+    if (__syncthreads_and(ok)) break;
+    if (threadIdx.x == 0 && (it & 15u) == 0u) {
+      const uint64_t now = global_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > p.limit_ns || ld_acquire_s32(&p.ctrl->abort)) s_give_up = 1;
+    }
+    __syncthreads();
+    if (s_give_up) return false;
+  }
+  for (int i = threadIdx.x; i < nent; i += kThreads) {
+    const int c = i / p.k, rank = i - c * p.k;
+    if (c % p.grp != 0 && cl.recs[first + c].x != kState0)
+      p.kids[static_cast<size_t>(slots[first + c]) * p.k + rank] = kEmptyKid;
+  }
+  __syncthreads();
+  return true;
+}
+
 // The request phase of one step, member g of request b's group (the leader,
 // g = 0, holds the request's tables): score the member's share of the last
 // GEMM's nodes; the leader gathers the members' children (waiting for their
@@ -1523,31 +1590,13 @@ __device__ bool group_step(const ChainParams &p, const Tables &t, TailState &ts,
     // 1. children of this member's nodes
     float T = p.temperature ? p.temperature[p.b0 + b] : 1.0f;
     T = (T == 0.0f) ? 1.0f : T;
-    if (p.r <= 256) score_cols<WDT, SLOTS, true>(p, leader ? &t : nullptr, b, g, cl, slots, T, mark, sm);
-    else score_cols<WDT, SLOTS, false>(p, leader ? &t : nullptr, b, g, cl, slots, T, mark, sm);
+    if (p.r <= 256) score_cols<WDT, SLOTS, true>(p, leader ? &t : nullptr, b, g, cl, slots, T, sm);
+    else score_cols<WDT, SLOTS, false>(p, leader ? &t : nullptr, b, g, cl, slots, T, sm);
     lap(2);
     if (leader) {
-      // 2. the other members' children, once their marks are set
-      if (p.grp > 1 && cnt > 1 &&
-          !wait_for(p, nullptr, [&] {
-            for (int c = 1; c < cnt; ++c)
-              if (c % p.grp != 0 && cl.recs[first + c].x != kState0 &&
-                  ld_acquire_u32(p.scored + slots[first + c]) != mark)
-                return false;
-            return true;
-          }))
-        return false;
-      for (int i = threadIdx.x; i < cnt * p.k; i += kThreads) {
-        const int c = i / p.k, rank = i - c * p.k;
-        if (c % p.grp == 0) continue;
-        const int e = cl.recs[first + c].x;
-        if (e == kState0) continue;
-        const size_t src = static_cast<size_t>(slots[first + c]) * p.k + rank;
-        t.child_score[e * p.k + rank] = __ldcg(p.kid_score + src);
-        t.child_tok[e * p.k + rank] = __ldcg(p.kid_tok + src);
-        t.child_exp[e * p.k + rank] = -1;
-      }
-      __syncthreads();
+      // 2. the other members' children: their words, polled until every one is
+      //    written, then emptied again for the next step
+      if (p.grp > 1 && cnt > 1 && !gather_kids(p, t, b, cl, slots)) return false;
       if (threadIdx.x == 0 && ts.n_runs == 0) {  // the root's children form the first run
         t.run_e[0] = 0; t.run_head[0] = 0; t.run_pos[0] = 0;
         t.run_hs[0] = head_score(p, t, 0, 0);
@@ -1568,14 +1617,11 @@ __device__ bool group_step(const ChainParams &p, const Tables &t, TailState &ts,
   // 4. the selection out (leader) or in (members), then the GRU cells
   if (leader) {
     __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      st_release_u32(p.sel_mark + b, mark);
-    }
+    if (threadIdx.x == 0) st_release_u32(p.sel_mark + b, mark);
   } else if (!wait_for(p, &help, [&] { return ld_acquire_u32(p.sel_mark + b) == mark; })) {
     return false;
   }
-  const bool ok = gru_cols(p, b, g, help);
+  const bool ok = gru_cols(p, b, g, help, leader ? &t : nullptr, leader ? &ts : nullptr);
   lap(5);
   return ok;
 }
@@ -1619,11 +1665,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     }
     fence_async_global();
   }
-  // marks of an earlier launch must not read as this launch's
+  // marks and child words of an earlier launch must not read as this launch's
   {
-    const int nm = p.cols_cap + p.cols_cap / p.P + (p.cols_cap / p.P) * (p.e_cap + 1);
+    const int wave = p.cols_cap / p.P;
+    const int nm = wave + wave * (p.e_cap + 1);
     for (int i = blockIdx.x * kThreads + threadIdx.x; i < nm; i += gridDim.x * kThreads)
-      p.scored[i] = 0u;   // scored, sel_mark and gh_mark are consecutive
+      p.sel_mark[i] = 0u;   // sel_mark and gh_mark are consecutive
+    for (int i = blockIdx.x * kThreads + threadIdx.x; i < p.cols_cap * p.k;
+         i += gridDim.x * kThreads)
+      p.kids[i] = kEmptyKid;
   }
   if (tail) tail_init(p, t, ts, b);
   unsigned bar_target = 0;
@@ -1785,11 +1835,8 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
   cp.gin = reinterpret_cast<float *>(w + pl.off_gin);
   cp.pbuf = reinterpret_cast<float *>(w + pl.off_p);
   cp.col_rec = reinterpret_cast<int4 *>(w + pl.off_colinfo);
-  cp.kid_score = reinterpret_cast<float *>(w + pl.off_kids);
-  cp.kid_tok = reinterpret_cast<int32_t *>(cp.kid_score +
-                                           static_cast<size_t>(pl.wave) * pl.spec * d.k);
-  cp.scored = reinterpret_cast<unsigned *>(w + pl.off_ghflag);
-  cp.sel_mark = cp.scored + static_cast<size_t>(pl.wave) * pl.spec;
+  cp.kids = reinterpret_cast<unsigned long long *>(w + pl.off_kids);
+  cp.sel_mark = reinterpret_cast<unsigned *>(w + pl.off_ghflag);
   cp.gh_mark = cp.sel_mark + pl.wave;
   {
     const int gsz = pl.chain_grid / a.nb;

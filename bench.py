@@ -51,6 +51,8 @@ def parse():
                     help="skip the Domino chain-decoding leg")
     ap.add_argument("--no-marginal", action="store_true",
                     help="skip the marginal-score (W2 = 0 ablation) leg")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the legs of the other configurations (0, 1, 2, 4)")
     ap.add_argument("--flags", type=int, default=0,
                     help="dt_options flags (DT_OPT_* bits of include/dt.h)")
     return ap.parse_args()
@@ -61,8 +63,11 @@ def peaks():
     if os.path.exists(p):
         d = json.load(open(p))
         return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained",
+                                                      d["bf16_tflops"])),
                     sm_max_mhz=float(d.get("sm_max_mhz", 2070.0)), source="measured")
-    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, sm_max_mhz=2070.0, source="fallback")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                sm_max_mhz=2070.0, source="fallback")
 
 
 class Clocks:
@@ -111,11 +116,64 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def oracle_sample(wl, reqs, threads):
+def oracle_sample(wl, reqs, threads, keep=False):
+    """Seconds the oracle takes for `reqs` on `threads` host threads (and the
+    trees when `keep`)."""
     import oracle
     t0 = time.perf_counter()
-    oracle.build_trees(wl, reqs, threads=threads, mask=True, topm_out=False)
-    return time.perf_counter() - t0
+    trees = oracle.build_trees(wl, reqs, threads=threads, mask=True, topm_out=keep)
+    dt_s = time.perf_counter() - t0
+    return (dt_s, dict(zip(reqs, trees))) if keep else dt_s
+
+
+def source_sha(path):
+    import hashlib
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(profile, source):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
+    kernel from a committed ncu summary, or None when the summary is missing
+    or was taken on another version of the kernel's source file."""
+    path = os.path.join(ROOT, "profiles", profile)
+    try:
+        d = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    if d.get("source_sha") != source_sha(os.path.join(ROOT, source)):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def parity_block(wl, g, refs):
+    """Oracle parity of the GPU trees `g` over the requests of `refs` (the
+    build's bar: top-M bit-exact, topology exact outside near ties within 1e-4,
+    scores within 1e-5): counts, or the first violation as a string."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import _parity
+    try:
+        return _parity.parity_summary(wl, g, refs)
+    except AssertionError as e:
+        return {"violation": str(e)[:300]}
 
 
 def algorithmic_counts(wl, out_tokens, out_depths):
@@ -350,6 +408,60 @@ def adaptive_leg(dt, torch, dev, st, K, out, N, c_fixed=1.0, c_node=1.0 / 256):
             "share_at_full_budget": float((c == N).float().mean())}
 
 
+def config_leg(c, wl, dt, torch, np, dev, flush, st, K, Wm, with_parity, oracle_reqs):
+    """One configuration of the build: device weights and inputs, Wm warm-up
+    and K timed rounds (CUDA events on the stream, L2 flushed before each),
+    round time, trees/s, the round's algorithmic HBM bytes against the measured
+    copy peak, the search GEMM flops against the measured bf16 peak, status of
+    every request and, when asked (bench rank 0 at N = 1), oracle parity on
+    `oracle_reqs`."""
+    tb = dt.TreeBuilder.from_numpy(wl, device=dev)
+    inp = tb.inputs_to_device(wl)
+    out = dt.alloc_outputs(tb.dims, dev)
+    ph = [[torch.cuda.Event(enable_timing=True) for _ in range(dt.NUM_PHASE_EVENTS)]
+          for _ in range(K)]
+    for evs in ph:
+        for e in evs:
+            e.record(st)
+    for _ in range(Wm):
+        flush.fill_(1)
+        tb.run(**inp, out=out)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0xff)
+        tb.run(**inp, out=out, opt=dt.options(0, ph[i]))
+    torch.cuda.synchronize()
+    per = sorted(ph[i][0].elapsed_time(ph[i][3]) for i in range(K))
+    search = statistics.median(ph[i][2].elapsed_time(ph[i][3]) for i in range(K))
+    ms = statistics.median(per)
+    o = {k: v.cpu().numpy() for k, v in out.items() if v is not None}
+    cnt = algorithmic_counts(wl, o["tokens"], o["depths"])
+    pk = peaks()
+    rb = cnt["topm_bytes"] + cnt["proj_bytes"] + cnt["search_bytes"]
+    ctrl = tb.workspace[:32].view(torch.int32).cpu().tolist()
+    leg = {"workload": f"{wl.name}: V={wl.V} d={wl.d} d_s={wl.d_s} r={wl.r} D={wl.D} M={wl.M} "
+                       f"k={wl.k} N={wl.N} batch={wl.batch} {wl.wdtype}",
+           "us_per_round_median": 1000.0 * ms, "us_per_round_min": 1000.0 * per[0],
+           "trees_per_s": wl.batch / (ms * 1e-3), "rounds": K,
+           "search_us_median": 1000.0 * search, "search_steps": ctrl[4],
+           "round_algorithmic_bytes": rb,
+           "round_hbm_gbs": rb / (ms * 1e-3) / 1e9,
+           "round_hbm_frac": rb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+           "search_gemm_tflops": cnt["search_flops"] / (search * 1e-3) / 1e12,
+           "search_tensor_frac_of_sustained": cnt["search_flops"] / (search * 1e-3) / 1e12
+           / pk["bf16_tflops_sustained"],
+           "all_status_ok": bool((o["status"] == 0).all())}
+    if with_parity and oracle_reqs:
+        cores = os.cpu_count() or 1
+        secs, refs = oracle_sample(wl, oracle_reqs, cores, keep=True)
+        leg["parity"] = parity_block(wl, o, refs)
+        leg["parity"]["requests"] = f"{len(oracle_reqs)} of {wl.batch}"
+        leg["oracle_s"] = secs
+    del tb, inp, out
+    torch.cuda.empty_cache()
+    return leg
+
+
 class TreeWeights:
     """The device weights of the main leg, shared with the chain leg."""
     w = None
@@ -382,7 +494,12 @@ def main():
         dtbuild.build()
     if world > 1:
         dist.barrier()
-    wl = W.make_workload(CFG)
+    # every configuration's seeded inputs, generated concurrently on the host
+    other_cfgs = [] if (args.no_configs or rank != 0) else [0, 1, 2, 4]
+    from concurrent.futures import ThreadPoolExecutor
+    gen = ThreadPoolExecutor(max_workers=1 + len(other_cfgs))
+    wl_f = {c: gen.submit(W.make_workload, c) for c in [CFG] + other_cfgs}
+    wl = wl_f[CFG].result()
     dev = torch.device("cuda", local)
 
     t0 = time.perf_counter()
@@ -461,6 +578,15 @@ def main():
     if not args.no_chain:
         chain = {"sampled": chain_leg(wl, W, dt, torch, dev, flush, st, K, Wm, inp, False),
                  "greedy": chain_leg(wl, W, dt, torch, dev, flush, st, K, Wm, inp, True)}
+    # the other configurations (rank 0): timing, rooflines, oracle parity
+    configs = {}
+    for c in other_cfgs:
+        wlc = wl_f[c].result()
+        reqs = list(range(wlc.batch)) if wlc.batch <= 32 else list(range(0, wlc.batch, 8))
+        configs[f"config{c}"] = config_leg(c, wlc, dt, torch, np, dev, flush, st, K, Wm,
+                                           world == 1 and not args.no_cpu_baseline, reqs)
+        wl_f[c] = None
+    gen.shutdown()
     if rank == 0:
         o = {k: v.cpu().numpy() for k, v in out.items() if v is not None}
         cnt = algorithmic_counts(wl, o["tokens"], o["depths"])
@@ -475,13 +601,17 @@ def main():
         # expansion) / search time, against the measured dense bf16 burst peak.
         ach = cnt["search_flops"] / (phases["search"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_tflops"], "traffic": None, "kernel": "dt::chain_kernel",
+                "frac": ach / pk["bf16_tflops"],
+                "traffic": ncu_traffic("chain_kernel_qwen3-8b-b32.json",
+                                       "conditional_draft_tree_gb300/csrc/dt_chain.cu"),
+                "kernel": "dt::chain_kernel",
                 "peak_kind": f"bf16 dense burst, {pk['source']}"}
         ach_t = cnt["topm_bytes"] / (phases["topm"] * 1e-3) / 1e9
         roof_topm = {"bound": "hbm", "achieved": ach_t, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": ach_t / pk["hbm_gbs"], "kernel": "dt::topm_kernel",
                      "note": "projection GEMM runs concurrently on a side stream"}
         round_bytes = cnt["topm_bytes"] + cnt["proj_bytes"] + cnt["search_bytes"]
+        status_ok = bool((o["status"] == 0).all())
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": Wm, "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -500,6 +630,8 @@ def main():
                        "chain_decoding": chain,
                        "verify_tree_attention": verify,
                        "cond_adaptive": adaptive,
+                       "all_status_ok": status_ok,
+                       "other_configs": configs or None,
                        "round_algorithmic_bytes": round_bytes,
                        "round_hbm_frac": round_bytes / (total_ms / K * 1e-3) / 1e9 / pk["hbm_gbs"],
                        "peaks": pk["source"], "wall_s": wall},
@@ -512,10 +644,16 @@ def main():
         if world == 1 and not args.no_cpu_baseline:
             cores = os.cpu_count() or 1
             reqs = list(range(wl.batch))
-            secs = oracle_sample(wl, reqs, cores)
+            secs, refs = oracle_sample(wl, reqs, cores, keep=True)
+            secs1 = oracle_sample(wl, [0], 1)
             line["cpu_baseline"] = {"value": len(reqs) / secs, "unit": UNIT, "cores": cores,
                                     "kind": "oracle",
-                                    "sample": f"all {len(reqs)} requests of one round, {cores} threads"}
+                                    "sample": f"all {len(reqs)} requests of one round, {cores} threads",
+                                    "single_thread": {"value": 1.0 / secs1, "unit": UNIT,
+                                                      "sample": "request 0, 1 thread"},
+                                    "cpu_model": cpu_model()}
+            # the timed trees of the last round against the oracle's (every request)
+            line["config"]["parity"] = parity_block(wl, o, refs)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

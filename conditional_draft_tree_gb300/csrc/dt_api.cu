@@ -101,11 +101,17 @@ int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, P
     // the opt-in limit covers static + dynamic shared memory of a block
     const int smem_max = smem_optin - static_cast<int>(fa.sharedSizeBytes);
     const int wave0 = d.batch < 256 ? (d.batch < p->num_sms ? d.batch : p->num_sms) : 256;
-    // e_cap (expansion slots) and shared memory for the GEMM choice in *p; false
-    // when even the smallest e_cap does not fit
+    // e_cap (expansion slots), B slice buffers and shared memory for the GEMM
+    // choice in *p: the full speculation budget with 4, 3 or 2 buffers, else
+    // a halved budget with 2; false when even the smallest e_cap does not fit
     auto fit_smem = [&](Plan *q, int wave) {
       int e_cap = d.N + 1 + (q->spec > 1 ? d.N + 1 : 0);
+      q->nbufs = 4;
       int smem = chain_smem_bytes(*q, e_cap, wave);
+      while (smem > smem_max && q->umma && q->nbufs > 2) {
+        --q->nbufs;
+        smem = chain_smem_bytes(*q, e_cap, wave);
+      }
       while (smem > smem_max && e_cap > d.N + 1) {
         e_cap = d.N + 1 + (e_cap - d.N - 1) / 2;
         smem = chain_smem_bytes(*q, e_cap, wave);

@@ -92,6 +92,7 @@ struct ChainParams {
   // tensor-core GEMM path (bf16 weights): A tiles of 128 rows x kc K stay in
   // shared memory; the input columns arrive as three bf16 terms per state
   int umma, n_mt, ks, kc, cols_cap;
+  int nbufs;           // B slice buffers (2..kMaxBufs)
   float *partial;      // [ks][cols_cap][R] per-K-chunk partial products, by slot
   uint16_t *gin16;     // B operand in tile layout (bcol_index)
   Ctrl *ctrl;
@@ -350,7 +351,7 @@ __device__ void load_a_tile(const ChainParams &p, unsigned char *sA) {
 // block whose first 32 * n bytes hold columns [0, n).
 constexpr int kTermBytes = 256 * 16 * 2;
 constexpr int kSliceBytes = 3 * kTermBytes;
-constexpr int kBufs = 4;                       // B slices in flight
+constexpr int kMaxBufs = 4;                    // B slice buffers at most (p.nbufs: 2..4)
 
 __device__ __forceinline__ size_t bcol_index(const ChainParams &p, int slot, int k) {
   const int kz = k / p.kc, kk = k - kz * p.kc;
@@ -362,7 +363,7 @@ __device__ __forceinline__ size_t bcol_index(const ChainParams &p, int slot, int
 
 struct UmmaState {
   uint32_t tmem;      // TMEM base column address
-  uint32_t next;      // global index of the next B slice (buffer = next % kBufs)
+  uint32_t next;      // global index of the next B slice (buffer = next % p.nbufs)
 };
 
 // Partial products of this block's (M tile, K chunk) for every active column,
@@ -372,7 +373,7 @@ struct UmmaState {
 // columns) = A B^T, A = 128 weight rows (K-major, resident), B = the node
 // columns as hi / mid / lo bf16 terms; one MMA per (K step, term) covers a
 // whole pass of 256 columns, since an MMA costs about the same for any N up to
-// 256. Thread 0 issues the bulk copies into kBufs slice buffers, thread 32 the
+// 256. Thread 0 issues the bulk copies into p.nbufs slice buffers, thread 32 the
 // MMAs and commits; all warps read the accumulators back. Every block lists
 // the active columns (slots, count in total_out) for the request phase.
 __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, int *slots,
@@ -403,7 +404,8 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, int *
   unsigned char *sA = smem + p.sm_A;
   unsigned char *sB = smem + p.sm_B;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
-  uint64_t *empty = full + kBufs;
+  const uint32_t nbufs = static_cast<uint32_t>(p.nbufs);
+  uint64_t *empty = full + kMaxBufs;
   const int nkb = p.kc >> 4;
   const bool clock_me = blockIdx.x == 0 && threadIdx.x == 0;
   for (int pass = 0; pass < n_pass; ++pass) {
@@ -422,10 +424,10 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, int *
       fence_async_smem();     // earlier generic use of the buffers -> bulk writes
       long long c_empty = 0, c_copy = 0;
       for (int s = 0; s < nkb; ++s) {
-        const uint32_t g = g0 + s, buf = g % kBufs;
+        const uint32_t g = g0 + s, buf = g % nbufs;
         // the buffer's previous slice must be consumed by its MMAs
         const long long c0 = clock64();
-        if (g >= kBufs && !mbar_wait(&empty[buf], ((g / kBufs) - 1) & 1u, p.limit_ns)) {
+        if (g >= nbufs && !mbar_wait(&empty[buf], ((g / nbufs) - 1) & 1u, p.limit_ns)) {
           s_fail = 1;
           break;
         }
@@ -448,9 +450,9 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, int *
       long long c_full = 0, c_mma = 0;
       int s = 0;
       for (; s < nkb; ++s) {
-        const uint32_t g = g0 + s, buf = g % kBufs;
+        const uint32_t g = g0 + s, buf = g % nbufs;
         const long long cf = clock64();
-        if (!mbar_wait(&full[buf], (g / kBufs) & 1u, p.limit_ns)) {
+        if (!mbar_wait(&full[buf], (g / nbufs) & 1u, p.limit_ns)) {
           s_fail = 1;
           break;
         }
@@ -468,7 +470,7 @@ __device__ bool gemm_phase_umma(const ChainParams &p, unsigned char *smem, int *
       const uint64_t tm = global_ns();
       if (s > 0) {   // commits complete in order: the last one covers every MMA
         const uint32_t last = g0 + s - 1;
-        if (!mbar_wait(&empty[last % kBufs], (last / kBufs) & 1u, p.limit_ns)) s_fail = 1;
+        if (!mbar_wait(&empty[last % nbufs], (last / nbufs) & 1u, p.limit_ns)) s_fail = 1;
       }
       if (blockIdx.x == 0) {
         p.ctrl->t_ns[12] += global_ns() - tm;
@@ -1645,7 +1647,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(ChainParams p) {
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + p.sm_mbar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + p.sm_tmem);
     if (threadIdx.x == 0)
-      for (int i = 0; i < 2 * kBufs; ++i) mbar_init(&mbar[i], 1);   // full, empty
+      for (int i = 0; i < 2 * kMaxBufs; ++i) mbar_init(&mbar[i], 1);   // full, empty
     load_a_tile(p, smem + p.sm_A);
     fence_async_smem();   // generic stores of the A tile -> tensor-core reads
     if ((threadIdx.x >> 5) == 0) tmem_alloc(tslot, kTmemCols);
@@ -1774,8 +1776,8 @@ static int chain_smem_layout(const Plan &pl, int e_cap, int wave, ChainParams *c
   cp->sm_A = cp->sm_B = cp->sm_mbar = cp->sm_tmem = 0;
   if (pl.umma) {
     cp->sm_A = off = al(off, 128);    off += 128 * pl.kc * 2;
-    cp->sm_B = off = al(off, 128);    off += kBufs * kSliceBytes;
-    cp->sm_mbar = off = al(off, 16);  off += 16 * kBufs;
+    cp->sm_B = off = al(off, 128);    off += pl.nbufs * kSliceBytes;
+    cp->sm_mbar = off = al(off, 16);  off += 16 * kMaxBufs;
     cp->sm_tmem = off;                off += 16;
   }
   cp->sm_slots = off = al(off, 16);   off += (wave * pl.spec + 2 * wave) * 4;   // slots, per request
@@ -1842,7 +1844,7 @@ cudaError_t launch_chain(const Plan &pl, const ChainArgs &a, void *ws, cudaStrea
     const int gsz = pl.chain_grid / a.nb;
     cp.grp = gsz < 1 ? 1 : (gsz > pl.spec ? pl.spec : gsz);
   }
-  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc;
+  cp.umma = pl.umma; cp.n_mt = pl.n_mt; cp.ks = pl.ks; cp.kc = pl.kc; cp.nbufs = pl.nbufs;
   cp.cols_cap = pl.wave * pl.spec;
   cp.partial = pl.umma ? reinterpret_cast<float *>(w + pl.off_partial) : nullptr;
   cp.gin16 = pl.umma ? reinterpret_cast<uint16_t *>(w + pl.off_gin16) : nullptr;

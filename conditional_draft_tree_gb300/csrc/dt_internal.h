@@ -21,6 +21,7 @@ struct Plan {
   int proj_ksplit;     // K split of the projection GEMM
   int umma;            // search GEMM on tcgen05 (bf16 weights)
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
+  int nbufs;           // its B slice buffers in flight (2..4)
   int test_timeout;    // DT_OPT_TEST_BARRIER_TIMEOUT
   int marginal;        // DT_OPT_MARGINAL: top-M, then the marginal tree kernel
   int num_sms;

@@ -63,9 +63,15 @@ def check_structure(wl, b, g):
 def compare_tree(wl, b, g, ref):
     """'exact' or 'near-tie'; raises AssertionError otherwise. g: dict of batch
     arrays from the GPU; ref: oracle.build_tree(wl, b) output."""
+    return compare_tree_err(wl, b, g, ref)[0]
+
+
+def compare_tree_err(wl, b, g, ref):
+    """compare_tree, plus the largest score difference over the nodes the two
+    trees share (0 for a request that reports an error status)."""
     assert int(g["status"][b]) == ref["status"], (g["status"][b], ref["status"])
     if ref["status"] != 0:
-        return "exact"
+        return "exact", 0.0
     np.testing.assert_array_equal(g["topm"][b], ref["topm"])
     check_structure(wl, b, g)
     gt, gp, gd, gs = (g[k][b] for k in ("tokens", "parents", "depths", "scores"))
@@ -75,12 +81,15 @@ def compare_tree(wl, b, g, ref):
         assert np.array_equal(np.isfinite(gs), fin)
         err = np.abs(gs[fin].astype(np.float64) - ref["scores"][fin])
         assert err.max(initial=0) <= TOL_SCORE, f"score error {err.max()}"
-        return "exact"
+        return "exact", float(err.max(initial=0))
     gpaths, opaths = paths_of(gt, gp), paths_of(ref["tokens"], ref["parents"])
     gmap = {p: float(gs[i]) for i, p in enumerate(gpaths)}
     omap = {p: float(ref["scores"][i]) for i, p in enumerate(opaths)}
+    common_err = 0.0
     for p in gmap.keys() & omap.keys():
         assert abs(gmap[p] - omap[p]) <= TOL_SCORE, (p, gmap[p], omap[p])
+        if np.isfinite(gmap[p]) and np.isfinite(omap[p]):
+            common_err = max(common_err, abs(gmap[p] - omap[p]))
     boundary = min(min(gmap.values()), min(omap.values()))
     only = (gmap.keys() - omap.keys()) | (omap.keys() - gmap.keys())
     roots = {p for p in only if p[:-1] not in only}
@@ -92,4 +101,16 @@ def compare_tree(wl, b, g, ref):
         sc_u, _ = oracle.score_path(wl, list(u), b)
         at_budget = abs(sc_u - boundary) < TOL_TIE
         assert at_topk or at_budget, f"divergence at {u} is not a near tie"
-    return "near-tie"
+    return "near-tie", common_err
+
+
+def parity_summary(wl, g, refs):
+    """Counts over the requests in `refs` ({b: oracle tree}): compared, exact,
+    near-tie, the largest score error; raises on any tree outside the bar."""
+    out = dict(compared=0, exact=0, near_tie=0, max_score_err=0.0)
+    for b, ref in refs.items():
+        kind, err = compare_tree_err(wl, b, g, ref)
+        out["compared"] += 1
+        out["exact" if kind == "exact" else "near_tie"] += 1
+        out["max_score_err"] = max(out["max_score_err"], err)
+    return out

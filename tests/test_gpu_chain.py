@@ -16,6 +16,8 @@ two orders of magnitude of room.
 """
 from __future__ import annotations
 
+import os
+
 import dataclasses
 
 import numpy as np
@@ -24,6 +26,7 @@ import torch
 
 import dt_workloads as W
 import oracle
+from _report import record
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +58,7 @@ def run_gpu(wl, uniforms=None, decoder=None, temperature=None):
 def compare(wl, g, reqs, uniforms=None, max_near=None):
     """Replays the oracle along the GPU tokens; returns the number of near ties."""
     refs = oracle.chains(wl, reqs, uniforms, forced=np.where(g["tokens"] >= 0, g["tokens"], 0),
-                         threads=8)
+                         threads=os.cpu_count() or 8)
     near = 0
     for b, ref in zip(reqs, refs):
         assert ref["status"] == 0
@@ -71,7 +74,9 @@ def compare(wl, g, reqs, uniforms=None, max_near=None):
             else:
                 assert abs(float(g["logprobs"][b, i]) - float(ref["lp"][i])) <= TOL_LP, \
                     (b, i, g["logprobs"][b, i], ref["lp"][i])
-    print(f"{wl.name}: {len(reqs)} chains x {wl.D} positions, {near} near ties")
+    record(f"chain decoding: {wl.name} (positions)",
+           dict(compared=len(reqs) * wl.D, exact=len(reqs) * wl.D - near, near_tie=near,
+                max_score_err=0.0))
     if max_near is not None:
         assert near <= max_near
     return near
@@ -102,8 +107,8 @@ def test_custom_shapes(name):
     wl = W.custom_workload(name=name, **SHAPES[name])
     u = W.chain_uniforms(wl.batch, wl.D, seed=SHAPES[name]["seed"])
     g = run_gpu(wl, u)
-    reqs = list(range(wl.batch)) if wl.batch <= 8 else [0, 1, 79, 80, 81, 99]
-    compare(wl, g, reqs, u, max_near=1)
+    reqs = list(range(wl.batch))
+    compare(wl, g, reqs, u, max_near=max(1, len(reqs) // 30))
 
 
 def test_two_waves_launch_count():
@@ -147,7 +152,7 @@ def test_deterministic():
 
 def test_config3_qwen3_8b_b32():
     """Batch 32 at the Qwen3-8B shape (V = 151936, d_s = 1024, r = 256, D = 15),
-    sampled at T = 1 and greedy: every chain valid, three of each against the oracle."""
+    sampled at T = 1 and greedy: every chain valid and against the oracle."""
     wl = W.make_workload(3)
     u = W.chain_uniforms(wl.batch, wl.D, seed=3)
     dec = dt.ChainDecoder.from_numpy(wl)
@@ -157,4 +162,6 @@ def test_config3_qwen3_8b_b32():
         assert ((g["tokens"] >= 0) & (g["tokens"] < wl.V)).all()
         assert (g["logprobs"] <= 1e-6).all()
         w = wl if T is None else dataclasses.replace(wl, temperature=T)
-        compare(w, g, [0, 13, 31], u, max_near=1)
+        # near ties are within the bar (counted and reported); a cap of 1% of
+        # the positions only guards against a systematic slip
+        compare(w, g, list(range(w.batch)), u, max_near=max(2, w.batch * w.D // 100))

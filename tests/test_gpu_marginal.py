@@ -12,6 +12,8 @@ those pointers are passed as NULL.
 """
 from __future__ import annotations
 
+import os
+
 import dataclasses
 import functools
 
@@ -70,7 +72,7 @@ def run_conditional(wl, spec=0):
 
 
 def check_against_oracle(wl, g, reqs, max_near_ties=None):
-    refs = oracle.build_trees(wl, reqs, threads=8)
+    refs = oracle.build_trees(wl, reqs, threads=os.cpu_count() or 8)
     kinds = [compare_tree(wl, b, g, ref) for b, ref in zip(reqs, refs)]
     if max_near_ties is not None:
         assert kinds.count("near-tie") <= max_near_ties
@@ -205,4 +207,4 @@ def test_config3_qwen3_8b_b32():
     for b in range(wl.batch):
         assert g["status"][b] == 0
         check_structure(wl, b, g)
-    check_against_oracle(wl, g, [0, 11, 31], max_near_ties=1)
+    check_against_oracle(wl, g, list(range(wl.batch)), max_near_ties=2)

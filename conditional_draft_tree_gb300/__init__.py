@@ -244,9 +244,20 @@ def select_topm_noalloc(base_logits, M: int, topm, status, stream=None) -> int:
     topm [batch][D][M] int32 and status [batch] int32 outputs. Allocates no
     device memory (the library's static scratch is used; see include/dt.h).
     Returns the C status code."""
+    if base_logits.dim() != 3 or base_logits.dtype != torch.float32 or \
+            not base_logits.is_contiguous() or not base_logits.is_cuda:
+        raise ValueError("base_logits must be a contiguous [batch][D][V] float32 CUDA tensor")
     batch, D, V = base_logits.shape
-    return lib().dt_select_topm_noalloc(_ptr(base_logits), batch, D, V, int(M), _ptr(topm),
-                                        _ptr(status), _stream(stream))
+    dev = base_logits.device
+    if topm.shape != (batch, D, int(M)) or topm.dtype != torch.int32 or \
+            not topm.is_contiguous() or topm.device != dev:
+        raise ValueError("topm must be a contiguous [batch][D][M] int32 tensor on base_logits' device")
+    if status.shape != (batch,) or status.dtype != torch.int32 or \
+            not status.is_contiguous() or status.device != dev:
+        raise ValueError("status must be a contiguous [batch] int32 tensor on base_logits' device")
+    with torch.cuda.device(dev):
+        return lib().dt_select_topm_noalloc(_ptr(base_logits), batch, D, V, int(M), _ptr(topm),
+                                            _ptr(status), _stream(stream))
 
 
 class TreeBuilder:

@@ -299,20 +299,48 @@ cudaStream_t side_stream() {
   return streams[dev];
 }
 
-// fork/join events of one call (released when the call returns; the CUDA driver
-// frees them once the recorded work has completed)
+// Fork/join events of the side stream, created once per (device, caller
+// stream) and kept for the process. Two calls on the same stream may record
+// them in turn: a wait then covers a later record of the same stream, which
+// orders no less work than the call needs.
 struct Events {
   cudaEvent_t fork = nullptr, join = nullptr;
-  bool ok = false;
-  Events() {
-    ok = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess;
-  }
-  ~Events() {
-    if (fork) cudaEventDestroy(fork);
-    if (join) cudaEventDestroy(join);
-  }
 };
+
+bool stream_events(cudaStream_t st, Events *ev) {
+  struct Entry {
+    int dev;
+    cudaStream_t st;
+    Events ev;
+  };
+  static std::mutex mu;
+  static Entry table[64];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].dev == dev && table[i].st == st) {
+      *ev = table[i].ev;
+      return true;
+    }
+  Events e;
+  if (cudaEventCreateWithFlags(&e.fork, cudaEventDisableTiming) != cudaSuccess) return false;
+  if (cudaEventCreateWithFlags(&e.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaEventDestroy(e.fork);
+    return false;
+  }
+  if (used < 64) {
+    table[used++] = Entry{dev, st, e};
+  } else {
+    // a full table drops its oldest entry; its events are not destroyed, since
+    // work already queued may still wait on them
+    for (int i = 1; i < 64; ++i) table[i - 1] = table[i];
+    table[63] = Entry{dev, st, e};
+  }
+  *ev = e;
+  return true;
+}
 
 int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const float *base_logits,
               const float *H, const float *state0, const int32_t *anchor_tok,
@@ -342,7 +370,7 @@ int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const f
   cudaStream_t side = side_stream();
   if (!side) return DT_ERR_CUDA;
   Events ev;
-  if (!ev.ok) return DT_ERR_CUDA;
+  if (!stream_events(st, &ev)) return DT_ERR_CUDA;
   if (cudaEventRecord(ev.fork, st) != cudaSuccess || cudaStreamWaitEvent(side, ev.fork, 0) != cudaSuccess)
     return DT_ERR_CUDA;
   float *U = reinterpret_cast<float *>(wsb + pl.off_U);

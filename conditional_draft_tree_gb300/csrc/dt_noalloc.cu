@@ -17,7 +17,9 @@
 // on different host threads on the same device -- race on the array and must
 // be serialised by the caller. The first call on a device resolves the array's
 // device address with cudaGetSymbolAddress (with that device current); make
-// that first call before any stream capture.
+// that first call before any stream capture. The address is kept per device
+// number, which is right for the primary context the runtime uses; it does not
+// follow a cudaDeviceReset or another driver-API context on the same device.
 #include <cstdint>
 #include <mutex>
 

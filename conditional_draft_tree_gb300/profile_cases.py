@@ -2,8 +2,11 @@
 
     python -m conditional_draft_tree_gb300.profile_cases topm  [--reps R] [--cfg C]
         top-M of a workload's base logits (Qwen3-8B batch 32 by default:
-        480 rows x 151936 fp32, 292 MB) through dt_select_topm_noalloc, whose
-        top-M kernel and launch shape are those of dt_build_trees. Only the
+        480 rows x 151936 fp32, 292 MB) through dt_select_topm_noalloc. Its
+        kernel is dt_build_trees' top-M kernel, and the launch shape is the same
+        while the row segments' partial lists fit in the static scratch (true
+        for this workload; a larger one, such as the batch-128 M = 256 stress
+        configuration, falls back to one block per row segment). Only the
         logits and the outputs live on the device.
     python -m conditional_draft_tree_gb300.profile_cases round [--reps R] [--cfg C] [--flags F]
         R whole dt_build_trees rounds of the workload (weights, prepared table

@@ -211,8 +211,11 @@ int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *pr
  * (plus 8*M bytes per extra row segment, which the call drops first when short
  * of room); shapes that do not fit return DT_ERR_INVALID_ARG. The first call on
  * a device resolves the array's address (cudaGetSymbolAddress) with that device
- * current; make it before any stream capture. All calls share the array, so
- * calls that overlap on the GPU race; serialise them. Asynchronous on `stream`. */
+ * current; make it before any stream capture. The address is kept per device
+ * number for the device's primary context (the one the CUDA runtime uses): it
+ * does not follow a cudaDeviceReset or a caller that switches to another
+ * driver-API context on the same device. All calls share the array, so calls
+ * that overlap on the GPU race; serialise them. Asynchronous on `stream`. */
 #define DT_NOALLOC_SCRATCH_BYTES (8u << 20)
 int dt_select_topm_noalloc(const float *base_logits, int batch, int D, int V, int M,
                            int32_t *topm, int32_t *status, void *stream);

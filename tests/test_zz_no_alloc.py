@@ -20,6 +20,7 @@ import pytest
 import torch
 
 import dt_workloads as W
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +41,13 @@ def reference_topm(dt, wl):
     out = tb.run(**tb.inputs_to_device(wl))
     torch.cuda.synchronize()
     return out["topm"].cpu().numpy(), out["status"].cpu().numpy()
+
+
+def oracle_topm(wl):
+    """The oracle's top-M of every row (the pinned CPU selection)."""
+    oracle.build()
+    return np.stack([[oracle.topm(wl.base_logits[b, j], wl.M) for j in range(wl.D)]
+                     for b in range(wl.batch)])
 
 
 def noalloc_topm(dt, wl, calls=2):
@@ -63,9 +71,39 @@ def noalloc_topm(dt, wl, calls=2):
 def test_noalloc_matches_build_trees_twice(dt, shape):
     wl = W.custom_workload(**shape)
     ref_topm, ref_status = reference_topm(dt, wl)
+    want = oracle_topm(wl)
+    np.testing.assert_array_equal(ref_topm, want)
     for topm, status in noalloc_topm(dt, wl, calls=2):
-        np.testing.assert_array_equal(topm, ref_topm)
+        np.testing.assert_array_equal(topm, want)
         np.testing.assert_array_equal(status, ref_status)
+
+
+def test_noalloc_segment_fallback_matches_oracle(dt):
+    """A shape whose contiguous-range launch does not fit the static scratch
+    (the row pieces' lists), so the call cuts the rows into fewer segments."""
+    wl = W.custom_workload(V=4096, d=16, d_s=8, r=8, D=16, M=256, k=4, N=8, batch=128,
+                           wdtype="f32", logits="zipf", zipf=(0.8, 1.6), seed=34)
+    want = oracle_topm(wl)
+    for topm, status in noalloc_topm(dt, wl, calls=2):
+        assert (status == dt.OK).all()
+        np.testing.assert_array_equal(topm, want)
+
+
+def test_noalloc_allocates_no_device_memory(dt):
+    """After a first call, further calls leave the device's free memory as it
+    is (the inputs and outputs are allocated before the measurement)."""
+    wl = W.custom_workload(V=151936, d=16, d_s=8, r=8, D=15, M=64, k=8, N=16, batch=4,
+                           wdtype="bf16", logits="zipf", zipf=(0.8, 1.6), seed=35)
+    logits = torch.from_numpy(np.ascontiguousarray(wl.base_logits)).cuda()
+    topm = torch.empty((wl.batch, wl.D, wl.M), dtype=torch.int32, device="cuda")
+    status = torch.empty((wl.batch,), dtype=torch.int32, device="cuda")
+    assert dt.select_topm_noalloc(logits, wl.M, topm, status) == dt.OK
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(5):
+        assert dt.select_topm_noalloc(logits, wl.M, topm, status) == dt.OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
 
 
 def test_noalloc_flags_nonfinite_and_recovers(dt):
@@ -75,12 +113,12 @@ def test_noalloc_flags_nonfinite_and_recovers(dt):
     bad[1, 2, 7] = np.nan
     (topm, status), = noalloc_topm(dt, dataclasses.replace(wl, base_logits=bad), calls=1)
     assert list(status) == [dt.OK, dt.ERR_NONFINITE, dt.OK]
-    ref_topm, _ = reference_topm(dt, wl)
-    np.testing.assert_array_equal(topm[0], ref_topm[0])
+    want = oracle_topm(wl)
+    np.testing.assert_array_equal(topm[0], want[0])
     # the next call starts from clean tickets and flags
     (topm, status), = noalloc_topm(dt, wl, calls=1)
     assert list(status) == [dt.OK] * 3
-    np.testing.assert_array_equal(topm, ref_topm)
+    np.testing.assert_array_equal(topm, want)
 
 
 def test_noalloc_rejects_shapes_beyond_the_static_scratch(dt):

@@ -1295,32 +1295,100 @@ __device__ __forceinline__ int head_exp(const ChainParams &p, const Tables &t, i
   return h < p.k ? t.child_exp[er * p.k + h] : -2;
 }
 
+// Per-run state of the register replay, slot s of lane l holding run
+// r = 32 s + l: the head (w1, w2, score rh), the next head (its score nrh and
+// w2 nw2) and, when the head is expanded, its first child (score fh, and fce
+// the first child's expansion, -2 when there is none). With the next values at
+// hand a pop needs one round of shared-memory loads, all issued together and
+// off the path to the next pop's argmax.
+template <int RS>
+struct RunRegs {
+  uint32_t w1[RS], w2[RS], nw2[RS];
+  float rh[RS], nrh[RS], fh[RS];
+  int fce[RS];
+};
+
+template <int RS>
+__device__ __forceinline__ float pick_f(const float (&v)[RS], int s) {
+  float x = v[0];
+#pragma unroll
+  for (int i = 1; i < RS; ++i) x = (s == i) ? v[i] : x;
+  return x;
+}
+template <int RS>
+__device__ __forceinline__ int pick_i(const int (&v)[RS], int s) {
+  int x = v[0];
+#pragma unroll
+  for (int i = 1; i < RS; ++i) x = (s == i) ? v[i] : x;
+  return x;
+}
+
+// the expansion field of a w2 word: run_w2 stores ce + 1 >= -1 in the upper 24
+// bits, so an arithmetic shift gives back -2 (past the last child) as well
+__device__ __forceinline__ int w2_exp(uint32_t w2) { return (static_cast<int>(w2) >> 8) - 1; }
+
 template <int RS>
 __device__ void replay_and_select_reg(const ChainParams &p, const Tables &t, TailState &ts, int b,
                                       int lane) {
+  const float nan = __int_as_float(0x7fc00000);
   int count = ts.count, n_runs = ts.n_runs;
   const int count0 = count;
   const bool clock_me = blockIdx.x == 0 && lane == 0;
   long long c_start = clock64();
   int it_pop = 0;
-  uint32_t w1[RS], w2[RS], plog[RS];
-  float rh[RS];
+  auto score_at = [&](int er, int h) { return h < p.k ? t.child_score[er * p.k + h] : nan; };
+  auto exp_at = [&](int er, int h) { return h < p.k ? static_cast<int>(t.child_exp[er * p.k + h]) : -2; };
+  RunRegs<RS> R;
+  uint32_t plog[RS];
 #pragma unroll
   for (int s = 0; s < RS; ++s) {
     const int r = s * 32 + lane;
     plog[s] = 0u;
+    R.w1[s] = 0u; R.w2[s] = 0u; R.nw2[s] = 0u;
+    R.rh[s] = nan; R.nrh[s] = nan; R.fh[s] = nan; R.fce[s] = -2;
     if (r < n_runs) {
       const int h = t.run_head[r], er = t.run_e[r];
-      w1[s] = run_w1(h, er, t.run_pos[r]);
-      w2[s] = run_w2(t.exp_depth[er] + 1, head_exp(p, t, er, h));
-      rh[s] = t.run_hs[r];
-    } else {
-      w1[s] = 0u;
-      w2[s] = 0u;
-      rh[s] = __int_as_float(0x7fc00000);
+      const int dep = t.exp_depth[er] + 1, ce = exp_at(er, h);
+      R.w1[s] = run_w1(h, er, t.run_pos[r]);
+      R.w2[s] = run_w2(dep, ce);
+      R.rh[s] = t.run_hs[r];
+      R.nrh[s] = score_at(er, h + 1);
+      R.nw2[s] = run_w2(dep, exp_at(er, h + 1));
+      if (ce >= 0) { R.fh[s] = score_at(ce, 0); R.fce[s] = exp_at(ce, 0); }
     }
   }
-  LaneBest lb = lane_best_reg<RS>(rh, n_runs, lane);
+  LaneBest lb = lane_best_reg<RS>(R.rh, n_runs, lane);
+  // one pop of run r (owner lane own, slot sl): its head advances to the next
+  // entry; when `grow`, the popped node's children (expansion ce) become run
+  // n_runs. Every lane evaluates the same loads (broadcast) and selects.
+  auto advance = [&](int sl, int own, uint32_t a, int dep, uint32_t nw, float nr, bool grow,
+                     int ce, float f, int fc, int pos) {
+    const int h = a & 63, er = (a >> 6) & 4095;
+    const int ce1 = w2_exp(nw);   // the new head's expansion
+    const float s2 = score_at(er, h + 2);
+    const int e2 = exp_at(er, h + 2);
+    const float f1 = ce1 >= 0 ? score_at(ce1, 0) : nan;
+    const int g1 = ce1 >= 0 ? exp_at(ce1, 0) : -2;
+    float c1 = nan, fr = nan;
+    int x1 = -2, xr = -2;
+    if (grow) {
+      c1 = score_at(ce, 1);
+      x1 = exp_at(ce, 1);
+      if (fc >= 0) { fr = score_at(fc, 0); xr = exp_at(fc, 0); }
+    }
+    const int ns = n_runs >> 5, nl = n_runs & 31;
+#pragma unroll
+    for (int s = 0; s < RS; ++s) {
+      if (lane == own && s == sl) {
+        R.w1[s] = a + 1u; R.w2[s] = nw; R.rh[s] = nr;
+        R.nrh[s] = s2; R.nw2[s] = run_w2(dep, e2); R.fh[s] = f1; R.fce[s] = g1;
+      }
+      if (grow && lane == nl && s == ns) {
+        R.w1[s] = run_w1(0, ce, pos); R.w2[s] = run_w2(dep + 1, fc); R.rh[s] = f;
+        R.nrh[s] = c1; R.nw2[s] = run_w2(dep + 1, x1); R.fh[s] = fr; R.fce[s] = xr;
+      }
+    }
+  };
   bool done = false;
   while (true) {
     ++it_pop;
@@ -1328,10 +1396,13 @@ __device__ void replay_and_select_reg(const ChainParams &p, const Tables &t, Tai
     const int r = warp_best(lb);
     if (r < 0) { done = true; break; }
     const int sl = r >> 5, own = r & 31;
-    const uint32_t a = __shfl_sync(kFull, pick_slot<RS>(w1, sl), own);
-    const uint32_t c = __shfl_sync(kFull, pick_slot<RS>(w2, sl), own);
-    const int h = a & 63, er = (a >> 6) & 4095;
-    const int dep = c & 255, ce = static_cast<int>(c >> 8) - 1, pos = count + 1;
+    const uint32_t a = __shfl_sync(kFull, pick_slot<RS>(R.w1, sl), own);
+    const uint32_t c = __shfl_sync(kFull, pick_slot<RS>(R.w2, sl), own);
+    const uint32_t nw = __shfl_sync(kFull, pick_slot<RS>(R.nw2, sl), own);
+    const float nr = __shfl_sync(kFull, pick_f<RS>(R.nrh, sl), own);
+    const float f = __shfl_sync(kFull, pick_f<RS>(R.fh, sl), own);
+    const int fc = __shfl_sync(kFull, pick_i<RS>(R.fce, sl), own);
+    const int dep = c & 255, ce = w2_exp(c), pos = count + 1;
     const bool need = dep < p.D && pos < p.N;
     if (need && ce < 0) break;  // stall: this node's children are not known yet
     const int i = pos - count0 - 1;   // pop index within this step
@@ -1340,26 +1411,10 @@ __device__ void replay_and_select_reg(const ChainParams &p, const Tables &t, Tai
       for (int s = 0; s < RS; ++s)
         if (s == (i >> 5)) plog[s] = a;
     }
-    if (lane == own) {
-      const float nh = head_score(p, t, er, h + 1);
-      const int nce = head_exp(p, t, er, h + 1);
-#pragma unroll
-      for (int s = 0; s < RS; ++s)
-        if (s == sl) { w1[s] = a + 1u; w2[s] = run_w2(dep, nce); rh[s] = nh; }
-      lb = lane_best_reg<RS>(rh, n_runs, lane);
-    }
-    if (need && lane == (n_runs & 31)) {
-      const float hs0 = head_score(p, t, ce, 0);
-      const int ce0 = head_exp(p, t, ce, 0);
-      const int s2 = n_runs >> 5;
-#pragma unroll
-      for (int s = 0; s < RS; ++s)
-        if (s == s2) { w1[s] = run_w1(0, ce, pos); w2[s] = run_w2(dep + 1, ce0); rh[s] = hs0; }
-      const uint32_t k0 = hs_key(hs0);
-      if (k0 > lb.key) { lb.key = k0; lb.run = n_runs; }
-    }
+    advance(sl, own, a, dep, nw, nr, need, ce, f, fc, pos);
     n_runs += need ? 1 : 0;
     count = pos;
+    lb = lane_best_reg<RS>(R.rh, n_runs, lane);
   }
   // the popped rows (pop i logged by lane i % 32), then the run state back to
   // the shared tables (it persists across steps)
@@ -1377,10 +1432,10 @@ __device__ void replay_and_select_reg(const ChainParams &p, const Tables &t, Tai
     }
     const int r = s * 32 + lane;
     if (r < n_runs) {
-      t.run_head[r] = static_cast<uint8_t>(w1[s] & 63);
-      t.run_e[r] = static_cast<int16_t>((w1[s] >> 6) & 4095);
-      t.run_pos[r] = static_cast<int16_t>(w1[s] >> 18);
-      t.run_hs[r] = rh[s];
+      t.run_head[r] = static_cast<uint8_t>(R.w1[s] & 63);
+      t.run_e[r] = static_cast<int16_t>((R.w1[s] >> 6) & 4095);
+      t.run_pos[r] = static_cast<int16_t>(R.w1[s] >> 18);
+      t.run_hs[r] = R.rh[s];
     }
   }
   __syncwarp();
@@ -1412,21 +1467,16 @@ __device__ void replay_and_select_reg(const ChainParams &p, const Tables &t, Tai
     ++vi;
     if (count + vi >= p.N) break;
     const int sl = r >> 5, own = r & 31;
-    const uint32_t a = __shfl_sync(kFull, pick_slot<RS>(w1, sl), own);
-    const uint32_t c = __shfl_sync(kFull, pick_slot<RS>(w2, sl), own);
-    const int h = a & 63, er = (a >> 6) & 4095;
-    const int dep = c & 255, ce = static_cast<int>(c >> 8) - 1;
+    const uint32_t a = __shfl_sync(kFull, pick_slot<RS>(R.w1, sl), own);
+    const uint32_t c = __shfl_sync(kFull, pick_slot<RS>(R.w2, sl), own);
+    const uint32_t nw = __shfl_sync(kFull, pick_slot<RS>(R.nw2, sl), own);
+    const float nr = __shfl_sync(kFull, pick_f<RS>(R.nrh, sl), own);
+    const int dep = c & 255, ce = w2_exp(c);
     const bool fresh = dep < p.D && ce == -1;
     const bool take = fresh && (nsel == 0 || nspec < spec_left);
     if (take && lane == nsel) my_pick = (a & 0x3ffffu) | (static_cast<uint32_t>(dep) << 18);
-    if (lane == own) {
-      const float nh = head_score(p, t, er, h + 1);
-      const int nce = head_exp(p, t, er, h + 1);
-#pragma unroll
-      for (int s = 0; s < RS; ++s)
-        if (s == sl) { w1[s] = a + 1u; w2[s] = run_w2(dep, nce); rh[s] = nh; }
-      lb = lane_best_reg<RS>(rh, n_runs, lane);
-    }
+    advance(sl, own, a, dep, nw, nr, false, -1, nan, -2, 0);
+    lb = lane_best_reg<RS>(R.rh, n_runs, lane);
     if (take) {
       nspec += (nsel > 0) ? 1 : 0;
       ++nsel;
@@ -1608,7 +1658,10 @@ __device__ bool group_step(const ChainParams &p, const Tables &t, TailState &ts,
       lap(3);
       // 3. canonical pops, then the next expansions
       if (warp == 0) {
-        if (p.N + 1 <= 128) replay_and_select_reg<4>(p, t, ts, b, lane);
+        // runs are at most N + 1: the register replay while they fit 4 x 32
+        if (p.N + 1 <= 64) replay_and_select_reg<2>(p, t, ts, b, lane);
+        else if (p.N + 1 <= 96) replay_and_select_reg<3>(p, t, ts, b, lane);
+        else if (p.N + 1 <= 128) replay_and_select_reg<4>(p, t, ts, b, lane);
         else replay_and_select(p, t, ts, b, lane);
       }
       __syncthreads();

@@ -600,10 +600,13 @@ def main():
         # terms); achieved = algorithmic GEMM flops (2 (3 d_s + r) d_s per
         # expansion) / search time, against the measured dense bf16 burst peak.
         ach = cnt["search_flops"] / (phases["search"] * 1e-3) / 1e12
+        traffic = ncu_traffic("chain_kernel_qwen3-8b-b32.json",
+                              "conditional_draft_tree_gb300/csrc/dt_chain.cu")
         roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_tflops"],
-                "traffic": ncu_traffic("chain_kernel_qwen3-8b-b32.json",
-                                       "conditional_draft_tree_gb300/csrc/dt_chain.cu"),
+                "frac": ach / pk["bf16_tflops"], "traffic": traffic,
+                "algorithmic_bytes": cnt["search_bytes"],
+                "traffic_over_algorithmic": (traffic / cnt["search_bytes"]
+                                             if traffic is not None else None),
                 "kernel": "dt::chain_kernel",
                 "peak_kind": f"bf16 dense burst, {pk['source']}"}
         ach_t = cnt["topm_bytes"] / (phases["topm"] * 1e-3) / 1e9

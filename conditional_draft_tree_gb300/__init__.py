@@ -23,6 +23,7 @@ F32, BF16 = 0, 1
 NUM_PHASE_EVENTS = 4
 OPT_TEST_BARRIER_TIMEOUT = 2  # dt_options.flags: failure-detection test hook
 OPT_MARGINAL = 8             # dt_options.flags: marginal (path-independent) scores
+OPT_STAGE_HOST_LOGITS = 16   # dt_options.flags: copy mapped host logits instead of reading in place
 MAX_SPEC = 16
 
 # every symbol include/dt.h declares
@@ -31,7 +32,7 @@ EXPORTS = ("dt_abi_version", "dt_status_string", "dt_prepared_bytes", "dt_prepar
            "dt_build_trees_host", "dt_select_topm_noalloc", "dt_kernel_launches",
            "dt_chain_prepared_bytes", "dt_prepare_chain", "dt_chain_workspace_bytes",
            "dt_chain_kernel_launches", "dt_decode_chains", "dt_tree_positions",
-           "dt_tree_attention", "dt_adaptive_budget")
+           "dt_tree_attention", "dt_adaptive_budget", "dt_mapped_host_pointer")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -87,6 +88,8 @@ def lib():
                C.POINTER(DtTreeOut), C.POINTER(DtOptions), C.c_void_p]
         L.dt_build_trees.argtypes = sig
         L.dt_build_trees_host.argtypes = sig
+        L.dt_mapped_host_pointer.restype = C.c_void_p
+        L.dt_mapped_host_pointer.argtypes = [C.c_void_p, C.c_size_t]
         L.dt_select_topm_noalloc.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
                                              C.c_void_p, C.c_void_p, C.c_void_p]
         L.dt_chain_prepared_bytes.restype = C.c_size_t
@@ -237,6 +240,12 @@ def build_trees_host(dims: DtDims, w: DeviceWeights, prepared, base_logits, H, s
                                      workspace.numel() * workspace.element_size(), C.byref(o),
                                      C.byref(opt) if opt else None, _stream(stream)),
            "dt_build_trees_host")
+
+
+def mapped_host_pointer(t) -> int | None:
+    """dt_mapped_host_pointer for a host tensor's whole storage extent: the
+    device address kernels can read it through in place, or None."""
+    return lib().dt_mapped_host_pointer(_ptr(t), t.numel() * t.element_size()) or None
 
 
 def select_topm_noalloc(base_logits, M: int, topm, status, stream=None) -> int:

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda.h>  // driver types for cuPointerGetAttribute, resolved at run time
 #include <cuda_runtime.h>
 
 #include "dt_internal.h"
@@ -285,7 +286,34 @@ int record(const dt_options *opt, int i, cudaStream_t st) {
              : DT_ERR_CUDA;
 }
 
-// The round on device buffers; `plan` is already made.
+// Range [start, start + size) of the registration that holds the device
+// address `dp`, from the driver's pointer attributes (resolved through the
+// runtime's entry-point query, so the library does not link the driver).
+bool registration_range(const void *dp, uintptr_t *start, size_t *size) {
+  using GetAttr = CUresult (*)(void *, CUpointer_attribute, CUdeviceptr);
+  static GetAttr fn = [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      f = nullptr;
+    }
+    return reinterpret_cast<GetAttr>(f);
+  }();
+  if (!fn) return false;
+  CUdeviceptr st = 0;
+  size_t sz = 0;
+  const CUdeviceptr p = reinterpret_cast<CUdeviceptr>(dp);
+  if (fn(&st, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, p) != CUDA_SUCCESS ||
+      fn(&sz, CU_POINTER_ATTRIBUTE_RANGE_SIZE, p) != CUDA_SUCCESS || !sz)
+    return false;
+  *start = static_cast<uintptr_t>(st);
+  *size = sz;
+  return true;
+}
+
 // One library-owned non-blocking stream per device for the work that runs
 // beside the caller's stream; created on first use, kept for the process.
 cudaStream_t side_stream() {
@@ -550,6 +578,33 @@ int dt_build_trees(const dt_dims *dims, const dt_weights *w, const void *prepare
                    out, opt, static_cast<cudaStream_t>(stream));
 }
 
+const void *dt_mapped_host_pointer(const void *host, size_t bytes) {
+  if (!host || !bytes) return nullptr;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  // memory registered for one device only is not mapped for the others
+  if (a.device != dev) {
+    unsigned flags = 0;
+    if (cudaHostGetFlags(&flags, const_cast<void *>(host)) != cudaSuccess ||
+        !(flags & cudaHostAllocPortable)) {
+      cudaGetLastError();
+      return nullptr;
+    }
+  }
+  uintptr_t start = 0;
+  size_t size = 0;
+  const uintptr_t dp = reinterpret_cast<uintptr_t>(a.devicePointer);
+  if (!registration_range(a.devicePointer, &start, &size)) return nullptr;
+  if (dp < start || dp - start > size || size - (dp - start) < bytes) return nullptr;
+  return a.devicePointer;
+}
+
 size_t dt_host_workspace_bytes(const dt_dims *dims, const dt_options *opt) {
   size_t ws = dt_workspace_bytes(dims, opt);
   if (!ws) return 0;
@@ -590,7 +645,16 @@ int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *pr
     return cudaMemcpyAsync(dst, wsb + off, bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess;
   };
   const size_t nb = static_cast<size_t>(d.batch);
-  if (!h2d(s.base, base_logits, sizeof(float) * nb * d.D * d.V) ||
+  // mapped page-locked logits are read in place by the top-M scan (the only
+  // reader of the full rows) instead of being copied first
+  const size_t base_bytes = sizeof(float) * nb * d.D * d.V;
+  const float *base_dev = nullptr;
+  if (!(opt && (opt->flags & DT_OPT_STAGE_HOST_LOGITS))) {
+    base_dev = static_cast<const float *>(dt_mapped_host_pointer(base_logits, base_bytes));
+    if (base_dev && (!dt::aligned4(base_dev) || (d.V % 4 == 0 && !dt::aligned16(base_dev))))
+      base_dev = nullptr;
+  }
+  if ((!base_dev && !h2d(s.base, base_logits, base_bytes)) ||
       (!marginal && !h2d(s.H, H, sizeof(float) * nb * d.D * d.d)) ||
       (!marginal && !h2d(s.state0, state0, sizeof(float) * nb * d.d_s)) ||
       !h2d(s.anchor, anchor_tok, sizeof(int32_t) * nb) ||
@@ -604,7 +668,8 @@ int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *pr
   dev.mask = host_out->mask ? reinterpret_cast<uint8_t *>(wsb + s.mask) : nullptr;
   dev.topm = host_out->topm ? reinterpret_cast<int32_t *>(wsb + s.topm) : nullptr;
   dev.status = reinterpret_cast<int32_t *>(wsb + s.status);
-  rc = run_round(pl, w, prepared, reinterpret_cast<const float *>(wsb + s.base),
+  rc = run_round(pl, w, prepared,
+                 base_dev ? base_dev : reinterpret_cast<const float *>(wsb + s.base),
                  reinterpret_cast<const float *>(wsb + s.H),
                  reinterpret_cast<const float *>(wsb + s.state0),
                  reinterpret_cast<const int32_t *>(wsb + s.anchor),

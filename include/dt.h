@@ -129,6 +129,11 @@ typedef struct {
  * and may be NULL; one small kernel replaces the projection and the search. */
 #define DT_OPT_MARGINAL 8
 
+/* dt_options.flags, dt_build_trees_host only: copy the base logits into the
+ * workspace even when they are mapped page-locked memory (by default such
+ * logits are read in place; see dt_build_trees_host). */
+#define DT_OPT_STAGE_HOST_LOGITS 16
+
 
 #define DT_NUM_PHASE_EVENTS 4 /* start, after top-M, after the projection, after the search */
 
@@ -183,13 +188,27 @@ int dt_build_trees(const dt_dims *dims, const dt_weights *w, const void *prepare
  * the workspace, builds the trees and copies the outputs back, all on `stream`;
  * synchronise the stream before reading the outputs. The workspace must be
  * dt_host_workspace_bytes() bytes. The weights and `prepared` stay on the device.
- * Host output pointers follow dt_tree_out (mask and topm may be NULL). */
+ * Host output pointers follow dt_tree_out (mask and topm may be NULL).
+ * Base logits in page-locked memory that the device maps (dt_mapped_host_pointer
+ * returns non-NULL for the whole [batch][D][V] extent, at the alignment
+ * dt_build_trees asks for) are not copied: the top-M scan, their only reader,
+ * reads them in place over the host link. DT_OPT_STAGE_HOST_LOGITS turns this
+ * off. Either way the host inputs must stay unchanged until `stream` has passed
+ * the call, as for any asynchronous copy. */
 size_t dt_host_workspace_bytes(const dt_dims *dims, const dt_options *opt);
 int dt_build_trees_host(const dt_dims *dims, const dt_weights *w, const void *prepared,
                         const float *base_logits, const float *H, const float *state0,
                         const int32_t *anchor_tok, const float *temperature,
                         void *workspace, size_t workspace_bytes, const dt_tree_out *host_out,
                         const dt_options *opt, void *stream);
+
+/* Device address through which kernels on the current device can read `bytes`
+ * bytes of host memory starting at `host` in place, or NULL. Non-NULL only for
+ * page-locked memory (cudaHostAlloc, cudaHostRegister) mapped for the current
+ * device whose registration covers the whole extent, as the driver reports it;
+ * pageable memory, device memory, a failed query or an extent past the end of
+ * its registration give NULL. Host only; clears any CUDA error it provokes. */
+const void *dt_mapped_host_pointer(const void *host, size_t bytes);
 
 /* Allocation-free top-M selection (the pages have no counterpart: this entry
  * point exists for callers of this library that may not allocate device memory,

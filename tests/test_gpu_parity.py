@@ -230,14 +230,32 @@ def test_host_io_variant_matches_device():
     host_ws = torch.empty(dt.host_workspace_bytes(tb.dims, tb.opt), dtype=torch.uint8,
                           device="cuda")
     pin = lambda a, t: torch.from_numpy(np.ascontiguousarray(a, dtype=t)).pin_memory()
-    out = dt.alloc_outputs(tb.dims, "cpu", pin=True)
-    dt.build_trees_host(tb.dims, tb.w, tb.prepared, pin(wl.base_logits, np.float32),
-                        pin(wl.H, np.float32), pin(wl.state0, np.float32),
-                        pin(wl.anchor, np.int32), pin(wl.temperature, np.float32), host_ws,
-                        out, tb.opt)
-    torch.cuda.synchronize()
-    for key in ("tokens", "parents", "depths", "scores", "mask", "topm", "status"):
-        np.testing.assert_array_equal(out[key].numpy(), dev[key])
+    base = pin(wl.base_logits, np.float32)
+    # page-locked logits are mapped: read in place by default, copied with the flag
+    assert dt.mapped_host_pointer(base) is not None
+    paged = torch.from_numpy(np.ascontiguousarray(wl.base_logits, dtype=np.float32))
+    for logits, flags in ((base, 0), (base, dt.OPT_STAGE_HOST_LOGITS), (paged, 0)):
+        out = dt.alloc_outputs(tb.dims, "cpu", pin=True)
+        dt.build_trees_host(tb.dims, tb.w, tb.prepared, logits,
+                            pin(wl.H, np.float32), pin(wl.state0, np.float32),
+                            pin(wl.anchor, np.int32), pin(wl.temperature, np.float32), host_ws,
+                            out, dt.options(flags=flags))
+        torch.cuda.synchronize()
+        for key in ("tokens", "parents", "depths", "scores", "mask", "topm", "status"):
+            np.testing.assert_array_equal(out[key].numpy(), dev[key])
+
+
+def test_mapped_host_pointer():
+    pinned = torch.zeros(1 << 20, dtype=torch.float32).pin_memory()
+    p = dt.mapped_host_pointer(pinned)
+    assert p is not None
+    lib = dt.lib()
+    # an extent past the registration, pageable memory and device memory are not mapped
+    assert lib.dt_mapped_host_pointer(pinned.data_ptr(), 1 << 40) is None
+    assert dt.mapped_host_pointer(torch.zeros(1 << 20, dtype=torch.float32)) is None
+    assert dt.mapped_host_pointer(torch.zeros(1 << 20, dtype=torch.float32, device="cuda")) is None
+    # a sub-range of the registration is mapped at the matching offset
+    assert lib.dt_mapped_host_pointer(pinned.data_ptr() + 4096, 4096) == p + 4096
 
 
 # --------------------------------------------- more requests than one wave

@@ -979,7 +979,8 @@ __device__ void score_cols(const ChainParams &p, const Tables *t, int b, int g, 
                 __float_as_uint(base_score + lp);
             st_relaxed_u64(p.kids + static_cast<size_t>(slot) * p.k + x, w);
           }
-          if (x < 4 && j < p.D)
+          // (a bulk prefetch of a bad address is a fault: the token is checked)
+          if (x < 4 && j < p.D && tok >= 0 && tok < p.V)
             prefetch_l2(p.G + static_cast<size_t>(tok) * 3 * p.d_s,
                         static_cast<uint32_t>(12u * p.d_s));
         }
@@ -1030,7 +1031,9 @@ __device__ bool gru_cols(const ChainParams &p, int b, int g, const GhWork &help,
   if (threadIdx.x < mine) {   // the rows that do not wait for a gh sum, on their way to L2
     const int4 rec = s_rec[threadIdx.x];
     const int pe = (rec.y & 0xffff) - 1;
-    prefetch_l2(p.G + static_cast<size_t>(rec.z) * 3 * p.d_s, static_cast<uint32_t>(12u * p.d_s));
+    if (rec.z >= 0 && rec.z < p.V)
+      prefetch_l2(p.G + static_cast<size_t>(rec.z) * 3 * p.d_s,
+                  static_cast<uint32_t>(12u * p.d_s));
     if (pe >= 0)
       prefetch_l2(p.S_store + (static_cast<size_t>(b) * (p.e_cap + 1) + pe) * p.d_s,
                   static_cast<uint32_t>(4u * p.d_s));

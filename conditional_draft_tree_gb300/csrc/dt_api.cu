@@ -445,7 +445,7 @@ int decode_plan_for(const dt_dims *dims, dt::DecodePlan *pl) {
     const int ks = sms / tiles, kmax = (d.d + 15) / 16;
     pl->proj_ksplit = ks < 1 ? 1 : (ks > 32 ? 32 : (ks > kmax ? kmax : ks));
   }
-  const size_t vpad = static_cast<size_t>(pl->n_tV) * 128, gn = static_cast<size_t>(pl->n_tV) * 4;
+  const size_t gn = static_cast<size_t>(pl->n_tV) * 4;
   size_t off = 0;
   pl->off_ctrl = off;  off = dt::al(off + sizeof(dt::Ctrl));
   pl->off_U = off;     off = dt::al(off + sizeof(float) * rows * d.r);
@@ -453,7 +453,6 @@ int decode_plan_for(const dt_dims *dims, dt::DecodePlan *pl) {
   off = dt::al(off + (pl->proj_ksplit > 1 ? sizeof(float) * pl->proj_ksplit * rows * d.r : 0));
   pl->off_ypart = off; off = dt::al(off + sizeof(float) * pl->n_kz * wave * pl->R);
   pl->off_S = off;     off = dt::al(off + sizeof(float) * wave * d.d_s);
-  pl->off_X = off;     off = dt::al(off + sizeof(float) * wave * vpad);
   pl->off_stm = off;   off = dt::al(off + sizeof(float) * wave * gn);
   pl->off_sts = off;   off = dt::al(off + sizeof(float) * wave * gn);
   pl->off_sta = off;   off = dt::al(off + sizeof(int32_t) * wave * gn);
@@ -769,7 +768,7 @@ int dt_decode_chains(const dt_dims *dims, const dt_weights *w, const void *prepa
   a.anchor = anchor_tok;
   a.ypart = reinterpret_cast<float *>(wsb + pl.off_ypart);
   a.S = reinterpret_cast<float *>(wsb + pl.off_S);
-  a.X = reinterpret_cast<float *>(wsb + pl.off_X);
+  a.W2 = static_cast<const uint16_t *>(w->W2);
   a.st_m = reinterpret_cast<float *>(wsb + pl.off_stm);
   a.st_s = reinterpret_cast<float *>(wsb + pl.off_sts);
   a.st_a = reinterpret_cast<int32_t *>(wsb + pl.off_sta);

@@ -24,10 +24,11 @@
 //      streamed by bulk copies through a 4-stage ring, h's three terms as B),
 //      two TMEM accumulators so that the epilogue of one tile overlaps the
 //      MMAs of the next. The epilogue sums the three terms, adds L_base,
-//      divides by T, stores x and reduces every 32-token group to (max, sum of
-//      exp, first argmax).
+//      divides by T and reduces every 32-token group to (max, sum of exp,
+//      first argmax); the logits themselves are not stored.
 //   D. per request: combine the groups, take the token (argmax, or the group
-//      and then the token where the CDF passes u Z), its log-probability, then
+//      where the CDF passes u Z and then the token in it, the group's 32
+//      logits recomputed from h and their W2 rows), its log-probability, then
 //      the GRU step S_i = GRU(S_{i-1}, E[d_i]) from the prepared input table G
 //      and the recurrent half from A.
 // Block roles: warps 0-7 build B operands, run epilogues, sampling and the GRU;
@@ -69,7 +70,8 @@ struct DecodeParams {
   const unsigned char *wall, *w2;
   const float *G, *b_hh, *U, *base, *state0, *temperature, *uniforms;
   const int32_t *anchor;
-  float *ypart, *S, *X, *st_m, *st_s;
+  const uint16_t *W2;           // [V][r] bf16 bits, the caller's W2 (the sampled group's logits)
+  float *ypart, *S, *st_m, *st_s;
   int32_t *st_a;
   int *flags;
   Ctrl *ctrl;
@@ -348,7 +350,6 @@ __device__ bool vocab_gemm(const DecodeParams &p, int i, unsigned char *ring, un
             const float bv = cur[c + j];
             if (bv != bv || bv == __int_as_float(0x7f800000)) atomicOr(&p.flags[b], 1);
             x = __fdiv_rn(bv + ((a[j] + m[j]) + l[j]), s_T[b]);
-            __stcs(p.X + static_cast<size_t>(b) * p.n_tV * 128 + v, x);
           }
           const float mx = warp_max(x);
           const float e = (x == ninf) ? 0.0f : expf(x - mx);
@@ -536,11 +537,58 @@ __device__ void choose_token(const DecodeParams &p, int i, int b) {
       s_f[1] = gsel >= 0 ? cum : __int_as_float(0x7f800000);   // +inf: take the last token with mass
     }
     __syncthreads();
+    // the chosen group's 32 logits: (L_base + W2[v] . h) / T with h = SiLU(U_i
+    // + W1_S S) of this request summed as the GEMM's B operand was (same
+    // order), h in chunks of 256 in shared memory; fp32 products (the GEMM took
+    // products of h's three bf16 terms: the same value to a few ulps, which
+    // moves a choice only at a near tie)
+    __shared__ float s_h[256];
+    const int gsel = s_i[3];   // >= 0: the group holding the CDF crossing or the last one with mass
+    const float before = s_f[1];
+    const bool gok = gsel >= 0 && gsel < p.Gn;
+    const int v = gok ? gsel * 32 + lane : p.V;   // (p.V: no token, nothing read)
+    float dl = 0.0f;
+    for (int k0 = 0; k0 < p.r; k0 += 256) {
+      const int kn = min(256, p.r - k0);
+      for (int k = tid; k < kn; k += kDThreads) {
+        // the K-range partials in order, kKzBatch loads in flight
+        const float *src = p.ypart + static_cast<size_t>(b) * p.R + 3 * p.d_s + k0 + k;
+        const size_t zstep = static_cast<size_t>(p.bpad) * p.R;
+        float acc = 0.0f;
+        for (int kz0 = 0; kz0 < p.n_kz; kz0 += kKzBatch) {
+          float q[kKzBatch];
+#pragma unroll
+          for (int z = 0; z < kKzBatch; ++z)
+            q[z] = kz0 + z < p.n_kz ? __ldcg(src + (kz0 + z) * zstep) : 0.0f;
+#pragma unroll
+          for (int z = 0; z < kKzBatch; ++z)
+            if (kz0 + z < p.n_kz) acc += q[z];
+        }
+        s_h[k] = siluf_(__ldg(p.U + (static_cast<size_t>(gb) * p.D + i) * p.r + k0 + k) + acc);
+      }
+      __syncthreads();
+      if (warp == 0 && v < p.V) {
+        const uint16_t *w = p.W2 + static_cast<size_t>(v) * p.r + k0;
+#pragma unroll 4
+        for (int k = 0; k < kn; k += 8) {
+          const uint4 q = __ldg(reinterpret_cast<const uint4 *>(w + k));
+          const uint32_t q4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            dl = fmaf(__uint_as_float(q4[t] << 16), s_h[k + 2 * t], dl);
+            dl = fmaf(__uint_as_float(q4[t] & 0xffff0000u), s_h[k + 2 * t + 1], dl);
+          }
+        }
+      }
+      __syncthreads();
+    }
     if (warp == 0) {
-      const int gsel = s_i[3];
-      const float before = s_f[1];
-      const int v = gsel * 32 + lane;
-      const float x = v < p.V ? __ldcs(p.X + static_cast<size_t>(b) * p.n_tV * 128 + v) : ninf;
+      float x = ninf;
+      if (v < p.V) {
+        const float bv = p.base[(static_cast<size_t>(gb) * p.D + i) * p.V + v];
+        const float T = p.temperature ? p.temperature[gb] : 1.0f;
+        x = __fdiv_rn(bv + dl, T);
+      }
       const float e = (x == ninf) ? 0.0f : expf(x - M);
       float c = e;
       for (int o = 1; o < 32; o <<= 1) {
@@ -786,7 +834,8 @@ cudaError_t launch_decode(const DecodePlan &pl, const DecodeArgs &a, cudaStream_
   p.w2 = p.wall + static_cast<size_t>(pl.n_tA) * pl.nchA * kChunkBytes;
   p.G = a.G; p.b_hh = a.b_hh; p.U = a.U; p.base = a.base; p.state0 = a.state0;
   p.temperature = a.temperature; p.uniforms = a.uniforms; p.anchor = a.anchor;
-  p.ypart = a.ypart; p.S = a.S; p.X = a.X; p.st_m = a.st_m; p.st_s = a.st_s; p.st_a = a.st_a;
+  p.ypart = a.ypart; p.S = a.S; p.st_m = a.st_m; p.st_s = a.st_s; p.st_a = a.st_a;
+  p.W2 = a.W2;
   p.flags = a.flags; p.ctrl = a.ctrl;
   p.tokens = a.tokens; p.logprobs = a.logprobs; p.status = a.status;
   void *args[] = {&p};

@@ -102,7 +102,7 @@ struct DecodePlan {
   int R, n_tA, nchA, n_kz, n_tV, nchV, kb;
   size_t smem;
   int proj_ksplit;
-  size_t off_ctrl, off_U, off_upart, off_ypart, off_S, off_X, off_stm, off_sts, off_sta,
+  size_t off_ctrl, off_U, off_upart, off_ypart, off_S, off_stm, off_sts, off_sta,
       off_flags, off_end;
 };
 struct DecodeArgs {
@@ -110,7 +110,8 @@ struct DecodeArgs {
   const float *G;              // dt_prepare_weights output [V][3 d_s]
   const float *b_hh, *U, *base, *state0, *temperature, *uniforms;
   const int32_t *anchor;
-  float *ypart, *S, *X, *st_m, *st_s;
+  const uint16_t *W2;          // [V][r] bf16 bits
+  float *ypart, *S, *st_m, *st_s;
   int32_t *st_a;
   int *flags;
   Ctrl *ctrl;

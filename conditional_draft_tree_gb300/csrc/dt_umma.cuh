@@ -145,61 +145,6 @@ __device__ __forceinline__ void fence_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// ------------------------------------------------------- thread-block clusters
-
-// shared::cluster address of the same shared-memory offset in CTA `rank`
-__device__ __forceinline__ uint32_t mapa_u32(uint32_t saddr, int rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(caddr)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void st_cluster_f4(uint32_t caddr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(caddr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-// one arrival (release, cluster scope) on an mbarrier of another CTA
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
-               : "memory");
-}
-// bounded wait (acquire, cluster scope) for the phase of the given parity
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *mbar, uint32_t parity,
-                                                  uint64_t limit_ns) {
-  const uint32_t a = smem_u32(mbar);
-  uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (done) return true;
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    if (it == 0) t0 = t;
-    else if (t - t0 > limit_ns) return false;
-  }
-}
-// hardware cluster barrier of every thread of every CTA in the cluster
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // 16-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros.
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),

@@ -366,7 +366,7 @@ def chain_leg(wl, W, dt, torch, dev, flush, st, K, Wm, inp, greedy):
             "sampling": "greedy (T = 0)" if greedy else "inverse CDF at the workload's T"}
 
 
-def verify_leg(W, dt, torch, np, dev, flush, st, K, Wm, mask):
+def verify_leg(W, dt, torch, np, dev, flush, st, K, Wm, mask, pk):
     """Verify-side tree attention (dt_tree_attention) over the trees of the main
     leg: Qwen3-8B attention shape (32 query heads, 8 key/value heads, dh 128),
     one layer, prefix cache padded to 1024 keys with lengths in [512, 1024],
@@ -391,13 +391,17 @@ def verify_leg(W, dt, torch, np, dev, flush, st, K, Wm, mask):
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     seen = mask.to(torch.int64).sum(-1).cpu().numpy() + plen[:, None]   # visible keys per row
-    flops = 4.0 * dh * H * float(seen.sum())           # q.k and p.v, 2 flops per product
-    peak = 152 * 128 * 2 * 2.07e9 / 1e12                # FP32 FMA lanes x clock (alu bound)
+    # useful flops: q.k and p.v over the visible keys, 2 flops per product (the
+    # tensor cores also compute masked keys of a chunk, S twice and P.V in two
+    # bf16 terms: about 4x as many issued)
+    flops = 4.0 * dh * H * float(seen.sum())
+    peak = pk["bf16_tflops"]
     ach = flops / (ms * 1e-3) / 1e12
     return {"us_per_layer": 1000.0 * ms, "shape": f"batch {B}, H {H}, Hkv {Hkv}, n1 {n1}, "
-            f"prefix <= {P}, dh {dh}", "roofline": {"bound": "alu", "achieved": ach, "peak": peak,
-            "unit": "TFLOP/s", "frac": ach / peak, "peak_kind": "FP32 FMA, 152 SMs x 128 lanes x "
-            "2.07 GHz"}, "finite": bool(torch.isfinite(out).all().item())}
+            f"prefix <= {P}, dh {dh}", "roofline": {"bound": "tensor", "achieved": ach,
+            "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+            "peak_kind": f"bf16 dense burst, {pk['source']}"},
+            "finite": bool(torch.isfinite(out).all().item())}
 
 
 def adaptive_leg(dt, torch, dev, st, K, out, N, c_fixed=1.0, c_node=1.0 / 256):
@@ -585,7 +589,7 @@ def main():
     adaptive = adaptive_leg(dt, torch, dev, st, K, out, wl.N)
     verify = None
     if not args.no_verify:
-        verify = verify_leg(W, dt, torch, np, dev, flush, st, K, Wm, out["mask"])
+        verify = verify_leg(W, dt, torch, np, dev, flush, st, K, Wm, out["mask"], peaks())
     chain = None
     if not args.no_chain:
         chain = {"sampled": chain_leg(wl, W, dt, torch, dev, flush, st, K, Wm, inp, False),

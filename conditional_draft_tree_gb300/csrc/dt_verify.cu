@@ -11,15 +11,22 @@
 // the anchor is tree row 0 at position prefix_len and a node at depth j sits at
 // prefix_len + j (empty rows: -1).
 //
-// Attention: one block per (request, query head), 8 warps; a warp owns up to
-// kQW query rows of a pass. Keys stream in chunks of 32 (one per lane) through
-// shared memory as fp32, the next chunk's global loads in flight while the
-// current one is used. Scores are q . k over the head dimension (each lane one
-// key), masked by visibility (prefix key p < prefix_len, tree key t iff
-// mask[row][t]), then an online softmax per row (running max and sum, warp
-// reductions) and the weighted sum of values (each lane 64/32 ... dh/32 output
-// dims). bf16 Q/K/V, fp32 arithmetic and output. CUDA cores (FFMA): the work per
-// request and layer is small and irregular (65 rows of a 64-node tree).
+// Attention on the tensor cores (tcgen05): one block of four warps per
+// (request, key/value head, tile of 128 query rows), where the rows of the
+// H / Hkv query heads that share the key/value head are stacked (head-major),
+// so K and V are staged once for all of them; TMEM lane t is query row t of
+// the tile, and thread t owns it. Keys are taken in chunks of 64: the visible
+// prefix [0, prefix_len) and the tree rows (prefix keys past prefix_len are
+// never read). Two passes over the chunks:
+//   1. S = Q K^T (bf16 operands, exact products, fp32 accumulation in TMEM),
+//      then the thread's running row maximum m and sum l of exp(x - m) over
+//      its visible keys (x = scale S);
+//   2. S again, e = exp(x - m) (0 where not visible) as two bf16 terms hi + lo
+//      (16 significant bits), O += e_hi V + e_lo V in TMEM;
+// and out = O / l (0 for a row that sees no key). Operands are staged in
+// shared memory in the K-major no-swizzle layout of dt_umma.cuh: Q and the
+// key chunk as they are stored, V transposed (head dimension as rows). One
+// thread issues the MMAs; completion is an mbarrier commit, every wait bounded.
 #include <cmath>
 #include <cstdint>
 
@@ -27,14 +34,15 @@
 
 #include "dt_common.cuh"
 #include "dt_internal.h"
+#include "dt_umma.cuh"
 
 namespace dt {
 
 namespace {
 
-constexpr int kVThreads = 256;
-constexpr int kQW = 9;                  // query rows per warp and pass (72 per pass)
-constexpr int kRows = 8 * kQW;
+constexpr int kAThreads = 128;         // one thread per query row of a tile
+constexpr int kKeys = 64;               // keys per chunk (the S tile's N)
+constexpr uint64_t kAttnLimitNs = 2000000000ull;
 
 struct TreeAttnArgs {
   const uint16_t *q, *k, *v;
@@ -45,171 +53,241 @@ struct TreeAttnArgs {
   float *out;
 };
 
-__device__ __forceinline__ void bf16x8_to_f32(uint4 x, float *dst) {
-  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    dst[2 * i] = __uint_as_float(w[i] << 16);
-    dst[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+// TMEM columns of the block: O (DH columns) at 0, S (kKeys) after it, rounded
+// up to a power of two
+template <int DH>
+__host__ __device__ constexpr uint32_t attn_tmem_cols() {
+  return DH + kKeys <= 128 ? 128u : (DH + kKeys <= 256 ? 256u : 512u);
+}
+template <int DH>
+__host__ __device__ constexpr int attn_smem_bytes() {
+  // Q tile, K chunk, V^T chunk, e in two terms
+  return 128 * DH * 2 + kKeys * DH * 2 + DH * kKeys * 2 + 2 * 128 * kKeys * 2;
 }
 
-// DPL consecutive floats at p (p is DPL * 4-byte aligned: float4 steps when
-// DPL is a multiple of 4, one float2 when DPL is 2)
-template <int DPL>
-__device__ __forceinline__ void load_dpl(const float *p, float (&v)[DPL]) {
-  static_assert(DPL == 2 || DPL % 4 == 0, "dims per lane");
-  if constexpr (DPL == 2) {
-    const float2 x = *reinterpret_cast<const float2 *>(p);
-    v[0] = x.x; v[1] = x.y;
-  } else {
-#pragma unroll
-    for (int e = 0; e < DPL; e += 4) {
-      const float4 x = *reinterpret_cast<const float4 *>(p + e);
-      v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
-    }
-  }
-}
-template <int DPL>
-__device__ __forceinline__ void store_dpl(float *p, const float (&v)[DPL]) {
-  static_assert(DPL == 2 || DPL % 4 == 0, "dims per lane");
-  if constexpr (DPL == 2) {
-    *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
-  } else {
-#pragma unroll
-    for (int e = 0; e < DPL; e += 4)
-      *reinterpret_cast<float4 *>(p + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-  }
-}
-
-// this thread's share of the K and V rows [c0, c0 + 32) (zeros past L)
-template <int U, int C8, int DH>
-__device__ __forceinline__ void fetch_chunk(const uint16_t *kb, const uint16_t *vb, int c0, int L,
-                                            uint4 (&pk)[U], uint4 (&pv)[U]) {
-#pragma unroll
-  for (int j = 0; j < U; ++j) {
-    const int u = threadIdx.x + j * kVThreads, key = u / C8, c8 = u - key * C8;
-    const int jj = c0 + key;
-    pk[j] = make_uint4(0u, 0u, 0u, 0u);
-    pv[j] = make_uint4(0u, 0u, 0u, 0u);
-    if (jj < L) {
-      pk[j] = *reinterpret_cast<const uint4 *>(kb + static_cast<size_t>(jj) * DH + c8 * 8);
-      pv[j] = *reinterpret_cast<const uint4 *>(vb + static_cast<size_t>(jj) * DH + c8 * 8);
-    }
-  }
-}
-
-template <int DPL>
-__global__ void __launch_bounds__(kVThreads) tree_attention_kernel(TreeAttnArgs a) {
-  constexpr int DH = 32 * DPL;          // head dimension
-  constexpr int KS = DH + 4;            // K row stride: conflict-free 16-byte reads by lane
-  constexpr int C8 = DH / 8;            // 16-byte units per row
-  constexpr int U = 32 * C8 / kVThreads;  // units per thread per chunk (K, and V)
-  static_assert(U >= 1, "head dimension too small");
-  extern __shared__ __align__(16) float sm[];
-  float *sK = sm;                       // [32][KS]
-  float *sV = sK + 32 * KS;             // [32][DH]
-  float *sQ = sV + 32 * DH;             // [kRows][DH]
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hk = h / (a.H / a.Hkv);
+template <int DH>
+__global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs a) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_fail;
+  unsigned char *sQ = sm;                              // [128 rows][DH], K-major
+  unsigned char *sK = sQ + 128 * DH * 2;               // [kKeys rows][DH]
+  unsigned char *sV = sK + kKeys * DH * 2;             // [DH rows][kKeys] (V^T)
+  unsigned char *sE = sV + DH * kKeys * 2;             // 2 x [128 rows][kKeys]
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int mt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int G = a.H / a.Hkv, rows = G * a.n1;
   const int L = a.P + a.n1;
   const int plen = min(max(a.prefix_len[b], 0), a.P);
   const uint16_t *kb = a.k + (static_cast<size_t>(b) * a.Hkv + hk) * L * DH;
   const uint16_t *vb = a.v + (static_cast<size_t>(b) * a.Hkv + hk) * L * DH;
-  const uint16_t *qb = a.q + (static_cast<size_t>(b) * a.H + h) * a.n1 * DH;
-  float *ob = a.out + (static_cast<size_t>(b) * a.H + h) * a.n1 * DH;
   const uint8_t *mb = a.mask + static_cast<size_t>(b) * a.n1 * a.n1;
+  // this thread's query row
+  const int g = mt * 128 + tid;
+  const bool mine = g < rows;
+  const int h = hk * G + (mine ? g / a.n1 : 0), qr = mine ? g % a.n1 : 0;
   const float ninf = -__int_as_float(0x7f800000);
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
 
-  for (int pass = 0; pass < a.n1; pass += kRows) {
-    __syncthreads();   // the previous pass is done with sQ
-    for (int u = threadIdx.x; u < kRows * C8; u += kVThreads) {
-      const int row = u / C8, c8 = u - row * C8, r = pass + row;
-      const uint4 x = r < a.n1 ? *reinterpret_cast<const uint4 *>(qb + static_cast<size_t>(r) * DH + c8 * 8)
-                               : zero;
-      bf16x8_to_f32(x, sQ + row * DH + c8 * 8);
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    s_fail = 0;
+  }
+  if (warp == 0) tmem_alloc(&s_tmem, attn_tmem_cols<DH>());
+  // Q tile: 16-byte pieces in place (rows past the group are zeros)
+  constexpr int C8 = DH / 8;
+  for (int u = tid; u < 128 * C8; u += kAThreads) {
+    const int r = u / C8, c8 = u - r * C8, gr = mt * 128 + r;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (gr < rows) {
+      const int hh = hk * G + gr / a.n1, rr = gr % a.n1;
+      x = *reinterpret_cast<const uint4 *>(
+          a.q + ((static_cast<size_t>(b) * a.H + hh) * a.n1 + rr) * DH + c8 * 8);
     }
-    float m[kQW], l[kQW], o[kQW][DPL];
+    *reinterpret_cast<uint4 *>(sQ + umma_offset(r, c8 * 8, DH)) = x;
+  }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t t_o = tmem, t_s = tmem + DH;
+  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t idesc_s = umma_idesc_bf16(128, kKeys), idesc_o = umma_idesc_bf16(128, DH);
+  // chunks: the visible prefix, then the tree rows
+  const int npre = (plen + kKeys - 1) / kKeys, ntree = (a.n1 + kKeys - 1) / kKeys;
+  const int nch = npre + ntree;
+  uint32_t phase = 0;
+  auto chunk_first = [&](int c) { return c < npre ? c * kKeys : a.P + (c - npre) * kKeys; };
+  auto chunk_end = [&](int c) { return c < npre ? plen : a.P + a.n1; };
+  // visibility of key j (within [first, end)) for this thread's row
+  auto visible = [&](int j) {
+    return j < a.P ? j < plen : mb[static_cast<size_t>(qr) * a.n1 + (j - a.P)] != 0;
+  };
+  // key chunk c in registers: unit i of this thread is key 32 (warp & 1) + lane
+  // of the chunk, 16-byte piece c8 = (warp >> 1) + 2 i (a warp covers 32
+  // consecutive keys, so the transposed V stores of a warp spread over banks);
+  // rows past the chunk's end are zeros
+  constexpr int UPT = kKeys * C8 / kAThreads;   // pieces per thread: 8 (DH 128)
+  static_assert(kKeys == 64 && UPT * kAThreads == kKeys * C8, "piece mapping");
+  uint4 pk[UPT], pv[UPT];
+  const int my_key = 32 * (warp & 1) + (tid & 31);
+  auto fetch = [&](int c, bool with_v) {
+    const int j = chunk_first(c) + my_key;
+    const bool in = j < chunk_end(c);
 #pragma unroll
-    for (int qq = 0; qq < kQW; ++qq) {
-      m[qq] = ninf;
-      l[qq] = 0.0f;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) o[qq][e] = 0.0f;
+    for (int i = 0; i < UPT; ++i) {
+      const int c8 = (warp >> 1) + 2 * i;
+      pk[i] = in ? *reinterpret_cast<const uint4 *>(kb + static_cast<size_t>(j) * DH + c8 * 8)
+                 : make_uint4(0u, 0u, 0u, 0u);
+      pv[i] = (in && with_v)
+                  ? *reinterpret_cast<const uint4 *>(vb + static_cast<size_t>(j) * DH + c8 * 8)
+                  : make_uint4(0u, 0u, 0u, 0u);
     }
-    uint4 pk[U], pv[U];
-    fetch_chunk<U, C8, DH>(kb, vb, 0, L, pk, pv);
-    for (int c0 = 0; c0 < L; c0 += 32) {
-      __syncthreads();   // the previous chunk is consumed (and sQ staged)
+  };
+  // the fetched chunk into shared memory (K as is, V transposed)
+  auto stage = [&](bool with_v) {
 #pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const int u = threadIdx.x + j * kVThreads, key = u / C8, c8 = u - key * C8;
-        bf16x8_to_f32(pk[j], sK + key * KS + c8 * 8);
-        bf16x8_to_f32(pv[j], sV + key * DH + c8 * 8);
-      }
-      __syncthreads();
-      if (c0 + 32 < L) fetch_chunk<U, C8, DH>(kb, vb, c0 + 32, L, pk, pv);
-      // scores of key c0 + lane for the warp's rows
-      float s[kQW];
+    for (int i = 0; i < UPT; ++i) {
+      const int c8 = (warp >> 1) + 2 * i;
+      *reinterpret_cast<uint4 *>(sK + umma_offset(my_key, c8 * 8, DH)) = pk[i];
+      if (with_v) {
+        const uint32_t w[4] = {pv[i].x, pv[i].y, pv[i].z, pv[i].w};
 #pragma unroll
-      for (int qq = 0; qq < kQW; ++qq) s[qq] = 0.0f;
-#pragma unroll 4
-      for (int d = 0; d < DH; d += 4) {
-        const float4 k4 = *reinterpret_cast<const float4 *>(sK + lane * KS + d);
-#pragma unroll
-        for (int qq = 0; qq < kQW; ++qq) {
-          const float4 q4 = *reinterpret_cast<const float4 *>(sQ + (warp + 8 * qq) * DH + d);
-          s[qq] = fmaf(q4.x, k4.x, s[qq]);
-          s[qq] = fmaf(q4.y, k4.y, s[qq]);
-          s[qq] = fmaf(q4.z, k4.z, s[qq]);
-          s[qq] = fmaf(q4.w, k4.w, s[qq]);
-        }
-      }
-      const int j = c0 + lane;
-      float p[kQW];
-#pragma unroll
-      for (int qq = 0; qq < kQW; ++qq) {
-        p[qq] = 0.0f;
-        const int r = pass + warp + 8 * qq;
-        if (r >= a.n1) continue;   // warp-uniform
-        const bool vis = j < L && (j < a.P ? j < plen : mb[static_cast<size_t>(r) * a.n1 + (j - a.P)] != 0);
-        const float x = vis ? s[qq] * a.scale : ninf;
-        const float mc = warp_max(x);
-        if (mc == ninf) continue;  // no visible key in this chunk (warp-uniform)
-        const float mn = fmaxf(m[qq], mc);
-        const float alpha = expf(m[qq] - mn);   // 0 while nothing was seen
-        p[qq] = vis ? expf(x - mn) : 0.0f;
-        l[qq] = l[qq] * alpha + warp_sum(p[qq]);
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[qq][e] *= alpha;
-        m[qq] = mn;
-      }
-      // weighted values: lane owns output dims [DPL lane, DPL lane + DPL)
-#pragma unroll 4
-      for (int kk = 0; kk < 32; ++kk) {
-        float vv[DPL];
-        load_dpl<DPL>(sV + kk * DH + lane * DPL, vv);
-#pragma unroll
-        for (int qq = 0; qq < kQW; ++qq) {
-          const float w = __shfl_sync(kFull, p[qq], kk);
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) o[qq][e] = fmaf(w, vv[e], o[qq][e]);
+        for (int e = 0; e < 8; ++e) {
+          const uint16_t x = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xffffu));
+          *reinterpret_cast<uint16_t *>(sV + umma_offset(c8 * 8 + e, my_key, kKeys)) = x;
         }
       }
     }
+    fence_async_smem();   // plain stores -> tensor-core reads
+  };
+  // one thread issues, everyone waits for the commit (bounded)
+  auto mma_wait = [&]() {
+    if (!mbar_wait(&s_bar, phase, kAttnLimitNs)) s_fail = 1;
+    phase ^= 1u;
+    tmem_fence_after();
+  };
+  auto issue_s = [&]() {
+    if (tid == 0) {
+      tmem_fence_after();
 #pragma unroll
-    for (int qq = 0; qq < kQW; ++qq) {
-      const int r = pass + warp + 8 * qq;
-      if (r >= a.n1) continue;
-      const float inv = l[qq] > 0.0f ? 1.0f / l[qq] : 0.0f;
-      float w[DPL];
+      for (int k = 0; k < DH / 16; ++k)
+        umma_bf16(t_s, umma_desc(smem_u32(sQ) + k * 256, 128, 16 * DH),
+                  umma_desc(smem_u32(sK) + k * 256, 128, 16 * DH), idesc_s, k > 0);
+      umma_commit(&s_bar);
+    }
+  };
+  // this thread's row of S for chunk c, scaled, -inf where not visible
+  auto row_scores = [&](int c, float (&x)[kKeys]) {
+    tmem_ld32(t_s + lane_off, x);
+    tmem_ld32(t_s + lane_off + 32, x + 32);
+    tmem_wait_ld();
+    const int j0 = chunk_first(c), j1 = chunk_end(c);
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) w[e] = o[qq][e] * inv;
-      store_dpl<DPL>(ob + static_cast<size_t>(r) * DH + lane * DPL, w);
+    for (int t = 0; t < kKeys; ++t) {
+      const int j = j0 + t;
+      x[t] = (mine && j < j1 && visible(j)) ? x[t] * a.scale : ninf;
+    }
+  };
+
+  // pass 1: row maximum and sum (the next chunk's keys load during the MMAs)
+  float m = ninf, l = 0.0f;
+  fetch(0, false);
+  for (int c = 0; c < nch && !s_fail; ++c) {
+    stage(false);
+    tmem_fence_before();
+    __syncthreads();
+    issue_s();
+    if (c + 1 < nch) fetch(c + 1, false);
+    mma_wait();
+    float x[kKeys];
+    row_scores(c, x);
+    float mc = ninf;
+#pragma unroll
+    for (int t = 0; t < kKeys; ++t) mc = fmaxf(mc, x[t]);
+    if (mc != ninf) {
+      const float mn = fmaxf(m, mc);
+      float sum = 0.0f;
+#pragma unroll
+      for (int t = 0; t < kKeys; ++t) sum += (x[t] == ninf) ? 0.0f : expf(x[t] - mn);
+      l = l * expf(m - mn) + sum;   // (exp(-inf) = 0 while nothing was seen)
+      m = mn;
+    }
+    tmem_fence_before();
+    __syncthreads();   // S read and sK free before the next chunk
+  }
+  // pass 2: O = sum of e V, e = exp(x - m) in two bf16 terms
+  if (!s_fail) fetch(0, true);
+  for (int c = 0; c < nch && !s_fail; ++c) {
+    stage(true);
+    tmem_fence_before();
+    __syncthreads();
+    issue_s();
+    if (c + 1 < nch) fetch(c + 1, true);
+    mma_wait();
+    float x[kKeys];
+    row_scores(c, x);
+#pragma unroll
+    for (int t0 = 0; t0 < kKeys; t0 += 8) {
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        float ev[2];
+#pragma unroll
+        for (int z = 0; z < 2; ++z) ev[z] = (x[t0 + e + z] == ninf) ? 0.0f : expf(x[t0 + e + z] - m);
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(ev[0]), h1 = __float2bfloat16_rn(ev[1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(ev[0] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(ev[1] - __bfloat162float(h1));
+        hi[e >> 1] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                     (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+        lo[e >> 1] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+                     (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+      }
+      *reinterpret_cast<uint4 *>(sE + umma_offset(tid, t0, kKeys)) =
+          make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4 *>(sE + 128 * kKeys * 2 + umma_offset(tid, t0, kKeys)) =
+          make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    fence_async_smem();
+    tmem_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tmem_fence_after();
+#pragma unroll
+      for (int term = 0; term < 2; ++term)
+#pragma unroll
+        for (int k = 0; k < kKeys / 16; ++k)
+          umma_bf16(t_o,
+                    umma_desc(smem_u32(sE) + term * 128 * kKeys * 2 + k * 256, 128, 16 * kKeys),
+                    umma_desc(smem_u32(sV) + k * 256, 128, 16 * kKeys), idesc_o,
+                    c > 0 || term > 0 || k > 0);
+      umma_commit(&s_bar);
+    }
+    mma_wait();
+    tmem_fence_before();
+    __syncthreads();   // sK, sV, sE and S free before the next chunk
+  }
+  // out = O / l
+  if (!s_fail && nch > 0) {
+    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+    float *ob = a.out + ((static_cast<size_t>(b) * a.H + h) * a.n1 + qr) * DH;
+#pragma unroll 1
+    for (int c0 = 0; c0 < DH; c0 += 32) {
+      float o[32];
+      tmem_ld32(t_o + lane_off + c0, o);
+      tmem_wait_ld();
+      if (mine) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4 *>(ob + c0 + e) =
+              make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+      }
     }
   }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, attn_tmem_cols<DH>());
 }
 
 __global__ void tree_positions_kernel(const int32_t *depths, const int32_t *prefix_len,
@@ -222,20 +300,14 @@ __global__ void tree_positions_kernel(const int32_t *depths, const int32_t *pref
   }
 }
 
-template <int DPL>
-size_t attn_smem() {
-  constexpr int DH = 32 * DPL;
-  return sizeof(float) * (32 * (DH + 4) + 32 * DH + kRows * DH);
-}
-
-template <int DPL>
+template <int DH>
 cudaError_t launch_attn(const TreeAttnArgs &a, int batch, cudaStream_t st) {
-  const size_t smem = attn_smem<DPL>();
-  cudaError_t e = cudaFuncSetAttribute(tree_attention_kernel<DPL>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  constexpr int smem = attn_smem_bytes<DH>();
+  cudaError_t e = cudaFuncSetAttribute(tree_attention_kernel<DH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tree_attention_kernel<DPL><<<dim3(a.H, batch), kVThreads, smem, st>>>(a);
+  const int rows = (a.H / a.Hkv) * a.n1;
+  tree_attention_kernel<DH><<<dim3((rows + 127) / 128, a.Hkv, batch), kAThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -274,9 +346,9 @@ int dt_tree_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   a.q = q; a.k = k; a.v = v; a.mask = mask; a.prefix_len = prefix_len;
   a.H = H; a.Hkv = Hkv; a.n1 = n1; a.P = P; a.scale = scale; a.out = out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = dh == 64 ? dt::launch_attn<2>(a, batch, st)
-                : dh == 128 ? dt::launch_attn<4>(a, batch, st)
-                            : dt::launch_attn<8>(a, batch, st);
+  cudaError_t e = dh == 64 ? dt::launch_attn<64>(a, batch, st)
+                : dh == 128 ? dt::launch_attn<128>(a, batch, st)
+                            : dt::launch_attn<256>(a, batch, st);
   return e == cudaSuccess ? DT_OK : DT_ERR_CUDA;
 }
 

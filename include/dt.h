@@ -310,7 +310,9 @@ int dt_decode_chains(const dt_dims *dims, const dt_weights *w, const void *prepa
  *        out_i = sum_j softmax_j(scale q_i . k_j) v_j over the visible keys j,
  *        0 for a row that sees no key
  * Query head h reads key/value head h / (H / Hkv) (H % Hkv == 0). dh is 64, 128
- * or 256; n1 <= DT_MAX_N + 1. fp32 arithmetic on the CUDA cores. Both calls
+ * or 256; n1 <= DT_MAX_N + 1. On the tensor cores: q.k as exact products of the
+ * bf16 inputs accumulated in fp32, the softmax weights in two bf16 terms (16
+ * significant bits) against the bf16 values, fp32 accumulation. Both calls
  * return DT_ERR_INVALID_ARG for bad sizes or pointers and are asynchronous on
  * `stream`. */
 int dt_tree_positions(const int32_t *depths, const int32_t *prefix_len, int batch, int n1,

@@ -105,7 +105,8 @@ def test_rows_that_see_nothing_are_zero():
 def test_qwen3_8b_verification_shape_sampled():
     """Batch 32 trees of the Qwen3-8B workload (N = 64), 32 query heads over 8
     key/value heads, dh = 128, prefix cache padded to 1024 with lengths in
-    [512, 1024]; sampled (request, head) pairs against the oracle, all finite."""
+    [512, 1024]; every head of three requests (all key/value heads and every
+    row tile of the stacked query heads) against the oracle, all finite."""
     wl = W.make_workload(3)
     tb = dt.TreeBuilder.from_numpy(wl)
     out = tb.run(**tb.inputs_to_device(wl))
@@ -113,4 +114,5 @@ def test_qwen3_8b_verification_shape_sampled():
     q, k, v, plen = W.verify_inputs(32, 32, 8, 65, 1024, 128, seed=3, min_prefix=512)
     got = run_attention(q, k, v, out["mask"], plen)
     assert np.isfinite(got).all()
-    check(q, k, v, out["mask"].cpu().numpy(), plen, got, pairs=[(0, 0), (5, 17), (31, 31)])
+    check(q, k, v, out["mask"].cpu().numpy(), plen, got,
+          pairs=[(b, h) for b in (0, 5, 31) for h in range(32)])

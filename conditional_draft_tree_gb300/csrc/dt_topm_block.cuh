@@ -419,14 +419,20 @@ __device__ void block_topm(const float *rowp, int V, int M, int a0, int nv, int 
       }
     }
   };
+  // the starting threshold is taken over the first two tiles of every warp
+  // (both in registers before the loop; the second is not loaded again)
   float4 ta[Q], tb[Q];
   load_tile(ta, w0);
   float lm = -__int_as_float(0x7f800000);
   tile_max(lm, ta, w0, w1, lane);
+  if (w0 + Q * 32 < w1) {
+    load_tile(tb, w0 + Q * 32);
+    tile_max(lm, tb, w0 + Q * 32, w1, lane);
+  }
   start_threshold(st, lm, s_wq);
   for (int base = w0; base < w1; base += 2 * Q * 32) {
     const int b2 = base + Q * 32;
-    if (b2 < w1) load_tile(tb, b2);
+    if (b2 < w1 && base != w0) load_tile(tb, b2);
     filter_tile(st, ta, base, w1, a0);
     if (b2 >= w1) break;
     if (b2 + Q * 32 < w1) load_tile(ta, b2 + Q * 32);

@@ -448,7 +448,11 @@ def config_leg(c, wl, dt, torch, np, dev, flush, st, K, Wm, with_parity, oracle_
         tb.run(**inp, out=out, opt=dt.options(0, ph[i]))
     torch.cuda.synchronize()
     per = sorted(ph[i][0].elapsed_time(ph[i][3]) for i in range(K))
-    search = statistics.median(ph[i][2].elapsed_time(ph[i][3]) for i in range(K))
+    # the search starts after the later of [1] (top-M) and [2] (projection)
+    search = statistics.median(
+        ph[i][0].elapsed_time(ph[i][3])
+        - max(ph[i][0].elapsed_time(ph[i][1]), ph[i][0].elapsed_time(ph[i][2]))
+        for i in range(K))
     ms = statistics.median(per)
     o = {k: v.cpu().numpy() for k, v in out.items() if v is not None}
     cnt = algorithmic_counts(wl, o["tokens"], o["depths"])
@@ -571,9 +575,22 @@ def main():
                             "pop_iterations", "pop_cycles", "select_iterations",
                             "select_cycles"], t_ns[24:32]))
     per = [ph[i][0].elapsed_time(ph[i][3]) for i in range(K)]
-    topm_ms = [ph[i][0].elapsed_time(ph[i][1]) for i in range(K)]
-    proj_ms = [ph[i][1].elapsed_time(ph[i][2]) for i in range(K)]
-    search_ms = [ph[i][2].elapsed_time(ph[i][3]) for i in range(K)]
+    # [1] after the top-M, [2] after the projection: with bf16 weights the
+    # projection runs first ([2] before [1]); with fp32 weights beside the top-M
+    t1 = [ph[i][0].elapsed_time(ph[i][1]) for i in range(K)]
+    t2 = [ph[i][0].elapsed_time(ph[i][2]) for i in range(K)]
+    t3 = [ph[i][0].elapsed_time(ph[i][3]) for i in range(K)]
+    proj_first = statistics.mean(t2) <= statistics.mean(t1)
+    if proj_first:
+        projection_ms = t2
+        topm_ms = [a - b for a, b in zip(t1, t2)]
+        proj_ms = [0.0] * K
+        search_ms = [c - a for a, c in zip(t1, t3)]
+    else:
+        projection_ms = [0.0] * K
+        topm_ms = t1
+        proj_ms = [b - a for a, b in zip(t1, t2)]
+        search_ms = [c - b for b, c in zip(t2, t3)]
     total_ms = max_over_ranks(sum(per), torch, dist, world, dev)
     value = whole_job_rate(world, wl.batch, K, total_ms)
     launches_per_round = dt.kernel_launches(tb.dims, tb.w.wdtype, tb.opt)
@@ -607,9 +624,11 @@ def main():
         o = {k: v.cpu().numpy() for k, v in out.items() if v is not None}
         cnt = algorithmic_counts(wl, o["tokens"], o["depths"])
         pk = peaks()
-        # phase events: top-M (the projection runs beside it on a side stream),
-        # the rest of the projection, the search
-        phases = {"topm": statistics.mean(topm_ms), "projection_tail": statistics.mean(proj_ms),
+        # phase events: the projection when it runs first (tensor cores), the
+        # top-M, the rest of the projection when it runs beside the top-M
+        # (CUDA cores, fp32 weights), the search
+        phases = {"projection": statistics.mean(projection_ms), "topm": statistics.mean(topm_ms),
+                  "projection_tail": statistics.mean(proj_ms),
                   "search": statistics.mean(search_ms)}
         # dominant kernel: the search. Its arithmetic is the recurrent GEMM on
         # the tensor cores (bf16 operands, fp32-exact products of three bf16
@@ -628,7 +647,9 @@ def main():
         ach_t = cnt["topm_bytes"] / (phases["topm"] * 1e-3) / 1e9
         roof_topm = {"bound": "hbm", "achieved": ach_t, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": ach_t / pk["hbm_gbs"], "kernel": "dt::topm_kernel",
-                     "note": "projection GEMM runs concurrently on a side stream"}
+                     "note": ("the projection runs before it on the tensor cores"
+                              if proj_first else
+                              "the projection GEMM runs concurrently on a side stream")}
         round_bytes = cnt["topm_bytes"] + cnt["proj_bytes"] + cnt["search_bytes"]
         status_ok = bool((o["status"] == 0).all())
         line = {

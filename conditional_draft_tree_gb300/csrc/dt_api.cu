@@ -159,9 +159,14 @@ int make_plan_uncached(const dt_dims *dims, int wdtype, const dt_options *opt, P
   const int wave = p->wave;
   const int e_cap = p->e_cap;
 
-  // projection GEMM: split K so that the tiles x chunks fill every SM once
+  // projection U = W1[:, :d] H: on the tensor cores for bf16 weights (about
+  // one block per SM), else the CUDA-core split-K GEMM, its K split so that
+  // the tiles x chunks fill every SM once
+  p->proj_umma = (!p->marginal && proj_umma_supported(d, wdtype)) ? 1 : 0;
   p->proj_ksplit = 1;
-  if (!p->marginal) {
+  if (p->proj_umma) {
+    p->proj_ksplit = proj_umma_split(static_cast<int>(rows), d.r, d.d, p->num_sms);
+  } else if (!p->marginal) {
     const int tiles = gemm_tiles(static_cast<int>(rows), d.r);
     int ks = p->num_sms / tiles;
     const int kmax = (d.d + 15) / 16;
@@ -393,8 +398,11 @@ int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const f
       return DT_ERR_CUDA;
     return record(opt, 3, st);
   }
-  // the projection (compute bound) runs on a side stream beside the top-M
-  // selection (HBM bound); the two touch disjoint workspace regions
+  // the projection runs on a side stream beside the top-M selection on the
+  // main stream; the two touch disjoint workspace regions. On device-resident
+  // logits the top-M blocks fill every SM first and the projection mostly runs
+  // in the slots they free at the end; where the top-M is bound by the host
+  // link (logits read in place from mapped memory) it is hidden entirely.
   cudaStream_t side = side_stream();
   if (!side) return DT_ERR_CUDA;
   Events ev;
@@ -402,10 +410,18 @@ int run_round(const Plan &pl, const dt_weights *w, const void *prepared, const f
   if (cudaEventRecord(ev.fork, st) != cudaSuccess || cudaStreamWaitEvent(side, ev.fork, 0) != cudaSuccess)
     return DT_ERR_CUDA;
   float *U = reinterpret_cast<float *>(wsb + pl.off_U);
-  if (dt::launch_gemm_nt(d.batch * d.D, d.r, d.d, H, DT_F32, d.d, w->W1, w->wdtype,
-                         static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r, pl.proj_ksplit,
-                         reinterpret_cast<float *>(wsb + pl.off_upart), side) != cudaSuccess)
+  float *upart = reinterpret_cast<float *>(wsb + pl.off_upart);
+  if (pl.proj_umma) {
+    // a bounded wait of the projection that runs out aborts the search
+    int *fail = reinterpret_cast<int *>(wsb + pl.off_ctrl + offsetof(dt::Ctrl, abort));
+    if (dt::launch_proj_umma(d.batch * d.D, d.r, d.d, H, d.d, w->W1, d.d + d.d_s, U,
+                             pl.proj_ksplit, upart, fail, side) != cudaSuccess)
+      return DT_ERR_CUDA;
+  } else if (dt::launch_gemm_nt(d.batch * d.D, d.r, d.d, H, DT_F32, d.d, w->W1, w->wdtype,
+                                static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r,
+                                pl.proj_ksplit, upart, side) != cudaSuccess) {
     return DT_ERR_CUDA;
+  }
   if (cudaEventRecord(ev.join, side) != cudaSuccess) return DT_ERR_CUDA;
   if (dt::launch_topm(pl, base_logits, ws, out->topm, st) != cudaSuccess) return DT_ERR_CUDA;
   rc = record(opt, 1, st);
@@ -440,7 +456,12 @@ int decode_plan_for(const dt_dims *dims, dt::DecodePlan *pl) {
   const dt_dims &d = *dims;
   const size_t wave = static_cast<size_t>(pl->wave);
   const long long rows = static_cast<long long>(d.batch) * d.D;
-  {
+  // the projection runs alone before the decoding kernel: on the tensor cores
+  // with about one block per SM, else the CUDA-core GEMM filling every SM once
+  pl->proj_umma = dt::proj_umma_supported(d, DT_BF16) ? 1 : 0;
+  if (pl->proj_umma) {
+    pl->proj_ksplit = dt::proj_umma_split(static_cast<int>(rows), d.r, d.d, sms);
+  } else {
     const int tiles = dt::gemm_tiles(static_cast<int>(rows), d.r);
     const int ks = sms / tiles, kmax = (d.d + 15) / 16;
     pl->proj_ksplit = ks < 1 ? 1 : (ks > 32 ? 32 : (ks > kmax ? kmax : ks));
@@ -751,11 +772,22 @@ int dt_decode_chains(const dt_dims *dims, const dt_weights *w, const void *prepa
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char *wsb = static_cast<char *>(workspace);
   float *U = reinterpret_cast<float *>(wsb + pl.off_U);
-  // U_i = W1[:, :d] H_i for every request and position (path independent)
-  if (dt::launch_gemm_nt(d.batch * d.D, d.r, d.d, H, DT_F32, d.d, w->W1, w->wdtype,
-                         static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r, pl.proj_ksplit,
-                         reinterpret_cast<float *>(wsb + pl.off_upart), st) != cudaSuccess)
+  float *upart = reinterpret_cast<float *>(wsb + pl.off_upart);
+  // the control block starts at zero; a bounded wait of the projection that
+  // runs out sets its abort flag, which every decoding wave then reports
+  if (cudaMemsetAsync(wsb + pl.off_ctrl, 0, sizeof(dt::Ctrl), st) != cudaSuccess)
     return DT_ERR_CUDA;
+  // U_i = W1[:, :d] H_i for every request and position (path independent)
+  if (pl.proj_umma) {
+    int *fail = reinterpret_cast<int *>(wsb + pl.off_ctrl + offsetof(dt::Ctrl, abort));
+    if (dt::launch_proj_umma(d.batch * d.D, d.r, d.d, H, d.d, w->W1, d.d + d.d_s, U,
+                             pl.proj_ksplit, upart, fail, st) != cudaSuccess)
+      return DT_ERR_CUDA;
+  } else if (dt::launch_gemm_nt(d.batch * d.D, d.r, d.d, H, DT_F32, d.d, w->W1, w->wdtype,
+                                static_cast<size_t>(d.d) + d.d_s, nullptr, U, d.r,
+                                pl.proj_ksplit, upart, st) != cudaSuccess) {
+    return DT_ERR_CUDA;
+  }
   dt::DecodeArgs a;
   a.chain_prepared = chain_prepared;
   a.G = static_cast<const float *>(prepared);
@@ -780,8 +812,12 @@ int dt_decode_chains(const dt_dims *dims, const dt_weights *w, const void *prepa
   for (int b0 = 0; b0 < d.batch; b0 += pl.wave) {
     a.b0 = b0;
     a.nb = (d.batch - b0) < pl.wave ? (d.batch - b0) : pl.wave;
-    if (cudaMemsetAsync(wsb + pl.off_ctrl, 0, sizeof(dt::Ctrl), st) != cudaSuccess)
-      return DT_ERR_CUDA;
+    if (b0 > 0) {   // a later wave: everything but the abort flag starts at zero again
+      const size_t ab = offsetof(dt::Ctrl, abort), ae = ab + sizeof(int);
+      if (cudaMemsetAsync(wsb + pl.off_ctrl, 0, ab, st) != cudaSuccess ||
+          cudaMemsetAsync(wsb + pl.off_ctrl + ae, 0, sizeof(dt::Ctrl) - ae, st) != cudaSuccess)
+        return DT_ERR_CUDA;
+    }
     if (dt::launch_decode(pl, a, st) != cudaSuccess) return DT_ERR_CUDA;
   }
   return DT_OK;

@@ -91,17 +91,6 @@ __device__ __forceinline__ bool bad_temperature(float T) {
   return !(T >= 0.0f) || T == __int_as_float(0x7f800000);
 }
 
-// fp32 -> three bf16 terms whose sum is the value (hi, mid, lo)
-__device__ __forceinline__ void split3(float v, uint16_t &a, uint16_t &b, uint16_t &c) {
-  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-  const float r1 = v - __bfloat162float(hi);
-  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-  a = __bfloat16_as_ushort(hi);
-  b = __bfloat16_as_ushort(mid);
-  c = __bfloat16_as_ushort(lo);
-}
-
 // Writes 8 consecutive K values (k0 = 8 kg) of B row b in the three term
 // blocks of the operand (term t at rows t * bpad + b), K-major layout of width kb.
 __device__ __forceinline__ void put_b8(unsigned char *sB, const DecodeParams &p, int b, int kg,

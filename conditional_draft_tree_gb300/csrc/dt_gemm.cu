@@ -123,19 +123,39 @@ gemm_nt_kernel(int M, int N, int K, const void *__restrict__ A, size_t lda,
   }
 }
 
-// C = sum_z partial[z] (+ bias), four outputs per thread, chunks in order.
-__global__ void splitk_reduce_kernel(const float *__restrict__ partial, int ksplit, int M, int N,
+// C = sum_z partial[z] (+ bias). Four lanes per four outputs (a float4):
+// lane q sums the planes q, q + 4, q + 8, ... (its loads in flight together),
+// then the four sums are combined by two exchanges, (s0 + s1) + (s2 + s3): a
+// fixed order, so the result is deterministic. Blocks of 128 threads with at
+// most 32 registers each (4 K registers) fit beside three top-M blocks on an
+// SM, so the reduction of the projection does not wait for the top-M.
+constexpr int kReduceThreads = 128;
+
+__global__ void __launch_bounds__(kReduceThreads, 16) splitk_reduce_kernel(const float *__restrict__ partial, int ksplit, int M, int N,
                                      const float *__restrict__ bias, float *__restrict__ C,
                                      size_t ldc) {
   const size_t plane = static_cast<size_t>(M) * N;
-  const size_t i4 = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
-  if (i4 >= plane) return;
-  const int m = static_cast<int>(i4 / N), n = static_cast<int>(i4 % N);
+  const size_t gid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t i4 = (gid >> 2) * 4;
+  const int q = static_cast<int>(gid & 3);
+  const bool valid = i4 < plane;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int z = 0; z < ksplit; ++z) {
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(partial + z * plane + i4));
-    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+  if (valid) {
+#pragma unroll 8
+    for (int z = q; z < ksplit; z += 4) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(partial + z * plane + i4));
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
   }
+#pragma unroll
+  for (int m = 1; m <= 2; m <<= 1) {
+    s.x += __shfl_xor_sync(0xffffffffu, s.x, m);
+    s.y += __shfl_xor_sync(0xffffffffu, s.y, m);
+    s.z += __shfl_xor_sync(0xffffffffu, s.z, m);
+    s.w += __shfl_xor_sync(0xffffffffu, s.w, m);
+  }
+  if (!valid || q != 0) return;
+  const int m = static_cast<int>(i4 / N), n = static_cast<int>(i4 % N);
   if (bias) { s.x += bias[n]; s.y += bias[n + 1]; s.z += bias[n + 2]; s.w += bias[n + 3]; }
   float *c = C + static_cast<size_t>(m) * ldc + n;
   c[0] = s.x; c[1] = s.y; c[2] = s.z; c[3] = s.w;
@@ -160,14 +180,18 @@ cudaError_t launch_gemm_nt(int M, int N, int K, const void *A, int a_dtype, size
   else
     gemm_nt_kernel<1, 1><<<grid, kThreads, 0, st>>>(DT_GEMM_ARGS);
 #undef DT_GEMM_ARGS
-  if (ksplit > 1) {
-    const size_t n4 = (static_cast<size_t>(M) * N + 3) / 4;
-    splitk_reduce_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(
-        partial, ksplit, M, N, bias, C, ldc);
-  }
+  if (ksplit > 1) return launch_splitk_reduce(partial, ksplit, M, N, bias, C, ldc, st);
   return cudaGetLastError();
 }
 
 int gemm_tiles(int M, int N) { return ((N + BN - 1) / BN) * ((M + BM - 1) / BM); }
+
+cudaError_t launch_splitk_reduce(const float *partial, int ksplit, int M, int N, const float *bias,
+                                 float *C, size_t ldc, cudaStream_t st) {
+  const size_t threads = (static_cast<size_t>(M) * N + 3) / 4 * 4;   // four lanes per float4
+  splitk_reduce_kernel<<<static_cast<unsigned>((threads + kReduceThreads - 1) / kReduceThreads),
+                         kReduceThreads, 0, st>>>(partial, ksplit, M, N, bias, C, ldc);
+  return cudaGetLastError();
+}
 
 }  // namespace dt

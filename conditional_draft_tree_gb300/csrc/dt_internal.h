@@ -19,6 +19,7 @@ struct Plan {
   int nsplit;          // top-M row segments (pieces per row at most, with topm_blocks)
   int topm_blocks;     // > 0: top-M over contiguous unit ranges, this many blocks
   int proj_ksplit;     // K split of the projection GEMM
+  int proj_umma;       // the projection on the tensor cores (dt_proj.cu)
   int umma;            // search GEMM on tcgen05 (bf16 weights)
   int n_mt, ks, kc;    // its 128-row tiles, K chunks and K chunk width
   int nbufs;           // its B slice buffers in flight (2..4)
@@ -81,6 +82,18 @@ cudaError_t launch_gemm_nt(int M, int N, int K, const void *A, int a_dtype, size
                            const void *B, int b_dtype, size_t ldb, const float *bias, float *C,
                            size_t ldc, int ksplit, float *partial, cudaStream_t st);
 int gemm_tiles(int M, int N);
+// C = sum of the ksplit planes [ksplit][M][N] (in order) + bias; N % 4 == 0
+cudaError_t launch_splitk_reduce(const float *partial, int ksplit, int M, int N, const float *bias,
+                                 float *C, size_t ldc, cudaStream_t st);
+
+// U = H W1[:, :K]^T on the tensor cores (bf16 W1; dt_proj.cu): rows x r
+// outputs, K split in split_k chunks (partials [split_k][rows][r] plus the
+// reduction when split_k > 1); *fail = 1 when a bounded wait runs out.
+bool proj_umma_supported(const dt_dims &d, int wdtype);
+int proj_umma_split(int rows, int r, int K, int target_blocks);
+cudaError_t launch_proj_umma(int rows, int r, int K, const float *H, int ldh, const void *W1,
+                             int ldw, float *U, int split_k, float *partial, int *fail,
+                             cudaStream_t st);
 
 // The best-first search for requests [b0, b0 + nb).
 struct ChainArgs {
@@ -102,6 +115,7 @@ struct DecodePlan {
   int R, n_tA, nchA, n_kz, n_tV, nchV, kb;
   size_t smem;
   int proj_ksplit;
+  int proj_umma;        // the projection on the tensor cores (dt_proj.cu)
   size_t off_ctrl, off_U, off_upart, off_ypart, off_S, off_stm, off_sts, off_sta,
       off_flags, off_end;
 };

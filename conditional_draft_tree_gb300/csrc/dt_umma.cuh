@@ -12,6 +12,8 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
+
 namespace dt {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -22,6 +24,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 __device__ __forceinline__ uint32_t umma_offset(int row, int k, int Kc) {
   return static_cast<uint32_t>((row >> 3) * (16 * Kc) + (k >> 3) * 128 + (row & 7) * 16 +
                                (k & 7) * 2);
+}
+
+// fp32 -> three bf16 terms whose sum is the value (hi, mid, lo): with exact
+// bf16 weights on the other side, the three products keep fp32 accuracy
+__device__ __forceinline__ void split3(float v, uint16_t &a, uint16_t &b, uint16_t &c) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  a = __bfloat16_as_ushort(hi);
+  b = __bfloat16_as_ushort(mid);
+  c = __bfloat16_as_ushort(lo);
 }
 
 // shared-memory matrix descriptor: start address, LBO, SBO (bytes), no swizzle
@@ -153,6 +167,11 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, uin
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// wait until at most N of this thread's commit groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");

@@ -135,7 +135,10 @@ typedef struct {
 #define DT_OPT_STAGE_HOST_LOGITS 16
 
 
-#define DT_NUM_PHASE_EVENTS 4 /* start, after top-M, after the projection, after the search */
+/* phase events: [0] start, [1] after the top-M, [2] after the projection
+ * (which runs beside the top-M on a second stream: [2] marks the later of the
+ * two), [3] after the search */
+#define DT_NUM_PHASE_EVENTS 4
 
 /* Bytes of the prepared-weights buffer for `dims`: the GRU input projection of
  * every vocabulary row, G[v] = W_ih E[v] + b_ih, as fp32 [V][3 d_s]. */

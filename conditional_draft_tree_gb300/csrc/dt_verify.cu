@@ -11,16 +11,20 @@
 // the anchor is tree row 0 at position prefix_len and a node at depth j sits at
 // prefix_len + j (empty rows: -1).
 //
-// Attention on the tensor cores (tcgen05): one block of four warps per
+// Attention on the tensor cores (tcgen05): one block of eight warps per
 // (request, key/value head, tile of 128 query rows), where the rows of the
 // H / Hkv query heads that share the key/value head are stacked (head-major),
 // so K and V are staged once for all of them; TMEM lane t is query row t of
-// the tile, and thread t owns it. Keys are taken in chunks of 64: the visible
+// the tile, and threads t and t + 128 own it, each for half of every chunk's
+// keys (and half of the output columns): two threads per row double the
+// resident warps at the same shared memory, the bound of this latency-bound
+// kernel. Keys are taken in chunks of 64: the visible
 // prefix [0, prefix_len) and the tree rows (prefix keys past prefix_len are
 // never read). Two passes over the chunks:
 //   1. S = Q K^T (bf16 operands, exact products, fp32 accumulation in TMEM),
 //      then the thread's running row maximum m and sum l of exp(x - m) over
-//      its visible keys (x = scale S);
+//      its visible keys (x = scale S); the two halves of a row are combined
+//      once at the end;
 //   2. S again, e = exp(x - m) (0 where not visible) as two bf16 terms hi + lo
 //      (16 significant bits), O += e_hi V + e_lo V in TMEM;
 // and out = O / l (0 for a row that sees no key). Operands are staged in
@@ -40,7 +44,8 @@ namespace dt {
 
 namespace {
 
-constexpr int kAThreads = 128;         // one thread per query row of a tile
+constexpr int kAThreads = 256;         // two threads per query row of a tile
+constexpr int kHalf = 32;               // keys of a chunk per thread
 constexpr int kKeys = 64;               // keys per chunk (the S tile's N)
 constexpr uint64_t kAttnLimitNs = 2000000000ull;
 
@@ -71,11 +76,13 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
   __shared__ __align__(8) uint64_t s_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
+  __shared__ float s_ml[2][128];         // the key-half-1 threads' (m, l) per row
   unsigned char *sQ = sm;                              // [128 rows][DH], K-major
   unsigned char *sK = sQ + 128 * DH * 2;               // [kKeys rows][DH]
   unsigned char *sV = sK + kKeys * DH * 2;             // [DH rows][kKeys] (V^T)
   unsigned char *sE = sV + DH * kKeys * 2;             // 2 x [128 rows][kKeys]
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int row = tid & 127, half = tid >> 7;   // TMEM lane; keys [32 half, 32 half + 32)
   const int mt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int G = a.H / a.Hkv, rows = G * a.n1;
   const int L = a.P + a.n1;
@@ -84,7 +91,7 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
   const uint16_t *vb = a.v + (static_cast<size_t>(b) * a.Hkv + hk) * L * DH;
   const uint8_t *mb = a.mask + static_cast<size_t>(b) * a.n1 * a.n1;
   // this thread's query row
-  const int g = mt * 128 + tid;
+  const int g = mt * 128 + row;
   const bool mine = g < rows;
   const int h = hk * G + (mine ? g / a.n1 : 0), qr = mine ? g % a.n1 : 0;
   const float ninf = -__int_as_float(0x7f800000);
@@ -111,7 +118,7 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
   tmem_fence_after();
   const uint32_t tmem = s_tmem;
   const uint32_t t_o = tmem, t_s = tmem + DH;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;   // lanes of row
   const uint32_t idesc_s = umma_idesc_bf16(128, kKeys), idesc_o = umma_idesc_bf16(128, DH);
   // chunks: the visible prefix, then the tree rows
   const int npre = (plen + kKeys - 1) / kKeys, ntree = (a.n1 + kKeys - 1) / kKeys;
@@ -124,10 +131,11 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
     return j < a.P ? j < plen : mb[static_cast<size_t>(qr) * a.n1 + (j - a.P)] != 0;
   };
   // key chunk c in registers: unit i of this thread is key 32 (warp & 1) + lane
-  // of the chunk, 16-byte piece c8 = (warp >> 1) + 2 i (a warp covers 32
+  // of the chunk, 16-byte piece c8 = (warp >> 1) + NWP i (a warp covers 32
   // consecutive keys, so the transposed V stores of a warp spread over banks);
   // rows past the chunk's end are zeros
-  constexpr int UPT = kKeys * C8 / kAThreads;   // pieces per thread: 8 (DH 128)
+  constexpr int UPT = kKeys * C8 / kAThreads;   // pieces per thread: 4 (DH 128)
+  constexpr int NWP = kAThreads / 64;           // warp pairs
   static_assert(kKeys == 64 && UPT * kAThreads == kKeys * C8, "piece mapping");
   uint4 pk[UPT], pv[UPT];
   const int my_key = 32 * (warp & 1) + (tid & 31);
@@ -136,7 +144,7 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
     const bool in = j < chunk_end(c);
 #pragma unroll
     for (int i = 0; i < UPT; ++i) {
-      const int c8 = (warp >> 1) + 2 * i;
+      const int c8 = (warp >> 1) + NWP * i;
       pk[i] = in ? *reinterpret_cast<const uint4 *>(kb + static_cast<size_t>(j) * DH + c8 * 8)
                  : make_uint4(0u, 0u, 0u, 0u);
       pv[i] = (in && with_v)
@@ -148,7 +156,7 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
   auto stage = [&](bool with_v) {
 #pragma unroll
     for (int i = 0; i < UPT; ++i) {
-      const int c8 = (warp >> 1) + 2 * i;
+      const int c8 = (warp >> 1) + NWP * i;
       *reinterpret_cast<uint4 *>(sK + umma_offset(my_key, c8 * 8, DH)) = pk[i];
       if (with_v) {
         const uint32_t w[4] = {pv[i].x, pv[i].y, pv[i].z, pv[i].w};
@@ -177,14 +185,13 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
       umma_commit(&s_bar);
     }
   };
-  // this thread's row of S for chunk c, scaled, -inf where not visible
-  auto row_scores = [&](int c, float (&x)[kKeys]) {
-    tmem_ld32(t_s + lane_off, x);
-    tmem_ld32(t_s + lane_off + 32, x + 32);
+  // this thread's half of its row of S for chunk c, scaled, -inf where not visible
+  auto row_scores = [&](int c, float (&x)[kHalf]) {
+    tmem_ld32(t_s + lane_off + kHalf * half, x);
     tmem_wait_ld();
-    const int j0 = chunk_first(c), j1 = chunk_end(c);
+    const int j0 = chunk_first(c) + kHalf * half, j1 = chunk_end(c);
 #pragma unroll
-    for (int t = 0; t < kKeys; ++t) {
+    for (int t = 0; t < kHalf; ++t) {
       const int j = j0 + t;
       x[t] = (mine && j < j1 && visible(j)) ? x[t] * a.scale : ninf;
     }
@@ -200,22 +207,41 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
     issue_s();
     if (c + 1 < nch) fetch(c + 1, false);
     mma_wait();
-    float x[kKeys];
+    float x[kHalf];
     row_scores(c, x);
     float mc = ninf;
 #pragma unroll
-    for (int t = 0; t < kKeys; ++t) mc = fmaxf(mc, x[t]);
+    for (int t = 0; t < kHalf; ++t) mc = fmaxf(mc, x[t]);
     if (mc != ninf) {
       const float mn = fmaxf(m, mc);
       float sum = 0.0f;
 #pragma unroll
-      for (int t = 0; t < kKeys; ++t) sum += (x[t] == ninf) ? 0.0f : expf(x[t] - mn);
+      for (int t = 0; t < kHalf; ++t) sum += (x[t] == ninf) ? 0.0f : expf(x[t] - mn);
       l = l * expf(m - mn) + sum;   // (exp(-inf) = 0 while nothing was seen)
       m = mn;
     }
     tmem_fence_before();
     __syncthreads();   // S read and sK free before the next chunk
   }
+  // the row's two halves: m = max(m0, m1), l = l0 exp(m0 - m) + l1 exp(m1 - m)
+  if (half == 1) {
+    s_ml[0][row] = m;
+    s_ml[1][row] = l;
+  }
+  __syncthreads();
+  if (half == 0) {
+    const float m1 = s_ml[0][row], l1 = s_ml[1][row];
+    const float mm = fmaxf(m, m1);
+    if (mm != ninf) {
+      l = (m == ninf ? 0.0f : l * expf(m - mm)) + (m1 == ninf ? 0.0f : l1 * expf(m1 - mm));
+      m = mm;
+    }
+    s_ml[0][row] = m;
+    s_ml[1][row] = l;
+  }
+  __syncthreads();
+  m = s_ml[0][row];
+  l = s_ml[1][row];
   // pass 2: O = sum of e V, e = exp(x - m) in two bf16 terms
   if (!s_fail) fetch(0, true);
   for (int c = 0; c < nch && !s_fail; ++c) {
@@ -225,10 +251,10 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
     issue_s();
     if (c + 1 < nch) fetch(c + 1, true);
     mma_wait();
-    float x[kKeys];
+    float x[kHalf];
     row_scores(c, x);
 #pragma unroll
-    for (int t0 = 0; t0 < kKeys; t0 += 8) {
+    for (int t0 = 0; t0 < kHalf; t0 += 8) {
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
@@ -243,9 +269,9 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
         lo[e >> 1] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
                      (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
       }
-      *reinterpret_cast<uint4 *>(sE + umma_offset(tid, t0, kKeys)) =
+      *reinterpret_cast<uint4 *>(sE + umma_offset(row, kHalf * half + t0, kKeys)) =
           make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4 *>(sE + 128 * kKeys * 2 + umma_offset(tid, t0, kKeys)) =
+      *reinterpret_cast<uint4 *>(sE + 128 * kKeys * 2 + umma_offset(row, kHalf * half + t0, kKeys)) =
           make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     fence_async_smem();
@@ -272,7 +298,7 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
     float *ob = a.out + ((static_cast<size_t>(b) * a.H + h) * a.n1 + qr) * DH;
 #pragma unroll 1
-    for (int c0 = 0; c0 < DH; c0 += 32) {
+    for (int c0 = (DH / 2) * half; c0 < (DH / 2) * (half + 1); c0 += 32) {
       float o[32];
       tmem_ld32(t_o + lane_off + c0, o);
       tmem_wait_ld();

@@ -20,14 +20,13 @@
 // resident warps at the same shared memory, the bound of this latency-bound
 // kernel. Keys are taken in chunks of 64: the visible
 // prefix [0, prefix_len) and the tree rows (prefix keys past prefix_len are
-// never read). Two passes over the chunks:
-//   1. S = Q K^T (bf16 operands, exact products, fp32 accumulation in TMEM),
-//      then the thread's running row maximum m and sum l of exp(x - m) over
-//      its visible keys (x = scale S); the two halves of a row are combined
-//      once at the end;
-//   2. S again, e = exp(x - m) (0 where not visible) as two bf16 terms hi + lo
-//      (16 significant bits), O += e_hi V + e_lo V in TMEM;
-// and out = O / l (0 for a row that sees no key). Operands are staged in
+// never read). One pass over the chunks with an online softmax: S = Q K^T
+// (bf16 operands, exact products, fp32 accumulation in TMEM); the row's
+// reference maximum m follows the running maximum of x = scale S, moved only
+// when the chunk maximum exceeds it by more than 8 (then O in TMEM and l are
+// rescaled); e = exp(x - m) (0 where not visible) as two bf16 terms hi + lo
+// (16 significant bits), O += e_hi V + e_lo V in TMEM, l += e; and out = O / l
+// (0 for a row that sees no key). Operands are staged in
 // shared memory in the K-major no-swizzle layout of dt_umma.cuh: Q and the
 // key chunk as they are stored, V transposed (head dimension as rows). One
 // thread issues the MMAs; completion is an mbarrier commit, every wait bounded.
@@ -197,62 +196,54 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
     }
   };
 
-  // pass 1: row maximum and sum (the next chunk's keys load during the MMAs)
-  float m = ninf, l = 0.0f;
-  fetch(0, false);
+  // One pass, online softmax. Per chunk: S = Q K_c^T; the row's chunk maximum
+  // (the two half-row threads exchange theirs); when it exceeds the row's
+  // reference maximum m by more than kRescale, O and l are rescaled to the new
+  // maximum (O in TMEM by tcgen05.ld / st, after the previous chunk's O
+  // product has completed), otherwise m stays and e stays below exp(kRescale);
+  // e = exp(x - m) as two bf16 terms (hi + lo), O += e V_c. The first chunk's
+  // product initialises O, so no row is ever rescaled from unwritten TMEM.
+  constexpr float kRescale = 8.0f;
+  float m = ninf, l = 0.0f;   // row reference maximum; this thread's half of l
+  fetch(0, true);
   for (int c = 0; c < nch && !s_fail; ++c) {
-    stage(false);
+    stage(true);   // sK, sV free: S and O of chunk c - 1 were waited for
     tmem_fence_before();
     __syncthreads();
     issue_s();
-    if (c + 1 < nch) fetch(c + 1, false);
-    mma_wait();
+    if (c + 1 < nch) fetch(c + 1, true);
+    mma_wait();    // S of chunk c (and O of chunk c - 1 before it)
     float x[kHalf];
     row_scores(c, x);
     float mc = ninf;
 #pragma unroll
     for (int t = 0; t < kHalf; ++t) mc = fmaxf(mc, x[t]);
-    if (mc != ninf) {
-      const float mn = fmaxf(m, mc);
-      float sum = 0.0f;
-#pragma unroll
-      for (int t = 0; t < kHalf; ++t) sum += (x[t] == ninf) ? 0.0f : expf(x[t] - mn);
-      l = l * expf(m - mn) + sum;   // (exp(-inf) = 0 while nothing was seen)
-      m = mn;
-    }
-    tmem_fence_before();
-    __syncthreads();   // S read and sK free before the next chunk
-  }
-  // the row's two halves: m = max(m0, m1), l = l0 exp(m0 - m) + l1 exp(m1 - m)
-  if (half == 1) {
-    s_ml[0][row] = m;
-    s_ml[1][row] = l;
-  }
-  __syncthreads();
-  if (half == 0) {
-    const float m1 = s_ml[0][row], l1 = s_ml[1][row];
-    const float mm = fmaxf(m, m1);
-    if (mm != ninf) {
-      l = (m == ninf ? 0.0f : l * expf(m - mm)) + (m1 == ninf ? 0.0f : l1 * expf(m1 - mm));
-      m = mm;
-    }
-    s_ml[0][row] = m;
-    s_ml[1][row] = l;
-  }
-  __syncthreads();
-  m = s_ml[0][row];
-  l = s_ml[1][row];
-  // pass 2: O = sum of e V, e = exp(x - m) in two bf16 terms
-  if (!s_fail) fetch(0, true);
-  for (int c = 0; c < nch && !s_fail; ++c) {
-    stage(true);
-    tmem_fence_before();
+    s_ml[half][row] = mc;
     __syncthreads();
-    issue_s();
-    if (c + 1 < nch) fetch(c + 1, true);
-    mma_wait();
-    float x[kHalf];
-    row_scores(c, x);
+    mc = fmaxf(mc, s_ml[half ^ 1][row]);
+    // both threads of a row take the same decision from the same values
+    const bool grow = mc > m + kRescale || (m == ninf && mc != ninf);
+    float f = 1.0f;
+    if (grow) {
+      f = (m == ninf) ? 0.0f : expf(m - mc);
+      l *= f;
+      m = mc;
+    }
+    // O follows (chunk 0's product has not written it yet); tcgen05.ld / st
+    // are warp-wide, so a warp with one growing row rescales all its rows,
+    // the others by 1
+    if (c > 0 && __any_sync(kFull, grow)) {
+#pragma unroll 1
+      for (int c0 = (DH / 2) * half; c0 < (DH / 2) * (half + 1); c0 += 32) {
+        float o[32];
+        tmem_ld32(t_o + lane_off + c0, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] *= f;
+        tmem_st32(t_o + lane_off + c0, o);
+      }
+      tmem_wait_st();
+    }
 #pragma unroll
     for (int t0 = 0; t0 < kHalf; t0 += 8) {
       uint32_t hi[4], lo[4];
@@ -260,7 +251,10 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
       for (int e = 0; e < 8; e += 2) {
         float ev[2];
 #pragma unroll
-        for (int z = 0; z < 2; ++z) ev[z] = (x[t0 + e + z] == ninf) ? 0.0f : expf(x[t0 + e + z] - m);
+        for (int z = 0; z < 2; ++z) {
+          ev[z] = (x[t0 + e + z] == ninf) ? 0.0f : expf(x[t0 + e + z] - m);
+          l += ev[z];
+        }
         const __nv_bfloat16 h0 = __float2bfloat16_rn(ev[0]), h1 = __float2bfloat16_rn(ev[1]);
         const __nv_bfloat16 l0 = __float2bfloat16_rn(ev[0] - __bfloat162float(h0));
         const __nv_bfloat16 l1 = __float2bfloat16_rn(ev[1] - __bfloat162float(h1));
@@ -276,7 +270,7 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
     }
     fence_async_smem();
     tmem_fence_before();
-    __syncthreads();
+    __syncthreads();   // e in sE, O rescaled, S read: O += e V
     if (tid == 0) {
       tmem_fence_after();
 #pragma unroll
@@ -289,10 +283,12 @@ __global__ void __launch_bounds__(kAThreads) tree_attention_kernel(TreeAttnArgs 
                     c > 0 || term > 0 || k > 0);
       umma_commit(&s_bar);
     }
-    mma_wait();
-    tmem_fence_before();
-    __syncthreads();   // sK, sV, sE and S free before the next chunk
+    mma_wait();    // O of chunk c: sE, sV, sK free
   }
+  // the row's l: the sum of its two halves (both taken against the same m)
+  s_ml[half][row] = l;
+  __syncthreads();
+  l += s_ml[half ^ 1][row];
   // out = O / l
   if (!s_fail && nch > 0) {
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;

@@ -3,9 +3,13 @@ oracle (needs a GB300).
 
 Positions are integers: bit-exact. Attention: bf16 inputs are exact in both,
 the GPU accumulates in fp32 (head dimension up to 256 products, softmax sums
-over at most P + n1 keys in chunks of 32) and the oracle in fp64; the outputs
+over at most P + n1 keys in chunks of 64) and the oracle in fp64; the outputs
 are convex combinations of N(0, 1) values, so an absolute 2e-4 (with 2e-4
-relative) leaves about an order of magnitude above the fp32 error.
+relative) leaves about an order of magnitude above the fp32 error. The kernel
+keeps a per-row reference maximum that moves only when a chunk's maximum
+exceeds it by more than 8 (then the accumulated output is rescaled);
+`test_rescaled_accumulator` drives that path with keys whose norms grow or
+shrink from chunk to chunk.
 """
 from __future__ import annotations
 
@@ -116,3 +120,28 @@ def test_qwen3_8b_verification_shape_sampled():
     assert np.isfinite(got).all()
     check(q, k, v, out["mask"].cpu().numpy(), plen, got,
           pairs=[(b, h) for b in (0, 5, 31) for h in range(32)])
+
+
+@pytest.mark.parametrize("profile", ["rising", "falling", "alternating"])
+def test_rescaled_accumulator(profile):
+    """Key norms set per 64-key chunk so that the scores' maximum jumps by about
+    10 from one chunk to the next (rising: every chunk moves the reference
+    maximum and rescales the accumulated output; falling: none does after the
+    first; alternating: every other one), prefix of 256 keys fully visible plus
+    the tree rows under a GPU-built mask; against the fp64 oracle."""
+    out = gpu_trees(64, 2, 131)
+    n1, P, dh, H, Hkv = 65, 256, 128, 4, 2
+    q, _, v, _ = W.verify_inputs(2, H, Hkv, n1, P, dh, seed=132)
+    plen = np.full(2, P, np.int32)
+    rng = np.random.default_rng(133)
+    L = P + n1
+    chunk = np.arange(L) // 64
+    nch = int(chunk.max()) + 1
+    order = {"rising": np.arange(nch), "falling": np.arange(nch)[::-1],
+             "alternating": np.where(np.arange(nch) % 2 == 0, np.arange(nch), 0)}[profile]
+    gain = (4.0 + 4.0 * order[chunk]).astype(np.float32)   # scores ~ N(0, gain^2)
+    k = W.f32_to_bf16_bits(rng.standard_normal((2, Hkv, L, dh), dtype=np.float32)
+                           * gain[None, None, :, None])
+    got = run_attention(q, k, v, out["mask"], plen)
+    assert np.isfinite(got).all()
+    check(q, k, v, out["mask"].cpu().numpy(), plen, got)

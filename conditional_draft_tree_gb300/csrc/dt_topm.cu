@@ -5,12 +5,11 @@
 // (request b, depth j) this kernel returns the M token ids with the largest
 // base logit, ordered by (logit desc, id asc).
 //
-// The rows are 151936 fp32 wide and read once: the kernel is HBM bound. Each
-// row is cut into segments, one block each, filtered by the block-level
-// selection of dt_topm_block.cuh; the last block of a row (atomic ticket, no
-// waiting) merges the segment lists and writes the row's result. The search
-// of dt_build_trees runs the same selection inside its own kernel; this one
-// serves the marginal-score mode and dt_select_topm_noalloc.
+// The rows are 151936 fp32 wide and read once. Each row is cut into pieces,
+// one block each, filtered by the block-level selection of dt_topm_block.cuh;
+// the last block of a row (atomic ticket, no waiting) merges the piece lists
+// and writes the row's result. It serves dt_build_trees (before the search),
+// the marginal-score mode and dt_select_topm_noalloc.
 #include <cstdint>
 
 #include "dt_common.cuh"

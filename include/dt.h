@@ -176,9 +176,12 @@ int dt_kernel_launches(const dt_dims *dims, int wdtype, const dt_options *opt);
  *               overlapping calls
  * Float inputs must be 16-byte aligned when their row length is a multiple of 4
  * floats. Returns DT_OK when the work was enqueued. Part of the work (the
- * projection) runs on a library-owned stream of the current device, forked from
- * and joined back into `stream` with events, so every result is ordered on
- * `stream` as usual. (The fork and join are events, as stream capture into a
+ * projection U = W1[:, :d] H: on the tensor cores for bf16 weights when d is a
+ * multiple of 32, r of 4 and d + d_s of 8, else on the CUDA cores) runs on a
+ * library-owned stream of the current device, forked from and joined back into
+ * `stream` with events, so every result is ordered on `stream` as usual. A
+ * bounded wait of the tensor-core projection that runs out makes every request
+ * of the call report DT_ERR_TIMEOUT. (The fork and join are events, as stream capture into a
  * CUDA graph requires; capture is not covered by a test yet.) */
 int dt_build_trees(const dt_dims *dims, const dt_weights *w, const void *prepared,
                    const float *base_logits, const float *H, const float *state0,

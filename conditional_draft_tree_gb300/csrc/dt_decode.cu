@@ -52,6 +52,10 @@ constexpr int kWork = 256;                          // threads of warps 0-7
 constexpr int kProd = 256, kMma = 288;              // issuing threads
 constexpr int kChunkK = 64;                         // K columns per A chunk
 constexpr uint32_t kChunkBytes = 128 * kChunkK * 2; // 16 KB
+// vocabulary epilogue: per work warp, x of 8 requests x 32 tokens (rows padded
+// to 33 floats, so the transposed reads hit 32 different banks)
+constexpr int kRedRow = 33;
+constexpr int kRedBytes = (kWork / 32) * 8 * kRedRow * 4;
 constexpr int kStages = 4;
 constexpr int kRangeK = 256;                        // K columns of one state-GEMM item
 constexpr int kMaxBpad = 80;                        // 3 terms x 80 = 240 accumulator columns
@@ -242,7 +246,8 @@ __device__ bool state_gemm(const DecodeParams &p, unsigned char *ring, unsigned 
 
 __device__ bool vocab_gemm(const DecodeParams &p, int i, unsigned char *ring, unsigned char *sB,
                            uint64_t *full, uint64_t *empty, uint64_t *accf, uint64_t *acce,
-                           uint32_t tmem, Pipe &pp, int *s_fail, const float *s_T) {
+                           uint32_t tmem, Pipe &pp, int *s_fail, const float *s_T,
+                           float *s_red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rp8 = p.nchV * (kChunkK / 8);
   // B: h = SiLU(U_i + W1_S S) in three terms, K padded with zeros to 64 nchV
@@ -291,9 +296,13 @@ __device__ bool vocab_gemm(const DecodeParams &p, int i, unsigned char *ring, un
   __syncthreads();
   bool ok = true;
   const float ninf = -__int_as_float(0x7f800000);
-  // Each work warp owns 32 tokens of a tile (its TMEM lane quarter) and half
-  // of the requests. The base logits of a tile's requests are loaded together,
-  // one tile ahead, so that their HBM latency overlaps the previous tile.
+  // Each work warp owns 32 tokens of a tile (its TMEM lane quarter, one 32-token
+  // group) and half of the requests. The base logits of a tile's requests are
+  // loaded together, one tile ahead, so that their HBM latency overlaps the
+  // previous tile. The group records are reduced transposed: the warp writes x
+  // of 8 requests x 32 tokens to shared memory, then four lanes per request
+  // scan 8 tokens each (maximum, sum of exp, first argmax) and combine by two
+  // exchanges, instead of two 32-lane reductions per request.
   constexpr int kHalf = kMaxBpad / 2;
   const int quarter = warp & 3, half = warp >> 2, hb = p.bpad >> 1;
   const int my0 = half * hb;
@@ -322,6 +331,8 @@ __device__ bool vocab_gemm(const DecodeParams &p, int i, unsigned char *ring, un
       const int grp = t * 4 + quarter;
       const bool valid = v < p.V;
       const uint32_t ta = tmem + ((quarter * 32u) << 16) + (pp.q & 1u) * kAccCols;
+      float *xr = s_red + warp * (8 * kRedRow);
+      const int vg = t * 128 + quarter * 32;   // first token of the group
 #pragma unroll
       for (int c = 0; c < kHalf; c += 8) {
         if (c >= myn) break;
@@ -332,25 +343,44 @@ __device__ bool vocab_gemm(const DecodeParams &p, int i, unsigned char *ring, un
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (c + j >= myn) break;
-          const int b = my0 + c + j;
           float x = ninf;
-          if (valid) {
+          if (c + j < myn && valid) {
+            const int b = my0 + c + j;
             const float bv = cur[c + j];
             if (bv != bv || bv == __int_as_float(0x7f800000)) atomicOr(&p.flags[b], 1);
             x = __fdiv_rn(bv + ((a[j] + m[j]) + l[j]), s_T[b]);
           }
-          const float mx = warp_max(x);
-          const float e = (x == ninf) ? 0.0f : expf(x - mx);
-          const float sum = warp_sum(e);
-          const unsigned ball = __ballot_sync(kFull, valid && x == mx);
-          if (lane == 0) {
-            const size_t o = static_cast<size_t>(b) * p.Gn + grp;
-            p.st_m[o] = mx;
-            p.st_s[o] = sum;
-            p.st_a[o] = ball ? grp * 32 + __ffs(ball) - 1 : -1;
-          }
+          xr[j * kRedRow + lane] = x;
         }
+        __syncwarp();
+        // request c + jr: lanes 4 jr .. 4 jr + 3, tokens t0 .. t0 + 7 each
+        const int jr = lane >> 2, t0 = (lane & 3) * 8;
+        float xv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) xv[u] = xr[jr * kRedRow + t0 + u];
+        float mx = xv[0];
+#pragma unroll
+        for (int u = 1; u < 8; ++u) mx = fmaxf(mx, xv[u]);
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+        float sum = 0.0f;
+        int first = 32;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          sum += (xv[u] == ninf) ? 0.0f : expf(xv[u] - mx);
+          if (first == 32 && vg + t0 + u < p.V && xv[u] == mx) first = t0 + u;
+        }
+        sum += __shfl_xor_sync(kFull, sum, 1);
+        sum += __shfl_xor_sync(kFull, sum, 2);
+        first = min(first, __shfl_xor_sync(kFull, first, 1));
+        first = min(first, __shfl_xor_sync(kFull, first, 2));
+        if ((lane & 3) == 0 && c + jr < myn) {
+          const size_t o = static_cast<size_t>(my0 + c + jr) * p.Gn + grp;
+          p.st_m[o] = mx;
+          p.st_s[o] = sum;
+          p.st_a[o] = first < 32 ? grp * 32 + first : -1;
+        }
+        __syncwarp();   // the rows are written again for the next 8 requests
       }
       release_acc(acce, pp);
     }
@@ -614,6 +644,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_kernel(DecodeParams p) {
   uint64_t *full = bars, *empty = bars + kStages, *accf = bars + 2 * kStages, *acce = accf + 2;
   unsigned char *ring = smem;
   unsigned char *sB = smem + kStages * kChunkBytes;
+  float *s_red = reinterpret_cast<float *>(sB + static_cast<size_t>(6) * p.bpad * p.kb);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -685,7 +716,7 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_kernel(DecodeParams p) {
     lap(0);
     ok = barrier(!g || s_fail);
     if (!ok) break;
-    g = vocab_gemm(p, i, ring, sB, full, empty, accf, acce, tmem, pp, &s_fail, s_T);
+    g = vocab_gemm(p, i, ring, sB, full, empty, accf, acce, tmem, pp, &s_fail, s_T, s_red);
     lap(1);
     ok = barrier(!g || s_fail);
     if (!ok) break;
@@ -774,12 +805,13 @@ int decode_plan(const dt_dims &d, int num_sms, int smem_optin, DecodePlan *p) {
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, decode_kernel) != cudaSuccess) return DT_ERR_CUDA;
   const long avail = static_cast<long>(smem_optin) - static_cast<long>(fa.sharedSizeBytes) -
-                     static_cast<long>(kStages) * kChunkBytes;
+                     static_cast<long>(kStages) * kChunkBytes - kRedBytes;
   int bpad = static_cast<int>(avail / (6L * p->kb)) / 16 * 16;
   if (bpad > kMaxBpad) bpad = kMaxBpad;
   if (bpad < 16) return DT_ERR_UNSUPPORTED;
   p->wave = bpad;
-  p->smem = static_cast<size_t>(kStages) * kChunkBytes + static_cast<size_t>(6) * bpad * p->kb;
+  p->smem = static_cast<size_t>(kStages) * kChunkBytes + static_cast<size_t>(6) * bpad * p->kb +
+            kRedBytes;
   if (cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(p->smem)) != cudaSuccess)
     return DT_ERR_CUDA;

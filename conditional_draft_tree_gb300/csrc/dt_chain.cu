@@ -744,6 +744,34 @@ __device__ __forceinline__ void write_column4(const ChainParams &p, int slot, in
 
 // ------------------------------------------------------------ request phase
 
+// The warp sums of G values at once (G a power of two, at most 32): at each
+// halving exchange a lane keeps the half of its values selected by one lane
+// bit and adds its partner's copy of that half, so after log2(G) exchanges a
+// lane holds one value summed over 2^log2(G) lanes, then a plain butterfly
+// finishes it; G - 1 + 5 - log2(G) shuffles instead of 5 G. Returns to lane q
+// (q < G) the warp sum of a[q] (a fixed order of additions, deterministic).
+template <int G>
+__device__ __forceinline__ float warp_sum_many(float (&a)[G], int lane) {
+  static_assert(G >= 1 && G <= 32 && (G & (G - 1)) == 0, "power of two");
+  int lg = 0;
+#pragma unroll
+  for (int n = G; n > 1; n >>= 1) ++lg;
+#pragma unroll
+  for (int n = G, o = 16; n > 1; n >>= 1, o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? a[i] : a[i + n / 2];
+      const float keep = upper ? a[i + n / 2] : a[i];
+      a[i] = keep + __shfl_xor_sync(kFull, send, o);
+    }
+  }
+#pragma unroll
+  for (int o = 16 >> lg; o >= 1; o >>= 1) a[0] += __shfl_xor_sync(kFull, a[0], o);
+  // value q sits at the lanes whose bits 4 .. 5 - lg spell q
+  return __shfl_sync(kFull, a[0], (lane << (5 - lg)) & 31);
+}
+
 // Children of the nodes the last GEMM expanded for request b: the columns
 // c = g, g + G, ... of the request (member g of its group of G blocks), one
 // warp per node. A warp forms h = SiLU(U_j + p) (p summed over the K-chunk
@@ -923,12 +951,7 @@ __device__ void score_cols(const ChainParams &p, const Tables *t, int b, int g, 
             }
           }
         }
-        float my_dl = 0.f;
-#pragma unroll
-        for (int q = 0; q < G; ++q) {
-          const float dl = warp_sum(acc[q]);
-          if (q == lane) my_dl = dl;
-        }
+        const float my_dl = warp_sum_many<G>(acc, lane);   // lane q < G: candidate c0 + q
         if (mine) Lw[my_c] = my_id >= 0 ? __fdiv_rn(my_base + my_dl, T) : ninf;
       }
     }

@@ -428,8 +428,12 @@ __device__ void gru_request(const DecodeParams &p, int b, int tok) {
   }
 }
 
-// Token of position i for request b (one block), then its GRU step.
-__device__ void choose_token(const DecodeParams &p, int i, int b) {
+// Token of position i for request b (one block), then its GRU step. The
+// request's group records are first copied into `stage` (the W2 ring, idle in
+// this phase) by coalesced loads when they fit, so that the passes below, in
+// which every thread walks its own contiguous range of groups, read shared
+// memory instead of strided global words.
+__device__ void choose_token(const DecodeParams &p, int i, int b, float *stage) {
   __shared__ float s_red[32];
   __shared__ float s_f[4];
   __shared__ int s_i[4];
@@ -441,6 +445,18 @@ __device__ void choose_token(const DecodeParams &p, int i, int b) {
   const bool greedy = (p.temperature ? p.temperature[gb] : 1.0f) == 0.0f;
   const float *m = p.st_m + static_cast<size_t>(b) * p.Gn;
   const float *sg = p.st_s + static_cast<size_t>(b) * p.Gn;
+  const bool staged = 2 * p.Gn <= static_cast<int>(kStages * kChunkBytes / 4);
+  float *sm_m = stage, *sm_s = stage + p.Gn;
+  if (staged) {
+    for (int u = tid; u < p.Gn; u += kDThreads) {
+      sm_m[u] = __ldcg(m + u);
+      sm_s[u] = __ldcg(sg + u);
+    }
+    __syncthreads();
+  }
+  // group record g (the records are rewritten at every position: global reads bypass L1)
+  auto ld_m = [&](int g) { return staged ? sm_m[g] : __ldcg(m + g); };
+  auto ld_s = [&](int g) { return staged ? sm_s[g] : __ldcg(sg + g); };
   const int cpt = (p.Gn + kWork - 1) / kWork;
   const int g0 = work ? min(p.Gn, tid * cpt) : p.Gn, g1 = min(p.Gn, g0 + cpt);
   // 1. maximum, its first group, the last group with mass
@@ -452,8 +468,8 @@ __device__ void choose_token(const DecodeParams &p, int i, int b) {
     float mv[kG], sv[kG];
 #pragma unroll
     for (int j = 0; j < kG; ++j) {
-      mv[j] = gb0 + j < g1 ? __ldcg(m + gb0 + j) : ninf;
-      sv[j] = gb0 + j < g1 ? __ldcg(sg + gb0 + j) : 0.0f;
+      mv[j] = gb0 + j < g1 ? ld_m(gb0 + j) : ninf;
+      sv[j] = gb0 + j < g1 ? ld_s(gb0 + j) : 0.0f;
     }
 #pragma unroll
     for (int j = 0; j < kG; ++j) {
@@ -492,8 +508,8 @@ __device__ void choose_token(const DecodeParams &p, int i, int b) {
       float mv[kG], sv[kG];
 #pragma unroll
       for (int j = 0; j < kG; ++j) {
-        mv[j] = gb0 + j < g1 ? __ldcg(m + gb0 + j) : ninf;
-        sv[j] = gb0 + j < g1 ? __ldcg(sg + gb0 + j) : 0.0f;
+        mv[j] = gb0 + j < g1 ? ld_m(gb0 + j) : ninf;
+        sv[j] = gb0 + j < g1 ? ld_s(gb0 + j) : 0.0f;
       }
 #pragma unroll
       for (int j = 0; j < kG; ++j)
@@ -540,8 +556,8 @@ __device__ void choose_token(const DecodeParams &p, int i, int b) {
         float mv[kG], sv[kG];
 #pragma unroll
         for (int j = 0; j < kG; ++j) {
-          mv[j] = gb0 + j < g1 ? __ldcg(m + gb0 + j) : ninf;
-          sv[j] = gb0 + j < g1 ? __ldcg(sg + gb0 + j) : 0.0f;
+          mv[j] = gb0 + j < g1 ? ld_m(gb0 + j) : ninf;
+          sv[j] = gb0 + j < g1 ? ld_s(gb0 + j) : 0.0f;
         }
 #pragma unroll
         for (int j = 0; j < kG; ++j) {
@@ -632,6 +648,7 @@ __device__ void choose_token(const DecodeParams &p, int i, int b) {
     p.logprobs[static_cast<size_t>(gb) * p.D + i] = lp;
   }
   if (i + 1 < p.D && !bad && work) gru_request(p, b, tok);
+  if (staged) fence_async_smem();   // the ring's generic writes -> its next bulk copies
   __syncthreads();
 }
 
@@ -720,7 +737,8 @@ __global__ void __launch_bounds__(kDThreads, 1) decode_kernel(DecodeParams p) {
     lap(1);
     ok = barrier(!g || s_fail);
     if (!ok) break;
-    for (int b = blockIdx.x; b < p.nb; b += gridDim.x) choose_token(p, i, b);
+    for (int b = blockIdx.x; b < p.nb; b += gridDim.x)
+      choose_token(p, i, b, reinterpret_cast<float *>(ring));
     lap(2);
     if (i + 1 < p.D) ok = barrier(false);
   }

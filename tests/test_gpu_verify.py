@@ -77,7 +77,7 @@ def test_positions_bit_exact(N, batch):
 
 CASES = {
     "dh64-ragged-prefix": dict(N=12, batch=3, H=4, Hkv=2, P=5, dh=64),
-    "dh128-two-passes": dict(N=100, batch=2, H=4, Hkv=1, P=30, dh=128),
+    "dh128-two-row-tiles": dict(N=100, batch=2, H=4, Hkv=1, P=30, dh=128),
     "dh128-n65": dict(N=64, batch=2, H=8, Hkv=2, P=100, dh=128),
     "dh256": dict(N=20, batch=2, H=2, Hkv=1, P=40, dh=256),
     "no-prefix": dict(N=30, batch=2, H=2, Hkv=2, P=0, dh=64),
